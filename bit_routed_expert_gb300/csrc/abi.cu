@@ -1,0 +1,148 @@
+// extern "C" entry points of libbre: host-side argument checks, then the launchers.
+#include <cuda_runtime.h>
+
+#include "bre.h"
+#include "kernels.h"
+
+namespace bre {
+
+namespace {
+struct DevAttr {
+  int sms = 0;
+  int smem_optin = 0;
+};
+DevAttr g_attr[64];
+
+const DevAttr& attr() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  DevAttr& a = g_attr[dev & 63];
+  if (a.sms == 0) {
+    cudaDeviceGetAttribute(&a.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&a.sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return a;
+}
+}  // namespace
+
+int device_sm_count() { return attr().sms; }
+int device_max_smem_optin() { return attr().smem_optin; }
+
+}  // namespace bre
+
+using namespace bre;
+
+static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static inline bre_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BRE_OK : BRE_ERR_CUDA; }
+
+extern "C" {
+
+const char* bre_status_string(bre_status s) {
+  switch (s) {
+    case BRE_OK: return "ok";
+    case BRE_ERR_ARG: return "invalid argument";
+    case BRE_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case BRE_ERR_CUDA: return "CUDA error";
+    case BRE_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+size_t moe_route_workspace(int T, int E) { return (T > 0 && E > 0) ? route_ws_bytes(T, E) : 0; }
+
+bre_status moe_route(const void* x_bf16, const float* w_r, const float* bias, int T, int d, int E, int k,
+                     int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, bre_stream_t stream) {
+  if (!x_bf16 || !w_r || !topk_ids || !topk_w || T <= 0 || d <= 0 || E <= 0 || k <= 0) return BRE_ERR_ARG;
+  if (k > E || k > 32 || E > 1024 || d % 32 != 0) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(w_r, 16)) return BRE_ERR_ARG;
+  if (!ws || ws_bytes < route_ws_bytes(T, E) || !aligned(ws, 256)) return BRE_ERR_WORKSPACE;
+  return cuda_status(launch_route(static_cast<const uint16_t*>(x_bf16), w_r, bias, T, d, E, k, topk_ids, topk_w, ws,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       int32_t* active, int32_t* n_active, int32_t* dev_err, bre_stream_t stream) {
+  if (!topk_ids || !offsets || !perm || !inv || !active || !n_active || T <= 0 || k <= 0 || E <= 0)
+    return BRE_ERR_ARG;
+  if (E > 1024) return BRE_ERR_UNSUPPORTED;
+  return cuda_status(
+      launch_permute(topk_ids, T, k, E, offsets, perm, inv, active, n_active, dev_err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_expert_ffn_workspace(int T, int k, int E, int d, int d_ff, int d_ff_shared) {
+  if (T <= 0 || k <= 0 || d <= 0 || d_ff <= 0 || d_ff_shared < 0) return 0;
+  return ffn_ws_bytes(T, k, E, d, d_ff, d_ff_shared);
+}
+
+static bool weights_ok(const bre_ffn_weights* w, int fmt) {
+  if (!w->gate || !w->up || !w->down || w->fmt != fmt || w->n_experts <= 0) return false;
+  if (!aligned(w->gate, 16) || !aligned(w->up, 16) || !aligned(w->down, 16)) return false;
+  if (w->n_experts > 1 && (w->expert_stride_gate % 16 || w->expert_stride_up % 16 || w->expert_stride_down % 16))
+    return false;
+  return true;
+}
+
+bre_status moe_expert_ffn(const bre_ffn_weights* routed, const bre_ffn_weights* shared, const void* x_bf16, int T,
+                          int k, const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                          const int32_t* n_active, float* y_pairs, float* y_shared, void* ws, size_t ws_bytes,
+                          int32_t* dev_err, bre_stream_t stream) {
+  if (!routed || !x_bf16 || !offsets || !perm || !active || !n_active || !y_pairs || T <= 0 || k <= 0)
+    return BRE_ERR_ARG;
+  if (!weights_ok(routed, BRE_FMT_Q2_K)) return BRE_ERR_ARG;
+  if (shared && (!weights_ok(shared, BRE_FMT_Q8_0) || shared->n_experts != 1 || !y_shared)) return BRE_ERR_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(y_pairs, 16) || (y_shared && !aligned(y_shared, 16))) return BRE_ERR_ARG;
+  bre_status st = ffn_check_shapes(routed, shared, T);
+  if (st != BRE_OK) return st;
+  const int Fs = shared ? shared->d_ff : 0;
+  if (!ws || !aligned(ws, 256) || ws_bytes < ffn_ws_bytes(T, k, routed->n_experts, routed->d, routed->d_ff, Fs))
+    return BRE_ERR_WORKSPACE;
+  FfnArgs a{routed, shared, static_cast<const uint16_t*>(x_bf16), T, k, offsets, perm, active, n_active,
+            y_pairs, y_shared, ws, ws_bytes, dev_err};
+  return cuda_status(launch_ffn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t* inv, const int32_t* offsets, int E,
+                       const float* y_shared, int T, int k, int d, void* out_bf16, float* out_f32,
+                       bre_stream_t stream) {
+  if (!y_pairs || !topk_w || !inv || !offsets || !out_bf16 || T <= 0 || k <= 0 || d <= 0 || E <= 0) return BRE_ERR_ARG;
+  if (d % 8 != 0) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(y_pairs, 16) || !aligned(out_bf16, 16) || (y_shared && !aligned(y_shared, 16)) ||
+      (out_f32 && !aligned(out_f32, 16)))
+    return BRE_ERR_ARG;
+  return cuda_status(launch_combine(y_pairs, topk_w, inv, offsets, E, y_shared, T, k, d,
+                                    static_cast<uint16_t*>(out_bf16), out_f32, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status moe_residual_norm(const void* x_bf16, const void* moe_bf16, int T, int d, float scale, float eps,
+                             void* x_out_bf16, void* u_out_bf16, bre_stream_t stream) {
+  if (!x_bf16 || !moe_bf16 || !x_out_bf16 || T <= 0 || d <= 0) return BRE_ERR_ARG;
+  if ((size_t)d * 4 > (size_t)device_max_smem_optin()) return BRE_ERR_UNSUPPORTED;
+  return cuda_status(launch_residual_norm(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(moe_bf16), T,
+                                          d, scale, eps, static_cast<uint16_t*>(x_out_bf16),
+                                          static_cast<uint16_t*>(u_out_bf16), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status engram_gather_decode(const uint8_t* const* tables, const int64_t* n_rows, int n_tables,
+                                const int64_t* row_ids, int T, int H, void* out_bf16, int32_t* dev_err,
+                                bre_stream_t stream) {
+  if (!tables || !n_rows || !row_ids || !out_bf16 || T <= 0 || H <= 0 || n_tables <= 0) return BRE_ERR_ARG;
+  if (n_tables > 8 || H > 64) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(out_bf16, 16) || !aligned(row_ids, 8)) return BRE_ERR_ARG;
+  EngramTables tabs{};
+  for (int i = 0; i < n_tables; ++i) {
+    if (!tables[i] || n_rows[i] < 0 || !aligned(tables[i], 8)) return BRE_ERR_ARG;
+    tabs.ptr[i] = tables[i];
+    tabs.n_rows[i] = n_rows[i];
+  }
+  return cuda_status(launch_engram(tabs, n_tables, row_ids, T, H, static_cast<uint16_t*>(out_bf16), dev_err,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status bre_dequant(int fmt, const void* blocks, int64_t n_blocks, float* out, bre_stream_t stream) {
+  if (!blocks || !out || n_blocks <= 0) return BRE_ERR_ARG;
+  if (fmt != BRE_FMT_Q2_K && fmt != BRE_FMT_Q8_0) return BRE_ERR_UNSUPPORTED;
+  return cuda_status(launch_dequant(fmt, static_cast<const uint8_t*>(blocks), n_blocks, out,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal launcher declarations of libbre (host side).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bre.h"
+
+namespace bre {
+
+struct EngramTables {
+  const uint8_t* ptr[8];
+  long long n_rows[8];
+};
+
+cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t* ids, int T, int H, uint16_t* out,
+                          int32_t* err, cudaStream_t s);
+
+// router
+size_t route_ws_bytes(int T, int E);
+cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                         int32_t* ids, float* w, void* ws, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
+                           int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s);
+
+// expert FFN
+struct FfnArgs {
+  const bre_ffn_weights* routed;
+  const bre_ffn_weights* shared;
+  const uint16_t* x;
+  int T, k;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* active;
+  const int32_t* n_active;
+  float* y_pairs;
+  float* y_shared;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* err;
+};
+constexpr int DECODE_T_MAX = 8;   // larger batches take the grouped-GEMM path
+size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs);
+size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs);
+bre_status ffn_check_shapes(const bre_ffn_weights* routed, const bre_ffn_weights* shared, int T);
+cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s);
+
+cudaError_t launch_combine(const float* y_pairs, const float* topk_w, const int32_t* inv, const int32_t* offsets,
+                           int E, const float* y_shared, int T, int k, int d, uint16_t* out, float* out_f32,
+                           cudaStream_t s);
+cudaError_t launch_residual_norm(const uint16_t* x, const uint16_t* moe, int T, int d, float scale, float eps,
+                                 uint16_t* x_out, uint16_t* u_out, cudaStream_t s);
+cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t n_blocks, float* out, cudaStream_t s);
+
+// device attributes (cached per device)
+int device_sm_count();
+int device_max_smem_optin();
+
+}  // namespace bre

@@ -1,0 +1,181 @@
+/*
+ * bre.h -- C ABI of libbre: a routed mixture-of-experts FFN layer over
+ * block-quantised expert weights, plus the Engram hashed-row gather-decode,
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, by page title and section:
+ *   [S] Strata-DSV4.1 README -- "DeepSeek-V4.1-Flash" (40 layers x 384 routed
+ *       experts, top-6); "Results" (selection-only route bias, mixing weights
+ *       stay exact; prefill and decode time split); "Latest (2026-10-14)" (a
+ *       verify pass serves the union of the pass's experts once per layer);
+ *       V4-Flash "How it works" (finish = shared expert + routed sum);
+ *       "Verifying it" (expert tier against a dequantised F32 reference).
+ *   [I] strix-llama.cpp issue "Feature Request: support DeepSeek V4.1 Flash
+ *       with bounded SSD expert caching" -- "Feature Description" (264-byte
+ *       Engram rows: 256 E4M3 values + 8 E8M0 scales; Q2_K / Q8_0 formats);
+ *       "DeepSeek V4.1 Engram graph integration" (rows gathered per token);
+ *       "Stack progress" (request-union planning; split routing from expert
+ *       execution); ROCm cached-expert notes (errors surfaced after
+ *       synchronisation with safe in-range indices).
+ *   [V] vllm.cpp PR, DeepSeek-V4-Flash-Vision -- device router notes (top-k
+ *       on the biased score, weights gathered from the unbiased scores; one
+ *       warp per row; refusal by name).
+ *
+ * Conventions (every entry point):
+ *   - All pointers are DEVICE pointers unless marked "host".  The caller owns
+ *     and allocates every buffer, workspaces included; the library allocates
+ *     nothing and keeps no state beyond a per-device attribute cache.
+ *   - Work is enqueued on `stream` and is asynchronous; nothing synchronises.
+ *   - Arguments the host can check (null pointers, sizes, alignment, shapes
+ *     the kernels do not support) return BRE_ERR_ARG / BRE_ERR_UNSUPPORTED
+ *     before any launch.  A failed launch returns BRE_ERR_CUDA.
+ *   - Data-dependent faults never trap: kernels clamp to a safe index, write
+ *     zeros for the affected values and OR a BRE_DEVERR_* bit into the
+ *     caller's int32 `dev_err` word (may be NULL), read after synchronising.
+ *   - BF16 values are passed as raw 16-bit patterns (uint16_t storage).
+ */
+#ifndef BRE_H
+#define BRE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bre_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  BRE_OK = 0,
+  BRE_ERR_ARG = 1,         /* invalid argument (null pointer, bad size or alignment) */
+  BRE_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement */
+  BRE_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+  BRE_ERR_WORKSPACE = 4    /* workspace missing or smaller than the *_workspace() size */
+} bre_status;
+
+/* bits of the device error word */
+#define BRE_DEVERR_EXPERT_ID 1 /* an expert id outside [0, E): pair excluded, its output zero */
+#define BRE_DEVERR_ROW_ID 2    /* an Engram row id outside [0, n_rows): row decoded as +0 */
+#define BRE_DEVERR_TIMEOUT 4   /* a bounded device wait gave up; outputs of that CTA are invalid */
+
+typedef enum { BRE_FMT_Q2_K = 1, BRE_FMT_Q8_0 = 2 } bre_fmt;
+
+/* One FFN weight set.  gate, up: [n_experts][d_ff][d] and down: [n_experts][d][d_ff]
+ * weights, each row stored as consecutive quant blocks along its inner
+ * (contraction) axis.  Q2_K block (84 B / 256 weights): uint8 scales[16]
+ * (low nibble scale, high nibble min), uint8 qs[64] (code i in bits
+ * 2*(i%4) of qs[i/4]), fp16 d, fp16 dmin; w = d*sc*q - dmin*m for weight i
+ * in sub-block i/16.  Q8_0 block (34 B / 32 weights): fp16 d, int8 q[32];
+ * w = d*q.  expert_stride_*: bytes from one expert's matrix to the next
+ * (ignored when n_experts == 1).  Base pointers and strides must be 16-byte
+ * aligned. */
+typedef struct {
+  const void *gate;
+  const void *up;
+  const void *down;
+  int32_t fmt; /* bre_fmt */
+  int32_t n_experts;
+  int32_t d;
+  int32_t d_ff;
+  int64_t expert_stride_gate;
+  int64_t expert_stride_up;
+  int64_t expert_stride_down;
+} bre_ffn_weights;
+
+const char *bre_status_string(bre_status s);
+
+/* Router: score, bias, top-k, renormalised weights ([S] "Results";
+ * [V] router notes).  For each token t and expert e:
+ *   z = x[t,:] . w_r[:,e]  -- FP32, 32 partial sums (partial j takes fmaf over
+ *       rows c = j, j+32, ... in ascending order, from +0), then a butterfly
+ *       p_j += p_(j^o) for o = 16, 8, 4, 2, 1; z = p_0
+ *   s = (float)(1 / (1 + exp(-(double)z)));  key = s + bias[e]  (float)
+ * ids[t,:] = the k experts with the largest key, ordered by key descending
+ * then id ascending (a NaN key ranks last); w[t,j] = s_j / S with
+ * S = (((s_0 + s_1) + s_2) ...) in slot order -- weights use the UNBIASED
+ * scores.
+ *   x_bf16 [T][d] BF16; w_r [d][E] FP32 row-major; bias [E] FP32 or NULL;
+ *   topk_ids [T][k] int32 out; topk_w [T][k] FP32 out.
+ *   ws: moe_route_workspace(T, E) bytes of scratch, zero-filled once after
+ *   allocation (the call leaves it ready for the next call).
+ * Requires 1 <= k <= min(E, 32), E <= 1024, d % 32 == 0. */
+size_t moe_route_workspace(int T, int E);
+bre_status moe_route(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
+                     int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, bre_stream_t stream);
+
+/* Expert permutation: the union of selected experts, each run once per call
+ * ([S] "Latest (2026-10-14)"; [I] "Stack progress", request-union planning).
+ * Stable counting sort of pair ids p = t*k + j by expert id:
+ *   offsets [E+1]: exclusive prefix sum of per-expert pair counts (valid ids only)
+ *   perm [T*k]: perm[offsets[e] + r] = r-th smallest p with ids[p] == e
+ *   inv [T*k]: inv[perm[q]] = q
+ *   active [E]: ascending experts with at least one pair (rest -1); n_active [1].
+ * Pairs with an id outside [0, E) are placed after every group, in p order,
+ * and set BRE_DEVERR_EXPERT_ID. */
+bre_status moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *offsets, int32_t *perm,
+                       int32_t *inv, int32_t *active, int32_t *n_active, int32_t *dev_err,
+                       bre_stream_t stream);
+
+/* Routed expert FFN plus the always-on shared expert ([S] V4-Flash "How it
+ * works", finish step; "Verifying it"): for every active expert e and each of
+ * its pairs p (token t = p / k):
+ *   h = silu(gate_e . x_t) * (up_e . x_t);  y_pairs[inv[p]] = down_e . h
+ * and for the shared expert (weight 1) on every token: y_shared[t].  No
+ * SwiGLU clamp.  Weights are dequantised exactly; accumulation is FP32.
+ *   routed: fmt BRE_FMT_Q2_K, n_experts = E.  shared: fmt BRE_FMT_Q8_0,
+ *   n_experts = 1, or NULL (then y_shared is not written).
+ *   x_bf16 [T][d]; offsets/perm/active/n_active from moe_permute (k pairs per
+ *   token); y_pairs [T*k][d] FP32 out, row q = permuted position q (rows of
+ *   pairs with an invalid id are not written); y_shared [T][d] FP32 out.
+ *   ws: moe_expert_ffn_workspace(...) bytes, zero-filled once after allocation.
+ * Shapes: d and d_ff multiples of 256; each of d, d_ff either <= 2048 or a
+ * multiple of 1024 (Q2_K rows are copied to shared memory with 16-byte
+ * aligned bulk copies). */
+size_t moe_expert_ffn_workspace(int T, int k, int E, int d, int d_ff, int d_ff_shared);
+bre_status moe_expert_ffn(const bre_ffn_weights *routed, const bre_ffn_weights *shared, const void *x_bf16,
+                          int T, int k, const int32_t *offsets, const int32_t *perm, const int32_t *active,
+                          const int32_t *n_active, float *y_pairs, float *y_shared, void *ws, size_t ws_bytes,
+                          int32_t *dev_err, bre_stream_t stream);
+
+/* Weighted combine ([S] "How it works", finish: shared expert + routed sum):
+ *   acc[t] = y_shared[t] + sum_j topk_w[t,j] * y_pairs[inv[t*k+j]],  out[t] = bf16_rne(acc[t])
+ * FP32 accumulation from y_shared (or 0 when NULL), j ascending.  A pair whose
+ * position inv >= offsets[E] (invalid id) contributes nothing.
+ *   out_bf16 [T][d] out; out_f32 [T][d] out (the value before rounding), or NULL. */
+bre_status moe_combine(const float *y_pairs, const float *topk_w, const int32_t *inv, const int32_t *offsets,
+                       int E, const float *y_shared, int T, int k, int d, void *out_bf16, float *out_f32,
+                       bre_stream_t stream);
+
+/* Residual update of a stack of MoE layers with no attention (verify batch of
+ * [S] "Latest (2026-10-14)"):
+ *   x_out = bf16_rne(x + bf16(moe) * scale)   (product and sum each rounded)
+ *   u_out = bf16_rne(x_out * r),  r = 1 / sqrtf(mean(x_out^2) + eps)
+ * where the sum of squares uses the router's 32-partial order.  u_out (the
+ * next layer's MoE input) may be NULL.  x, moe, x_out, u_out: [T][d] BF16. */
+bre_status moe_residual_norm(const void *x_bf16, const void *moe_bf16, int T, int d, float scale, float eps,
+                             void *x_out_bf16, void *u_out_bf16, bre_stream_t stream);
+
+/* Engram gather-decode ([I] "Feature Description"; "DeepSeek V4.1 Engram
+ * graph integration").  Row layout: 256 E4M3 (OCP, bias 7, no inf) bytes, then
+ * 8 E8M0 scale bytes, one per 32 values.  For each token t, table tau, head h:
+ *   v_h[c] = e4m3(row[c]) * 2^(row[256 + c/32] - 127),  row = tables[tau][ids[t,tau,h]]
+ *   out[t, tau*256 + c] = bf16_rne(((v_0 + v_1) + v_2) + ...)   (FP32, h ascending)
+ * NaN results are written as 0x7FC0; -0 is kept.
+ *   tables: HOST array of n_tables device pointers (8-byte aligned);
+ *   n_rows: HOST array [n_tables]; row_ids [T][n_tables][H] int64;
+ *   out_bf16 [T][n_tables*256].  An id outside [0, n_rows) decodes as +0 and
+ *   sets BRE_DEVERR_ROW_ID.  Requires 1 <= n_tables <= 8, 1 <= H <= 64. */
+bre_status engram_gather_decode(const uint8_t *const *tables, const int64_t *n_rows, int n_tables,
+                                const int64_t *row_ids, int T, int H, void *out_bf16, int32_t *dev_err,
+                                bre_stream_t stream);
+
+/* Dequantise n_blocks blocks of format fmt to FP32 on the device, with the
+ * same decode the FFN kernels use (exact: every product is exact in FP32 and
+ * the one rounding is the final subtraction).  out [n_blocks * 256 or * 32]. */
+bre_status bre_dequant(int fmt, const void *blocks, int64_t n_blocks, float *out, bre_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BRE_H */

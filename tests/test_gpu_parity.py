@@ -1,0 +1,353 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle, on the same seeded inputs.
+
+Bar: bit-exact for ids, permutation, dequantised values and Engram BF16 output;
+max|out - ref| <= 1e-2 * rms(ref) for MoE layer outputs (ref in FP64).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_routed_expert_gb300 import api, synth
+from bit_routed_expert_gb300.api import BRE_FMT_Q2_K, BRE_FMT_Q8_0
+from helpers import assert_layer_close, bf16_bits, device_layer, oracle_layer, run_layer
+
+pytestmark = pytest.mark.gpu
+
+SEED = 1
+
+
+def _sync():
+    torch.cuda.synchronize()
+
+
+# --------------------------------------------------------------------------- #
+# generator: identical bytes on CPU and GPU
+# --------------------------------------------------------------------------- #
+
+def test_generator_cpu_gpu_identical(cuda_dev):
+    s = synth.stream(synth.S_GATE, 2)
+    a = synth.q2k_blocks(SEED, s, 1000, 5000, device="cpu")
+    b = synth.q2k_blocks(SEED, s, 1000, 5000, device=cuda_dev).cpu()
+    assert torch.equal(a, b)
+    a = synth.q8_0_blocks(SEED, s, 7, 3000, device="cpu")
+    b = synth.q8_0_blocks(SEED, s, 7, 3000, device=cuda_dev).cpu()
+    assert torch.equal(a, b)
+    r = torch.tensor([0, 5, 4194303, 77777], dtype=torch.int64)
+    assert torch.equal(synth.engram_rows_at(SEED, 16, r), synth.engram_rows_at(SEED, 16, r.to(cuda_dev)).cpu())
+
+
+# --------------------------------------------------------------------------- #
+# formats
+# --------------------------------------------------------------------------- #
+
+def test_dequant_q2k_bit_exact(cuda_dev):
+    blk = synth.q2k_blocks(SEED, 99, 0, 20000)
+    rng = np.random.default_rng(0)
+    special = rng.integers(0, 256, (65536, 84), dtype=np.uint64).astype(np.uint8)
+    special[:, 80:82] = np.arange(65536, dtype=np.uint16).view(np.uint8).reshape(-1, 2)
+    special[:, 82:84] = np.roll(np.arange(65536, dtype=np.uint16), 999).view(np.uint8).reshape(-1, 2)
+    allb = torch.cat([blk, torch.from_numpy(special)])
+    got = api.bre_dequant(BRE_FMT_Q2_K, allb.to(cuda_dev)).cpu().numpy()
+    ref = oracle.dequant_q2k(allb.numpy())
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_dequant_q80_bit_exact(cuda_dev):
+    blk = synth.q8_0_blocks(SEED, 98, 0, 20000)
+    got = api.bre_dequant(BRE_FMT_Q8_0, blk.to(cuda_dev)).cpu().numpy()
+    ref = oracle.dequant_q8_0(blk.numpy())
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# --------------------------------------------------------------------------- #
+# Engram
+# --------------------------------------------------------------------------- #
+
+def _all_pairs_table():
+    rows = np.zeros((256, 264), dtype=np.uint8)
+    for r in range(32):
+        for rot in range(8):
+            i = r * 8 + rot
+            rows[i, :256] = (np.arange(256) + 32 * rot) % 256
+            rows[i, 256:] = np.arange(8 * r, 8 * r + 8)
+    return rows
+
+
+def test_engram_exhaustive_codes_and_scales(cuda_dev):
+    tab = _all_pairs_table()
+    ids = np.arange(256, dtype=np.int64).reshape(256, 1, 1)
+    ref, err = oracle.engram_gather([tab], ids)
+    got = api.engram_gather_decode([torch.from_numpy(tab).to(cuda_dev)], torch.from_numpy(ids).to(cuda_dev))
+    assert np.array_equal(bf16_bits(got), ref)
+
+
+def test_engram_tiny_config(cuda_dev):
+    tab = synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE), 1024)
+    ids = synth.engram_ids_uniform(SEED, 64, 1024).view(64, 1, 1)
+    ref, err = oracle.engram_gather([tab.numpy()], ids.numpy())
+    dev_err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    got = api.engram_gather_decode([tab.to(cuda_dev)], ids.to(cuda_dev), dev_err=dev_err)
+    assert np.array_equal(bf16_bits(got), ref) and err == 0 and int(dev_err) == 0
+
+
+def test_engram_heads_and_bad_ids(cuda_dev):
+    rng = np.random.default_rng(3)
+    tabs = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), 500 + 37 * tau) for tau in range(3)]
+    for tb in tabs:
+        tb[:, 256:] = torch.from_numpy(rng.integers(100, 160, (tb.shape[0], 8)).astype(np.uint8))
+    for H in (1, 3, 8, 13):
+        ids = np.stack([rng.integers(0, tb.shape[0], (37, H)) for tb in tabs], axis=1).astype(np.int64)
+        ids[3, 0, 0] = -1                       # invalid ids: negative, = n_rows, far beyond
+        ids[10, 1, H - 1] = tabs[1].shape[0]
+        ids[36, 2, H // 2] = 1 << 40
+        ref, err = oracle.engram_gather([t.numpy() for t in tabs], ids)
+        dev_err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+        got = api.engram_gather_decode([t.to(cuda_dev) for t in tabs], torch.from_numpy(ids).to(cuda_dev),
+                                       dev_err=dev_err)
+        assert np.array_equal(bf16_bits(got), ref)
+        assert int(dev_err) == err == 2
+
+
+def test_engram_full_size_sampled(cuda_dev):
+    n_rows, T, H = 4194304, 8192, 8
+    tabs = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), n_rows, device=cuda_dev)
+            for tau in range(2)]
+    ids = synth.engram_ids_ngram(SEED, T, 2, H, n_rows)
+    got = api.engram_gather_decode(tabs, torch.from_numpy(ids).to(cuda_dev))
+    sample = np.unique(np.concatenate([np.arange(8), np.random.default_rng(1).integers(0, T, 500), [T - 1]]))
+    sub = ids[sample]
+    # oracle on the rows those ids name, regenerated on the CPU
+    small_tabs, remap = [], np.empty_like(sub)
+    for tau in range(2):
+        u, inv = np.unique(sub[:, tau, :], return_inverse=True)
+        small_tabs.append(synth.engram_rows_at(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau),
+                                               torch.from_numpy(u)).numpy())
+        remap[:, tau, :] = inv.reshape(sub.shape[0], H)
+    ref, err = oracle.engram_gather(small_tabs, remap)
+    assert np.array_equal(bf16_bits(got)[sample], ref)
+
+
+# --------------------------------------------------------------------------- #
+# router and permutation
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("shape,T", [(synth.TINY, 4), (synth.V41, 1), (synth.V41, 2), (synth.V41, 4), (synth.V41, 8),
+                                     (synth.V41, 5), (synth.TINY, 33), (synth.TINY, 300)])
+def test_route_bit_exact(cuda_dev, shape, T):
+    for tset in range(2):
+        x = synth.x_bf16(SEED, 0, tset, T, shape.d)
+        w_r = synth.router_weight(SEED, 0, shape.d, shape.E)
+        b = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width)
+        ids_ref, w_ref = oracle.route(x, w_r, b, shape.k)
+        ids, w = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), shape.k)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+
+
+def test_route_prefill_zipf_sampled(cuda_dev):
+    shape, T = synth.V41_PREFILL, 8192
+    x = synth.x_bf16(SEED, 0, 0, T, shape.d)
+    w_r = synth.router_weight(SEED, 0, shape.d, shape.E)
+    b = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width, shape.zipf)
+    ids, w = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), shape.k)
+    sample = np.concatenate([np.arange(0, T, 17), [T - 1]])
+    ids_ref, w_ref = oracle.route(x[sample], w_r, b, shape.k)
+    assert np.array_equal(ids.cpu().numpy()[sample], ids_ref)
+    assert np.array_equal(w.cpu().numpy()[sample].view(np.uint32), w_ref.view(np.uint32))
+
+
+def test_route_ties_and_zero_bias(cuda_dev):
+    d, E, k = 64, 16, 6
+    x = synth.x_bf16(2, 0, 0, 3, d)
+    w_r = torch.zeros((d, E))
+    b = torch.zeros(E)
+    b[9] = 0.25
+    b[12] = 0.25
+    for bias in (None, b):
+        ids_ref, w_ref = oracle.route(x, w_r, bias, k)
+        ids, w = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), None if bias is None else bias.to(cuda_dev), k)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(w.cpu().numpy(), w_ref)
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 6, 384), (8, 6, 384), (5, 6, 384), (4, 6, 32), (8192, 6, 384), (3000, 8, 1024),
+                                   (7, 1, 1)])
+def test_permute_bit_exact(cuda_dev, T, k, E):
+    rng = np.random.default_rng(T * 31 + E)
+    if T == 8192:   # the skewed prefill routing: a few experts take most pairs
+        p = np.exp(-np.arange(E) / 3.0)
+        p /= p.sum()
+        ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    else:
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ref = oracle.permute(ids, E)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    got = api.moe_permute(torch.from_numpy(ids).to(cuda_dev), E, dev_err=err)
+    for key in ("offsets", "perm", "inv"):
+        assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+    na = int(got["n_active"])
+    assert na == ref["n_active"]
+    assert np.array_equal(got["active"].cpu().numpy()[:na], ref["active"])
+    assert np.all(got["active"].cpu().numpy()[na:] == -1)
+    assert int(err) == 0
+
+
+def test_permute_bad_ids(cuda_dev):
+    ids = np.array([[0, 5], [40, 1], [-3, 5]], dtype=np.int32)
+    ref = oracle.permute(ids, 8)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    got = api.moe_permute(torch.from_numpy(ids).to(cuda_dev), 8, dev_err=err)
+    for key in ("offsets", "perm", "inv"):
+        assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+    assert int(err) & 1
+
+
+# --------------------------------------------------------------------------- #
+# MoE layer
+# --------------------------------------------------------------------------- #
+
+def test_layer_tiny(cuda_dev):
+    shape = synth.TINY
+    layer = device_layer(SEED, 0, shape, 8, cuda_dev)
+    for T in (1, 4, 8):
+        for tset in range(3):
+            x = synth.x_bf16(SEED, 0, tset, T, shape.d)
+            out, of, info = run_layer(layer, x.to(cuda_dev))
+            ref = oracle_layer(SEED, 0, shape, x)
+            assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+            assert_layer_close(out, of, ref)
+            assert int(layer.dev_err) == 0
+
+
+def test_layer_tiny_without_shared_expert(cuda_dev):
+    shape = synth.TINY
+    layer = device_layer(SEED, 0, shape, 8, cuda_dev, with_shared=False)
+    x = synth.x_bf16(SEED, 0, 5, 6, shape.d)
+    out, of, info = run_layer(layer, x.to(cuda_dev))
+    ref = oracle_layer(SEED, 0, shape, x, with_shared=False)
+    assert_layer_close(out, of, ref)
+
+
+def test_layer_one_expert_all_tokens(cuda_dev):
+    # k = E = 1: every token hits the same expert (8 columns of one tile)
+    shape = synth.MoeShape(d=512, E=1, k=1, F=256, F_shared=256, bias_half_width=0.0)
+    layer = device_layer(3, 0, shape, 8, cuda_dev)
+    x = synth.x_bf16(3, 0, 0, 8, shape.d)
+    out, of, _ = run_layer(layer, x.to(cuda_dev))
+    assert_layer_close(out, of, oracle_layer(3, 0, shape, x))
+
+
+def test_layer_decode_full_shape(cuda_dev):
+    shape = synth.V41
+    layer = device_layer(SEED, 0, shape, 8, cuda_dev)
+    for T in (1, 2, 4, 8):
+        x = synth.x_bf16(SEED, 0, 100 + T, T, shape.d)
+        out, of, info = run_layer(layer, x.to(cuda_dev))
+        ref = oracle_layer(SEED, 0, shape, x)
+        assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+        assert_layer_close(out, of, ref)
+        assert int(layer.dev_err) == 0
+
+
+def test_layer_repeatable(cuda_dev):
+    shape = synth.V41
+    layer = device_layer(SEED, 0, shape, 8, cuda_dev)
+    x = synth.x_bf16(SEED, 0, 7, 8, shape.d).to(cuda_dev)
+    a, _ = layer.forward(x)
+    b, _ = layer.forward(x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_residual_norm_bit_exact(cuda_dev):
+    x = (synth.x_bf16(SEED, 0, 0, 5, 4096).float() * 13).to(torch.bfloat16)
+    m = synth.x_bf16(SEED, 0, 1, 5, 4096)
+    s = float(np.float32(1 / math.sqrt(2)))
+    xo, uo = api.moe_residual_norm(x.to(cuda_dev), m.to(cuda_dev), s, 1e-6)
+    xr = oracle.residual(x, m, s)
+    ur = oracle.rmsnorm(torch.from_numpy(xr.view(np.int16)).view(torch.bfloat16), 1e-6)
+    assert np.array_equal(bf16_bits(xo), xr)
+    assert np.array_equal(bf16_bits(uo), ur)
+
+
+# --------------------------------------------------------------------------- #
+# grouped-GEMM path (T > 8)
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("T", [9, 64, 300])
+def test_layer_gemm_tiny_ragged(cuda_dev, T):
+    shape = synth.TINY
+    layer = device_layer(SEED, 0, shape, T, cuda_dev)
+    x = synth.x_bf16(SEED, 0, 50 + T, T, shape.d)
+    out, of, info = run_layer(layer, x.to(cuda_dev))
+    ref = oracle_layer(SEED, 0, shape, x)
+    assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+    assert_layer_close(out, of, ref)
+    assert int(layer.dev_err) == 0
+
+
+def test_layer_gemm_matches_decode_path(cuda_dev):
+    # the same 8 tokens through both paths (a 9th token forces the GEMM path)
+    shape = synth.TINY
+    x9 = synth.x_bf16(SEED, 0, 77, 9, shape.d)
+    layer = device_layer(SEED, 0, shape, 9, cuda_dev)
+    _, f9, _ = run_layer(layer, x9.to(cuda_dev))
+    _, f8, _ = run_layer(layer, x9[:8].contiguous().to(cuda_dev))
+    a = f9[:8].cpu().numpy()
+    b = f8.cpu().numpy()
+    rms = float(np.sqrt(np.mean(b.astype(np.float64) ** 2)))
+    assert np.max(np.abs(a - b)) <= 1e-2 * rms
+
+
+def test_layer_prefill_full_shape_sampled(cuda_dev):
+    shape, T = synth.V41_PREFILL, 8192
+    layer = device_layer(SEED, 0, shape, T, cuda_dev)
+    x = synth.x_bf16(SEED, 0, 0, T, shape.d)
+    out, of, info = run_layer(layer, x.to(cuda_dev))
+    ids = info["ids"].cpu().numpy()
+    # sample: the first and last tokens plus tokens that cover every active expert
+    chosen = {0, T - 1}
+    seen = set()
+    for t in range(T):
+        new = set(ids[t]) - seen
+        if new:
+            chosen.add(t)
+            seen |= new
+        if len(chosen) >= 24:
+            break
+    sample = np.array(sorted(chosen))
+    ref = oracle_layer(SEED, 0, shape, x[sample])
+    assert np.array_equal(ids[sample], ref["ids"])
+    assert_layer_close(out[sample], of[sample], ref)
+    assert int(layer.dev_err) == 0
+
+
+# --------------------------------------------------------------------------- #
+# verify batch through a 24-layer stack (teacher-forced per layer)
+# --------------------------------------------------------------------------- #
+
+def test_verify_stack_24_layers_teacher_forced(cuda_dev):
+    shape, T, L = synth.V41, 5, 24
+    layers = [device_layer(SEED, l, shape, T, cuda_dev) for l in range(L)]
+    stack = api.MoeStack(layers)
+    x0 = synth.x_bf16(SEED, 0, 999, T, shape.d).to(cuda_dev)
+    trace = []
+    xf = stack.forward(x0, trace=trace)
+    torch.cuda.synchronize()
+    assert torch.isfinite(xf.float()).all()
+    for l in (0, 11, 23):
+        x_l, u_l, out_l, f_l, info = trace[l]
+        # the norm of the layer input is bit-exact
+        u_ref = oracle.rmsnorm(x_l.cpu(), 1e-6)
+        assert np.array_equal(bf16_bits(u_l), u_ref)
+        # ids bit-exact and the layer output within tolerance, on the device's own input
+        ref = oracle_layer(SEED, l, shape, u_l.cpu())
+        assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+        assert_layer_close(out_l, f_l, ref)
+        # the residual update is bit-exact given the layer output
+        nxt = trace[l + 1][0] if l + 1 < L else xf
+        assert np.array_equal(bf16_bits(nxt), oracle.residual(x_l.cpu(), out_l.cpu(), stack.scale))

@@ -534,3 +534,24 @@ def test_rmsnorm_and_residual():
     exp_ = (x.float().numpy() + (m.float().numpy() * np.float32(1 / math.sqrt(2))).astype(np.float32)).astype(np.float32)
     ref2 = torch.from_numpy(exp_).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(xn, ref2)
+
+
+def test_verify_stack_literal_recurrence_overflows():
+    """The layer-stack recurrence x <- x + moe(x)/sqrt(2) applied literally (no norm on the
+    MoE input) overflows BF16 within a few layers, because h = silu(g)*u grows like |x|^2;
+    this is why the stack normalises each layer's MoE input (a stated reading)."""
+    sh = synth.TINY
+    x = synth.x_bf16(1, 0, 0, 5, sh.d)
+    s = float(np.float32(1 / math.sqrt(2)))
+    finite_layers = 0
+    for layer in range(6):
+        lw = synth.layer_weights(1, layer, sh)
+        r = oracle.moe_layer(x, lw.w_r, lw.bias, sh.k, sh.F, list(lw.gate.numpy()), list(lw.up.numpy()),
+                             list(lw.down.numpy()), lw.sh_gate.numpy(), lw.sh_up.numpy(), lw.sh_down.numpy(),
+                             sh.F_shared)
+        x = torch.from_numpy(oracle.residual(x, torch.from_numpy(r["out"].view(np.int16)).view(torch.bfloat16), s)
+                             .view(np.int16)).view(torch.bfloat16)
+        if not bool(torch.isfinite(x.float()).all()):
+            break
+        finite_layers += 1
+    assert finite_layers < 6
