@@ -104,6 +104,23 @@ size_t moe_route_workspace(int T, int E);
 bre_status moe_route(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
                      int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, bre_stream_t stream);
 
+/* moe_route without a workspace argument, for callers that cannot allocate device memory
+ * (code running under stream capture in global mode, where cudaMalloc is refused; serving
+ * loops that must not call cudaMalloc because it may synchronise the device; integrations
+ * handed only pre-allocated buffers).  The pages have no counterpart: it is an interface
+ * convenience of this library.  It computes exactly what moe_route computes.
+ *   Scratch: one fixed device array inside the library (256 + 4 * BRE_ROUTE_STATIC_MAX_TE
+ *   bytes), held by every GPU that loads the library until the process exits.  T * E above
+ *   BRE_ROUTE_STATIC_MAX_TE returns BRE_ERR_WORKSPACE.  Allocates nothing.
+ *   The first call on a device looks up the array's device address (and may load the
+ *   library's device code); make that first call before any stream capture.
+ *   Every call shares the array: calls that overlap on the GPU (different streams or host
+ *   threads without ordering) race.  Each call clears the part that must start at zero
+ *   with a memset on `stream`. */
+#define BRE_ROUTE_STATIC_MAX_TE 32768
+bre_status moe_route_static(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
+                            int32_t *topk_ids, float *topk_w, bre_stream_t stream);
+
 /* Expert permutation: the union of selected experts, each run once per call
  * ([S] "Latest (2026-10-14)"; [I] "Stack progress", request-union planning).
  * Stable counting sort of pair ids p = t*k + j by expert id:
