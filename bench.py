@@ -141,13 +141,19 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(ws, v: float) -> float:
+def max_over_ranks(ws, v: float, device="cuda") -> float:
+    """Largest value over all ranks (the job's time is its slowest replica's)."""
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t)
+
+
+def job_throughput(ws: int, units_per_rank: float, steps: int, total_ms_max: float) -> float:
+    """Whole-job units/s: every replica processes units_per_rank per step; time = slowest rank."""
+    return ws * units_per_rank * steps / (total_ms_max * 1e-3)
 
 
 # --------------------------------------------------------------------------- #
@@ -157,8 +163,9 @@ def max_over_ranks(ws, v: float) -> float:
 class DecodeWorkload:
     """MoE layer at the V4.1 decode shape (T tokens) + Engram gather of the same tokens."""
 
-    def __init__(self, dev, T: int, rank: int):
+    def __init__(self, dev, T: int, rank: int, engram: bool = True):
         self.dev, self.T = dev, T
+        self.engram = engram
         self.shape = synth.V41
         sh = self.shape
         lw = synth.layer_weights(SEED, 0, sh, device=dev)
@@ -167,7 +174,7 @@ class DecodeWorkload:
                                                                           sh.F),
                               FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
         self.tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
-                       for tau in range(2)]
+                       for tau in range(2)] if engram else None
         ids_all = synth.engram_ids_ngram(SEED + rank, N_SETS * T, 2, ENGRAM_H, ENGRAM_ROWS)
         self.xs_h = [synth.x_bf16(SEED + 1000 * rank, 0, 200 + s, T, sh.d) for s in range(N_SETS)]
         self.ids_h = [torch.from_numpy(ids_all[s * T:(s + 1) * T].copy()) for s in range(N_SETS)]
@@ -184,19 +191,24 @@ class DecodeWorkload:
         self.eout_pin = torch.empty((T, 512), dtype=torch.bfloat16).pin_memory()
         self.ffn_events = None
 
-    launches_per_step = 6   # route, permute, FFN gate/up, FFN down, combine, Engram
+    @property
+    def launches_per_step(self):
+        # route, permute, FFN prep, FFN gate/up, FFN down, combine (+ Engram)
+        return 7 if self.engram else 6
 
     def step(self, i: int, ffn_events=None):
         s = i % N_SETS
         self.layer.forward(self.xs[s], out=self.out, ffn_events=ffn_events)
-        api.engram_gather_decode(self.tables, self.ids[s], out=self.eout)
+        if self.engram:
+            api.engram_gather_decode(self.tables, self.ids[s], out=self.eout)
 
     def step_e2e(self, i: int):
         s = i % N_SETS
         self.x_dev.copy_(self.xs_pin[s], non_blocking=True)
         self.ids_dev.copy_(self.ids_pin[s], non_blocking=True)
         self.layer.forward(self.x_dev, out=self.out)
-        api.engram_gather_decode(self.tables, self.ids_dev, out=self.eout)
+        if self.engram:
+            api.engram_gather_decode(self.tables, self.ids_dev, out=self.eout)
         self.out_pin.copy_(self.out, non_blocking=True)
         self.eout_pin.copy_(self.eout, non_blocking=True)
 
@@ -207,6 +219,25 @@ class DecodeWorkload:
     @property
     def d2h_bytes(self):
         return self.T * self.shape.d * 2 + self.T * 512 * 2
+
+    def step_breakdown(self, i: int, ev):
+        """The step's calls one by one with an event after each (ev: list of 6 events)."""
+        s = i % N_SETS
+        L = self.layer
+        x = self.xs[s]
+        ev[0].record()
+        ids, w = api.moe_route(x, L.w_r, L.bias, L.k, ws=L.route_ws)
+        ev[1].record()
+        perm = api.moe_permute(ids, L.E, dev_err=L.dev_err)
+        ev[2].record()
+        yp, ys = api.moe_expert_ffn(L.routed, L.shared, x, L.k, perm, ws=L.ffn_ws, dev_err=L.dev_err,
+                                    y_pairs=L.y_pairs[:self.T * L.k], y_shared=L.y_shared[:self.T])
+        ev[3].record()
+        api.moe_combine(yp, w, perm["inv"], perm["offsets"], L.E, ys, L.k, out=self.out)
+        ev[4].record()
+        if self.engram:
+            api.engram_gather_decode(self.tables, self.ids[s], out=self.eout)
+        ev[5].record()
 
     def active_counts(self):
         """Distinct experts per token set (route + permute rerun outside the timed region)."""
@@ -228,7 +259,7 @@ class DecodeWorkload:
         T = self.T
         router = sh.d * sh.E * 4 + sh.E * 4 + T * sh.d * 2
         combine = (T * sh.k + T) * sh.d * 4 + T * sh.d * 2
-        engram = T * 2 * ENGRAM_H * (264 + 8) + T * 512 * 2
+        engram = T * 2 * ENGRAM_H * (264 + 8) + T * 512 * 2 if self.engram else 0
         return router + self.ffn_bytes(n_active) + combine + engram
 
 
@@ -236,44 +267,222 @@ def flush_l2(buf):
     buf.fill_(1)
 
 
+def timed(fn, K, flush, stream, per_call_events=False):
+    """K timed calls of fn(i) with an L2 flush before each; returns per-call ms."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush_l2(flush)
+        ev[i][0].record(stream)
+        fn(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def layer_breakdown(layer, xs, out, n, flush):
+    """Median time of each call of a layer forward (route, permute, expert FFN, combine), in us."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    for i, ev in enumerate(evs):
+        flush_l2(flush)
+        x = xs[i % len(xs)]
+        T = x.shape[0]
+        ev[0].record()
+        ids, w = api.moe_route(x, layer.w_r, layer.bias, layer.k, ws=layer.route_ws)
+        ev[1].record()
+        perm = api.moe_permute(ids, layer.E, dev_err=layer.dev_err)
+        ev[2].record()
+        yp, ys = api.moe_expert_ffn(layer.routed, layer.shared, x, layer.k, perm, ws=layer.ffn_ws,
+                                    dev_err=layer.dev_err, y_pairs=layer.y_pairs[:T * layer.k],
+                                    y_shared=None if layer.y_shared is None else layer.y_shared[:T])
+        ev[3].record()
+        api.moe_combine(yp, w, perm["inv"], perm["offsets"], layer.E, ys, layer.k, out=out)
+        ev[4].record()
+    torch.cuda.synchronize()
+    names = ["route", "permute", "expert_ffn", "combine"]
+    return {nm: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in evs) * 1e3, 2)
+            for q, nm in enumerate(names)}
+
+
+def run_prefill(args, ws, rank, local):
+    """One MoE layer at T = 8192 with Zipf(1.1)-skewed routing (grouped GEMM on tcgen05)."""
+    dev = torch.device("cuda", local)
+    sh, T = synth.V41_PREFILL, 8192
+    lw = synth.layer_weights(SEED, 0, sh, device=dev)
+    layer = MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
+                     FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
+    xs = [synth.x_bf16(SEED + 1000 * rank, 0, s, T, sh.d).to(dev) for s in range(2)]
+    out = torch.empty((T, sh.d), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.warmup):
+        layer.forward(xs[i % 2], out=out)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(ws)
+    clocks.start()
+    ms = timed(lambda i: layer.forward(xs[i % 2], out=out, ffn_events=fev[i]), args.steps, flush, stream)
+    clk = clocks.stop()
+    ffn_ms = [a.elapsed_time(b) for a, b in fev]
+    bd = layer_breakdown(layer, xs, out, min(args.steps, 10), flush)
+    _, info = layer.forward(xs[0], out=out)
+    P = T * sh.k
+    flops = 2 * 3 * sh.d * sh.F * P + 2 * 3 * sh.d * sh.F_shared * T
+    pk = peaks()
+    total = max_over_ranks(ws, sum(ms))
+    tfl = flops / (statistics.median(ffn_ms) * 1e-3) / 1e12
+    return {"metric": "MoE-layer prefill TFLOP/s (T=8192, Zipf-skewed routing), % of BF16 tensor peak",
+            "value": round(flops / (total / args.steps * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "tokens_per_s": round(ws * T * args.steps / (total * 1e-3), 1), "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill MoE layer T=8192, Zipf(1.1) popularity via bias (V4.1 shape)",
+                       "T": T, "pairs": P, "active_experts": int(info["n_active"].item()),
+                       "algorithmic_tflop": round(flops / 1e12, 4), "l2": "flushed before every timed step"},
+            "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (grouped GEMM, two launches)",
+                         "achieved": round(tfl, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tfl / pk["bf16_tflops"], 4), "traffic": None, "peak_source": pk["source"]},
+            "ffn_ms_median": round(statistics.median(ffn_ms), 4), "step_ms_median": round(statistics.median(ms), 4),
+            "breakdown_us_median": bd, "clocks": clk}
+
+
+def run_verify(args, ws, rank, local):
+    """Speculative-verify batch: T = 5 rows through 24 MoE layers (76 GB of experts resident)."""
+    dev = torch.device("cuda", local)
+    sh, T, L = synth.V41, 5, 24
+    layers = []
+    for l in range(L):
+        lw = synth.layer_weights(SEED, l, sh, device=dev)
+        layers.append(MoeLayer(lw.w_r.to(dev), lw.bias.to(dev),
+                               FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
+                               FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T))
+    stack = api.MoeStack(layers)
+    xs = [synth.x_bf16(SEED + 1000 * rank, 0, 500 + s, T, sh.d).to(dev) for s in range(N_SETS)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        stack.forward(xs[i % N_SETS])
+    torch.cuda.synchronize()
+    eager_ms = timed(lambda i: stack.forward(xs[i % N_SETS]), min(args.steps, 10), flush, stream)
+    graphs = [api.StepGraph(lambda s=s: stack.forward(xs[s])) for s in range(N_SETS)]
+    for i in range(args.warmup):
+        graphs[i % N_SETS].replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(ws)
+    clocks.start()
+    ms = timed(lambda i: graphs[i % N_SETS].replay(), args.steps, flush, stream)
+    clk = clocks.stop()
+    # expert bytes actually read per pass (distinct experts per layer, rerun outside timing)
+    trace = []
+    stack.forward(xs[0], trace=trace)
+    ub = sum(int(tr[4]["n_active"].item()) for tr in trace)
+    expert_bytes = ub * sh.expert_bytes
+    all_bytes = expert_bytes + L * (sh.shared_bytes + sh.d * sh.E * 4)
+    total = max_over_ranks(ws, sum(ms))
+    med = statistics.median(ms)
+    pk = peaks()
+    return {"metric": "verify-pass latency (T=5, 24 layers) + expert-byte GB/s", "value": round(med * 1e3, 1),
+            "unit": "us/pass", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "verify batch T=5 through 24 MoE layers (V4.1 shape)", "T": T, "layers": L,
+                       "distinct_experts_first_pass": ub, "l2": "flushed before every timed pass",
+                       "launch": "each pass replayed as one captured CUDA graph"},
+            "eager_pass_us_median": round(statistics.median(eager_ms) * 1e3, 1),
+            "expert_gbs": round(expert_bytes / (med * 1e-3) / 1e9, 1),
+            "all_bytes_gbs": round(all_bytes / (med * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "kernel": "whole pass", "achieved": round(all_bytes / (med * 1e-3) / 1e9, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(all_bytes / (med * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": pk["source"]},
+            "gpu_launches_per_pass": 1 + L * 8, "clocks": clk}
+
+
+def run_engram(args, ws, rank, local):
+    """Engram gather-decode at scale: T = 8192 tokens x 2 tables x 8 heads over 4,194,304-row tables."""
+    dev = torch.device("cuda", local)
+    T = 8192
+    tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
+              for tau in range(2)]
+    ids = [torch.from_numpy(synth.engram_ids_ngram(SEED + 17 * s + rank, T, 2, ENGRAM_H, ENGRAM_ROWS)).to(dev)
+           for s in range(4)]
+    out = torch.empty((T, 512), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        api.engram_gather_decode(tables, ids[i % 4], out=out)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(ws)
+    clocks.start()
+    ms = timed(lambda i: api.engram_gather_decode(tables, ids[i % 4], out=out), args.steps, flush, stream)
+    clk = clocks.stop()
+    med = statistics.median(ms)
+    alg = T * 2 * ENGRAM_H * 264 + T * 2 * ENGRAM_H * 8 + T * 512 * 2
+    pk = peaks()
+    total = max_over_ranks(ws, sum(ms))
+    gbs = alg / (med * 1e-3) / 1e9
+    return {"metric": "Engram gather-decode GB/s (T=8192, 2 tables x 8 heads)", "value": round(gbs, 1),
+            "unit": "GB/s", "tokens_per_s": round(ws * T * args.steps / (total * 1e-3), 1), "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "Engram gather-decode, 2 x 4194304 x 264 B tables, T=8192, H=8",
+                       "algorithmic_bytes": alg, "l2": "flushed before every timed call"},
+            "roofline": {"bound": "hbm", "kernel": "engram_gather_kernel", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": pk["source"]},
+            "us_median": round(med * 1e3, 2), "clocks": clk}
+
+
 def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     T = args.T
-    wl = DecodeWorkload(dev, T, rank)
+    wl = DecodeWorkload(dev, T, rank, engram=not args.no_engram)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):
         wl.step(i)
         wl.step_e2e(i)
     torch.cuda.synchronize()
+    # one captured graph per token set: the step, and the step with its host copies
+    graphs = [api.StepGraph(lambda s=s: wl.step(s)) for s in range(N_SETS)]
+    graphs_e2e = [api.StepGraph(lambda s=s: wl.step_e2e(s)) for s in range(N_SETS)]
+    for i in range(args.warmup):
+        graphs[i % N_SETS].replay()
+        graphs_e2e[i % N_SETS].replay()
+    torch.cuda.synchronize()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local)
     barrier(ws)
     torch.cuda.synchronize()
     clocks.start()
     t_wall = time.perf_counter()
-    for i in range(K):
-        flush_l2(flush)
-        ev[i][0].record(stream)
-        wl.step(i, ffn_events=fev[i])
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(lambda i: graphs[i % N_SETS].replay(), K, flush, stream)
     wall = time.perf_counter() - t_wall
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ffn_ms = [a.elapsed_time(b) for a, b in fev]
-    # end to end through the public API with host buffers (copies inside the timed region)
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for i in range(K):
-        flush_l2(flush)
-        eev[i][0].record(stream)
-        wl.step_e2e(i)
-        eev[i][1].record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = timed(lambda i: graphs_e2e[i % N_SETS].replay(), K, flush, stream)
     clk = clocks.stop()
     barrier(ws)
-    e2e_ms = [a.elapsed_time(b) for a, b in eev]
+    # the expert FFN alone (its own flush-separated loop) for the roofline line
+    L = wl.layer
+    perms = []
+    for s in range(N_SETS):
+        ids, w = api.moe_route(wl.xs[s], L.w_r, L.bias, L.k, ws=L.route_ws)
+        perms.append(api.moe_permute(ids, L.E))
+    torch.cuda.synchronize()
+    ffn_ms = timed(lambda i: api.moe_expert_ffn(L.routed, L.shared, wl.xs[i % N_SETS], L.k, perms[i % N_SETS],
+                                                ws=L.ffn_ws, dev_err=L.dev_err, y_pairs=L.y_pairs[:T * L.k],
+                                                y_shared=L.y_shared[:T]), K, flush, stream)
+    eager_ms = timed(lambda i: wl.step(i), min(K, 50), flush, stream)
+    # per-call breakdown (eager, separate pass)
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(min(K, 50))]
+    for i, evs in enumerate(bev):
+        flush_l2(flush)
+        wl.step_breakdown(i, evs)
+    torch.cuda.synchronize()
+    names = ["route", "permute", "expert_ffn", "combine", "engram"]
+    breakdown = {n: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in bev) * 1e3, 2)
+                 for q, n in enumerate(names)}
 
     total_ms = max_over_ranks(ws, sum(step_ms))
     total_e2e = max_over_ranks(ws, sum(e2e_ms))
@@ -283,7 +492,7 @@ def run_ours(args, ws, rank, local):
     step_bytes = [wl.step_bytes(n) for n in nact]
     pk = peaks()
     achieved = sum(ffn_bytes) / (sum(ffn_ms) * 1e-3) / 1e9
-    value = ws * T * K / (total_ms * 1e-3)
+    value = job_throughput(ws, T, K, total_ms)
     res = {
         "metric": "MoE-layer tokens/s (decode, V4.1 shape, T=8) + expert HBM GB/s, % roofline",
         "value": round(value, 1),
@@ -297,22 +506,26 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "decode MoE layer T=8 + Engram gather (V4.1 shape)", "T": T, "d": 4096, "E": 384,
+        "config": {"workload": "decode MoE layer T=8" + ("" if args.no_engram else " + Engram gather") +
+                   " (V4.1 shape)", "T": T, "d": 4096, "E": 384,
                    "k": 6, "d_ff": 2048, "shared_d_ff": 2048, "route_bias": "U(-0.5,0.5)",
                    "expert_format": "Q2_K (84 B / 256)", "shared_format": "Q8_0 (34 B / 32)",
                    "engram": "2 tables x 4194304 rows x 264 B, 8 heads/table", "token_sets": N_SETS,
+                   "launch": "each step replayed as one captured CUDA graph",
                    "l2": "flushed by a 256 MiB write before every timed step", "parallelism": f"replicas{ws}"},
-        "e2e": {"value": round(ws * T * K / (total_e2e * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(ws, T, K, total_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": K * wl.launches_per_step,
-        "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (gate/up + down launches)",
+        "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (prep + gate/up + down launches)",
                      "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
                      "peak_source": pk["source"], "bytes_per_launch_avg": int(np.mean(ffn_bytes))},
         "step_hbm_gbs": round(sum(step_bytes) / (sum(step_ms) * 1e-3) / 1e9, 1),
         "ffn_us_median": round(statistics.median(ffn_ms) * 1e3, 2),
         "step_us_median": round(statistics.median(step_ms) * 1e3, 2),
+        "eager_step_us_median": round(statistics.median(eager_ms) * 1e3, 2),
         "active_experts_per_set": counts,
+        "breakdown_us_median_eager": breakdown,
         "clocks": clk,
         "wall_s_timed_loop": round(wall, 3),
     }
@@ -401,7 +614,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--T", type=int, default=8)
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "verify", "engram"],
+                    help="decode (default, the headline line) or one of the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-engram", action="store_true",
+                    help="leave the Engram gather out of the step (smaller device footprint, for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -412,6 +629,11 @@ def main():
             print(json.dumps(res), flush=True)
         return
     ws, rank, local = dist_setup()
+    if args.workload != "decode":
+        res = {"prefill": run_prefill, "verify": run_verify, "engram": run_engram}[args.workload](args, ws, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     res = run_ours(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:

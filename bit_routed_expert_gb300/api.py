@@ -48,29 +48,33 @@ def moe_route_workspace(T: int, E: int) -> int:
     return _lib.load().moe_route_workspace(T, E)
 
 
-def moe_route(x, w_r, bias, k: int, ws=None, stream=None):
+def moe_route(x, w_r, bias, k: int, ws=None, stream=None, ids=None, w=None):
     L = _lib.load()
     T, d = x.shape
     E = w_r.shape[1]
     _dev(x, "x"), _dev(w_r, "w_r")
     if ws is None:
         ws = torch.zeros(L.moe_route_workspace(T, E), dtype=torch.uint8, device=x.device)
-    ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
-    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=x.device)
     check(L.moe_route(ptr(x), ptr(w_r), ptr(bias), T, d, E, k, ptr(ids), ptr(w), ptr(ws), ws.numel(),
                       stream_handle(stream)), "moe_route")
     return ids, w
 
 
-def moe_permute(ids, E: int, dev_err=None, stream=None):
+def moe_permute(ids, E: int, dev_err=None, stream=None, out=None):
+    """out: optional dict of preallocated offsets [E+1], perm/inv [T*k], active [E], n_active [1]."""
     L = _lib.load()
     T, k = ids.shape
     dv = ids.device
-    out = dict(offsets=torch.empty(E + 1, dtype=torch.int32, device=dv),
-               perm=torch.empty(T * k, dtype=torch.int32, device=dv),
-               inv=torch.empty(T * k, dtype=torch.int32, device=dv),
-               active=torch.empty(E, dtype=torch.int32, device=dv),
-               n_active=torch.empty(1, dtype=torch.int32, device=dv))
+    if out is None:
+        out = dict(offsets=torch.empty(E + 1, dtype=torch.int32, device=dv),
+                   perm=torch.empty(T * k, dtype=torch.int32, device=dv),
+                   inv=torch.empty(T * k, dtype=torch.int32, device=dv),
+                   active=torch.empty(E, dtype=torch.int32, device=dv),
+                   n_active=torch.empty(1, dtype=torch.int32, device=dv))
     check(L.moe_permute(ptr(_dev(ids, "ids")), T, k, E, ptr(out["offsets"]), ptr(out["perm"]), ptr(out["inv"]),
                         ptr(out["active"]), ptr(out["n_active"]), ptr(dev_err), stream_handle(stream)), "moe_permute")
     return out
@@ -163,13 +167,25 @@ class MoeLayer:
         self.y_pairs = torch.zeros((T_max * k, self.d), dtype=torch.float32, device=dv)
         self.y_shared = torch.zeros((T_max, self.d), dtype=torch.float32, device=dv) if shared is not None else None
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dv)
+        # per-call outputs, preallocated so that a forward can be captured in a CUDA graph
+        self.ids = torch.empty((T_max, k), dtype=torch.int32, device=dv)
+        self.w = torch.empty((T_max, k), dtype=torch.float32, device=dv)
+        self.perm_buf = dict(offsets=torch.empty(self.E + 1, dtype=torch.int32, device=dv),
+                             perm=torch.empty(T_max * k, dtype=torch.int32, device=dv),
+                             inv=torch.empty(T_max * k, dtype=torch.int32, device=dv),
+                             active=torch.empty(self.E, dtype=torch.int32, device=dv),
+                             n_active=torch.empty(1, dtype=torch.int32, device=dv))
 
     def forward(self, x, out=None, stream=None, ffn_events=None, out_f32=None):
         """ffn_events: optional (start, end) CUDA events recorded around the expert FFN call;
         out_f32: optional [T, d] FP32 tensor for the layer output before BF16 rounding."""
         T = x.shape[0]
-        ids, w = moe_route(x, self.w_r, self.bias, self.k, ws=self.route_ws, stream=stream)
-        perm = moe_permute(ids, self.E, dev_err=self.dev_err, stream=stream)
+        ids, w = moe_route(x, self.w_r, self.bias, self.k, ws=self.route_ws, stream=stream,
+                           ids=self.ids[:T], w=self.w[:T])
+        pb = self.perm_buf
+        perm = moe_permute(ids, self.E, dev_err=self.dev_err, stream=stream,
+                           out=dict(offsets=pb["offsets"], perm=pb["perm"][:T * self.k], inv=pb["inv"][:T * self.k],
+                                    active=pb["active"], n_active=pb["n_active"]))
         s = stream if stream is not None else torch.cuda.current_stream()
         if ffn_events is not None:
             ffn_events[0].record(s)
@@ -211,3 +227,26 @@ class MoeStack:
                 trace.append((x, u, out.clone(), out_f32, info))
             x, u = moe_residual_norm(x, out, self.scale, self.eps, stream=stream)
         return x
+
+
+class StepGraph:
+    """A sequence of library calls captured once as a CUDA graph and replayed.
+
+    `fn` issues the calls on the current stream (every call above does); buffers it
+    touches must stay allocated while the graph is used.  Decode-size steps are a few
+    tens of microseconds of GPU work, so launching them one by one from the host would
+    dominate; a replay launches the whole step at once."""
+
+    def __init__(self, fn, warmup: int = 2):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+
+    def replay(self):
+        self.graph.replay()

@@ -37,6 +37,7 @@ constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
+constexpr int BAR_BYTES = 256;                  // mbarrier region: MAX_WARPS * NS ring barriers + package
 
 struct DecParams {
   const uint8_t* rw0;  // routed: phase 1 gate, phase 2 down
@@ -65,6 +66,7 @@ struct DecParams {
   int* counters;
   int32_t* err;
   int xstride;  // bytes per token row of the permuted activations in shared memory
+  const unsigned char* pkg;  // activation package in global memory (phase 1)
 };
 
 struct Item {
@@ -152,6 +154,35 @@ __device__ __forceinline__ void q2k_frag(uint32_t qw, uint32_t sc, int s, uint32
   hi = prmt(v, C43, SEL_HI);
 }
 
+// Q2_K A fragments of one row for step s, codes left in place: one LOP3 per register gives the
+// BF16 pair 128 + c * 4^e (e = min(s, 2); the code occupies mantissa bits 2e, 2e+1).  lo holds
+// codes (s, 8+s) of the sub-block word (bytes 0 and 2), hi codes (4+s, 12+s) (bytes 1 and 3).
+__device__ __forceinline__ void q2k_pairs(uint32_t w, int s, uint32_t& lo, uint32_t& hi) {
+  constexpr uint32_t M43 = 0x43004300u;
+  if (s < 3) {
+    const uint32_t m = 0x00030003u << (2 * s);
+    lo = (w & m) | M43;
+    hi = ((w >> 8) & m) | M43;
+  } else {
+    const uint32_t m = 0x00030003u << 4;
+    lo = ((w >> 2) & m) | M43;
+    hi = ((w >> 10) & m) | M43;
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// (sc, sc) and (-128 sc, -128 sc) as BF16 pairs for sub-block byte jj of a scales word (exact).
+__device__ __forceinline__ void q2k_scale_pairs(uint32_t sclo, int jj, uint32_t& sc2, uint32_t& nsc2) {
+  const uint32_t u = prmt(sclo, C43, (uint32_t)(jj | (4 << 4) | (jj << 8) | (4 << 12)));   // 128 + sc
+  sc2 = bf16x2_fma(u, 0x3F803F80u, 0xC300C300u);                                          // u - 128
+  nsc2 = bf16x2_fma(u, 0xC300C300u, 0x46804680u);                                         // 16384 - 128 u
+}
+
 // Q8_0 nibble planes of one row word (4 consecutive int8): (128+lo) and (128+hi') pairs.
 __device__ __forceinline__ void q80_frag(uint32_t w, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
                                          uint32_t& hi23) {
@@ -186,22 +217,24 @@ __device__ __forceinline__ void p1_q2k_chunk(const unsigned char* stage, int cb,
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) qw[m][rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
       }
-    float P[2][4], M[2][4];
+    // one accumulator per (matrix, jj): four independent MMA chains per matrix
+    float P[2][4][4], M[2][4];
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        P[m][i] = 0.0f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) P[m][jj][i] = 0.0f;
         M[m][i] = 0.0f;
       }
     const unsigned char* xblk = xb_g ? xb_g + b * 512 : nullptr;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      uint32_t sc[2][2];
+      uint32_t sc2[2][2], nsc2[2][2];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) sc[m][rr] = (sw[m][rr] >> (8 * jj)) & 15u;
+        for (int rr = 0; rr < 2; ++rr) q2k_scale_pairs(sw[m][rr] & 0x0F0F0F0Fu, jj, sc2[m][rr], nsc2[m][rr]);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         uint2 bv = make_uint2(0u, 0u);
@@ -209,9 +242,13 @@ __device__ __forceinline__ void p1_q2k_chunk(const unsigned char* stage, int cb,
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           uint32_t a0, a1, a2, a3;
-          q2k_frag(qw[m][0][jj], sc[m][0], s, a0, a2);
-          q2k_frag(qw[m][1][jj], sc[m][1], s, a1, a3);
-          mma_bf16_16816(P[m], a0, a1, a2, a3, bv.x, bv.y);
+          q2k_pairs(qw[m][0][jj], s, a0, a2);
+          q2k_pairs(qw[m][1][jj], s, a1, a3);
+          a0 = bf16x2_fma(a0, sc2[m][0], nsc2[m][0]);
+          a2 = bf16x2_fma(a2, sc2[m][0], nsc2[m][0]);
+          a1 = bf16x2_fma(a1, sc2[m][1], nsc2[m][1]);
+          a3 = bf16x2_fma(a3, sc2[m][1], nsc2[m][1]);
+          mma_bf16_16816(P[m][jj], a0, a1, a2, a3, bv.x, bv.y);
         }
       }
     }
@@ -236,9 +273,9 @@ __device__ __forceinline__ void p1_q2k_chunk(const unsigned char* stage, int cb,
         const uint32_t ddv = dd[m][i >> 1];
         const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
         const float xs = (i & 1) ? x1 : x0;
-        const float pv = fmaf(-128.0f, xs, P[m][i]);
+        const float psum = (P[m][0][i] + P[m][1][i]) + (P[m][2][i] + P[m][3][i]);
         const float mv = fmaf(-128.0f, xs, M[m][i]);
-        acc[m][i] = fmaf(dv, pv, fmaf(-dmv, mv, acc[m][i]));
+        acc[m][i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[m][i]));
       }
   }
 }
@@ -310,20 +347,33 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
     }
-    float P[4] = {0.f, 0.f, 0.f, 0.f}, M[4] = {0.f, 0.f, 0.f, 0.f};
+    float P[4][4], M[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) P[jj][i] = 0.0f;
     const uint16_t* hblk = (pos_g >= 0) ? hB + ((long long)pos_g * nb + b) * 512 : nullptr;
+    uint4 bvs[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      bvs[q] = hblk ? __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t sc0 = (sw[0] >> (8 * jj)) & 15u, sc1 = (sw[1] >> (8 * jj)) & 15u;
+      uint32_t sc2[2], nsc2[2];
+      q2k_scale_pairs(sw[0] & 0x0F0F0F0Fu, jj, sc2[0], nsc2[0]);
+      q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, jj, sc2[1], nsc2[1]);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-        if (hblk) bv = __ldg(reinterpret_cast<const uint4*>(hblk + ((jj * 4 + s) * 4 + t) * 8));
+        const uint4 bv = bvs[jj * 4 + s];
         uint32_t a0, a1, a2, a3;
-        q2k_frag(qw[0][jj], sc0, s, a0, a2);
-        q2k_frag(qw[1][jj], sc1, s, a1, a3);
-        mma_bf16_16816(P, a0, a1, a2, a3, bv.x, bv.y);
-        mma_bf16_16816(P, a0, a1, a2, a3, bv.z, bv.w);
+        q2k_pairs(qw[0][jj], s, a0, a2);
+        q2k_pairs(qw[1][jj], s, a1, a3);
+        a0 = bf16x2_fma(a0, sc2[0], nsc2[0]);
+        a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
+        a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
+        a3 = bf16x2_fma(a3, sc2[1], nsc2[1]);
+        mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.x, bv.y);
+        mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.z, bv.w);
       }
     }
     float hsum = 0.0f;
@@ -351,9 +401,9 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
       const uint32_t ddv = dd[i >> 1];
       const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
       const float xs = (i & 1) ? x1 : x0;
-      const float pv = fmaf(-128.0f, xs, P[i]);
+      const float psum = (P[0][i] + P[1][i]) + (P[2][i] + P[3][i]);
       const float mv = fmaf(-128.0f, xs, M[i]);
-      acc[i] = fmaf(dv, pv, fmaf(-dmv, mv, acc[i]));
+      acc[i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[i]));
     }
   }
 }
@@ -403,6 +453,77 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb,
 __device__ __forceinline__ float silu_mul(float gv, float uv) { return gv / (1.0f + expf(-gv)) * uv; }
 
 // ----------------------------------------------------------------------------
+// activation package: x permuted into the Q2_K fragment order, the 16-value sub-block
+// sums of x as three BF16 limbs, their block totals, and 32-value sums for Q8_0.  Built
+// once per call by ffn_prep_kernel and copied whole into shared memory by phase 1.
+// ----------------------------------------------------------------------------
+struct PkgLayout {
+  int xB, XBm, XbM, X32, total;
+};
+
+__host__ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
+
+__host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
+  const int nbx = d / 256, xstride = d * 2 + 32;
+  PkgLayout L;
+  L.xB = 0;
+  L.XBm = T * xstride;
+  L.XbM = L.XBm + T * nbx * 96;
+  L.X32 = L.XbM + round16(T * nbx * 4);
+  L.total = L.X32 + round16(T * (d / 32) * 4);
+  return L;
+}
+
+// grid (d/256, T), 256 threads: thread i owns value k = 256*b + i of token t.
+//   xB: x (BF16) permuted into the Q2_K fragment order; XBm: 16-value sub-block sums as
+//   three BF16 limbs; XbM: their block total; X32: 32-value sums (Q8_0 shared expert).
+__global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restrict__ x, int T, int d,
+                                                       unsigned char* __restrict__ pkg) {
+  __shared__ float sub_limbs[16];
+  pdl_wait();
+  const int b = blockIdx.x, t = blockIdx.y, i = threadIdx.x, lane = i & 31;
+  const int nbx = d / 256;
+  const PkgLayout L = pkg_layout(T, d);
+  const uint32_t v = x[(size_t)t * d + 256 * b + i];
+  {
+    // fragment order: step (jj, s) of thread tq holds codes s, 8+s | 4+s, 12+s of sub-block 4tq+jj,
+    // each activation scaled by 4^-min(s,2) to match the code left in place in the A fragment
+    const int j = i >> 4, tq = j >> 2, jj = j & 3, ip = i & 15;
+    const int byte = ip >> 2, s = ip & 3;
+    const int v4 = (byte & 1) * 2 + (byte >> 1);
+    const int rem = ((((b * 4 + jj) * 4 + s) * 4 + tq) * 4 + v4);
+    const float scaled = __fmul_rn(bf16_bits_to_f32(v), s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f));
+    reinterpret_cast<uint16_t*>(pkg + L.xB + (size_t)t * (d * 2 + 32))[rem] = (uint16_t)f32_to_bf16_rne(scaled);
+  }
+  const float f = bf16_bits_to_f32(v);
+  // 16-value sub-block sum (lanes of a half warp), fixed tree order
+  float s16 = f;
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);
+  // 32-value sum
+  float s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 16);
+  if (lane == 0) reinterpret_cast<float*>(pkg + L.X32)[(size_t)t * (d / 32) + b * 8 + (i >> 5)] = s32;
+  if ((i & 15) == 0) {
+    const int j = i >> 4;
+    const uint32_t hi = f32_to_bf16_rne(s16);
+    const float r1 = s16 - bf16_bits_to_f32(hi);
+    const uint32_t mid = f32_to_bf16_rne(r1);
+    const uint32_t lo = f32_to_bf16_rne(r1 - bf16_bits_to_f32(mid));
+    uint16_t* dst = reinterpret_cast<uint16_t*>(pkg + L.XBm + (size_t)t * nbx * 96) + ((b * 4 + (j >> 2)) * 3) * 4 + (j & 3);
+    dst[0] = (uint16_t)hi;
+    dst[4] = (uint16_t)mid;
+    dst[8] = (uint16_t)lo;
+    sub_limbs[j] = (bf16_bits_to_f32(hi) + bf16_bits_to_f32(mid)) + bf16_bits_to_f32(lo);
+  }
+  __syncthreads();
+  if (i == 0) {
+    float sacc = 0.0f;
+    for (int j = 0; j < 16; ++j) sacc += sub_limbs[j];
+    reinterpret_cast<float*>(pkg + L.XbM)[(size_t)t * nbx + b] = sacc;
+  }
+}
+
+// ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
 template <int PHASE>
@@ -413,12 +534,19 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
   const int g = lane >> 2, t = lane & 3;
   unsigned char* stages = sm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + nw * NS * STAGE);
-  unsigned char* xprep = reinterpret_cast<unsigned char*>(bars + MAX_WARPS * NS);
+  uint64_t* pkg_bar = bars + MAX_WARPS * NS;
+  unsigned char* xprep = reinterpret_cast<unsigned char*>(bars) + BAR_BYTES;
 
   pdl_wait();
   if (threadIdx.x < nw * NS) mbar_init(&bars[threadIdx.x], 1);
+  if (threadIdx.x == 0) mbar_init(pkg_bar, 1);
   fence_mbar_init();
   __syncthreads();
+  const PkgLayout PL = pkg_layout(p.T, p.d);
+  if (PHASE == 1 && threadIdx.x == 0) {
+    mbar_arrive_expect_tx(pkg_bar, PL.total);
+    bulk_g2s(xprep, p.pkg, PL.total, pkg_bar);
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
 
   const int n_act = *p.n_active;
@@ -455,54 +583,20 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
   };
   for (int i = 0; i < NS; ++i) issue_next();
 
-  // ---- phase 1: activations into shared memory (permuted x, sub-block sums, 32-block sums)
+  // ---- phase 1: the activation package arrives in shared memory by one bulk copy
   const int T = p.T;
   const int d = p.d;
   const int nbx = d / 256;
-  unsigned char* xB = xprep;                                                      // [T][xstride]
-  unsigned char* XBm = xB + (size_t)T * p.xstride;                                // [T][nbx][4][3][4] bf16
-  float* XbM = reinterpret_cast<float*>(XBm + (size_t)T * nbx * 96);             // [T][nbx]
-  float* X32 = XbM + T * nbx;                                                     // [T][d/32]
+  unsigned char* xB = xprep + PL.xB;                                   // [T][xstride]
+  unsigned char* XBm = xprep + PL.XBm;                                 // [T][nbx][4][3][4] bf16
+  float* XbM = reinterpret_cast<float*>(xprep + PL.XbM);              // [T][nbx]
+  float* X32 = reinterpret_cast<float*>(xprep + PL.X32);              // [T][d/32]
   if (PHASE == 1) {
-    for (int i = threadIdx.x; i < T * d; i += blockDim.x) {
-      const int tok = i / d, rem = i % d;
-      const int v = rem & 3, tq = (rem >> 2) & 3, s = (rem >> 4) & 3, jj = (rem >> 6) & 3, b = rem >> 8;
-      const int kk = 256 * b + 16 * (4 * tq + jj) + 4 * v + s;
-      reinterpret_cast<uint16_t*>(xB + (size_t)tok * p.xstride)[rem] = p.x[(size_t)tok * d + kk];
+    if (!mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT)) {
+      if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
+      for (int q = 0; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
+      return;
     }
-    for (int i = threadIdx.x; i < T * nbx * 16; i += blockDim.x) {
-      const int tok = i / (nbx * 16), b = (i / 16) % nbx, j = i % 16;
-      const uint16_t* xr = p.x + (size_t)tok * d + 256 * b + 16 * j;
-      float sacc = 0.0f;
-      for (int u = 0; u < 16; ++u) sacc += bf16_bits_to_f32(xr[u]);
-      const uint32_t hi = f32_to_bf16_rne(sacc);
-      const float r1 = sacc - bf16_bits_to_f32(hi);
-      const uint32_t mid = f32_to_bf16_rne(r1);
-      const uint32_t lo = f32_to_bf16_rne(r1 - bf16_bits_to_f32(mid));
-      uint16_t* dst = reinterpret_cast<uint16_t*>(XBm + (size_t)tok * nbx * 96) + ((b * 4 + (j >> 2)) * 3) * 4 + (j & 3);
-      dst[0] = (uint16_t)hi;
-      dst[4] = (uint16_t)mid;
-      dst[8] = (uint16_t)lo;
-    }
-    for (int i = threadIdx.x; i < T * (d / 32); i += blockDim.x) {
-      const int tok = i / (d / 32), bq = i % (d / 32);
-      const uint16_t* xr = p.x + (size_t)tok * d + 32 * bq;
-      float sacc = 0.0f;
-      for (int u = 0; u < 32; ++u) sacc += bf16_bits_to_f32(xr[u]);
-      X32[i] = sacc;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < T * nbx; i += blockDim.x) {
-      const int tok = i / nbx, b = i % nbx;
-      const uint16_t* src = reinterpret_cast<const uint16_t*>(XBm + (size_t)tok * nbx * 96) + b * 48;
-      float sacc = 0.0f;
-      for (int j = 0; j < 16; ++j) {
-        const uint16_t* e = src + ((j >> 2) * 3) * 4 + (j & 3);
-        sacc += (bf16_bits_to_f32(e[0]) + bf16_bits_to_f32(e[4])) + bf16_bits_to_f32(e[8]);
-      }
-      XbM[i] = sacc;
-    }
-    __syncthreads();
   }
 
   int cs_seq = 0;
@@ -579,10 +673,13 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
           } else {
             const int pos = it.off + 2 * t + (i & 1);
             const int b2 = row >> 8, j = (row >> 4) & 15, ip = row & 15;
-            const size_t base =
-                ((((size_t)pos * Fnb + b2) * 4 + (j & 3)) * 4 + (ip & 3)) * 4 * 8 + (size_t)(j >> 2) * 8;
-            p.hB[base + (ip >> 2)] = (uint16_t)hi;
-            p.hB[base + 4 + (ip >> 2)] = (uint16_t)lo;
+            const int byte = ip >> 2, s = ip & 3, v4 = (byte & 1) * 2 + (byte >> 1);
+            // limbs of h * 4^-min(s,2) (the down projection's A fragments keep codes in place)
+            uint32_t shi, slo;
+            split_bf16x2(__fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f)), shi, slo);
+            const size_t base = ((((size_t)pos * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 8 + (size_t)(j >> 2) * 8;
+            p.hB[base + v4] = (uint16_t)shi;
+            p.hB[base + 4 + v4] = (uint16_t)slo;
           }
         }
       }
@@ -647,7 +744,7 @@ size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs) {
   (void)E;
   if (T > DECODE_T_MAX) return ffn_gemm_ws_bytes(T, k, d, F, Fs);
   const size_t P = (size_t)T * k;
-  size_t s = 256;                                        // counters
+  size_t s = 1024 + pkg_layout(T, d).total;              // counters, activation package
   s += P * (F / 256) * 512 * 2;                          // hB
   s += P * (F / 256) * 4 * 12 * 2;                       // HBm
   s += (size_t)T * 2 * Fs * 2;                           // hS
@@ -690,7 +787,10 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   const size_t P = (size_t)a.T * a.k;
   char* w = reinterpret_cast<char*>(a.ws);
   p.counters = reinterpret_cast<int*>(w);
-  w += 256;
+  w += 1024;
+  p.pkg = reinterpret_cast<const unsigned char*>(w);
+  unsigned char* pkg_w = reinterpret_cast<unsigned char*>(w);
+  w += pkg_layout(a.T, p.d).total;
   p.hB = reinterpret_cast<uint16_t*>(w);
   w += P * (p.F / 256) * 512 * 2;
   p.HBm = reinterpret_cast<uint16_t*>(w);
@@ -702,6 +802,11 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
 
   const int sms = device_sm_count();
   const int smem_max = device_max_smem_optin();
+  ffn_prep_kernel<<<dim3(p.d / 256, a.T), 256, 0, s>>>(a.x, a.T, p.d, pkg_w);
+  {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   for (int phase = 1; phase <= 2; ++phase) {
     const int cap = (phase == 1) ? STAGE / 2 : STAGE;
     if (phase == 1) {
@@ -730,14 +835,10 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     p.cb_r = pick_chunk(p.nb_r, Q2K_BB, cap, 4, &p.whole_r);
     p.cb_s = S ? pick_chunk(p.nb_s, Q80_BB, cap, 8, &p.whole_s) : 1;
     if (p.cb_r <= 0 || p.cb_s <= 0) return cudaErrorInvalidValue;
-    size_t xbytes = 0;
-    if (phase == 1) {
-      const int nbx = p.d / 256;
-      xbytes = (size_t)a.T * p.xstride + (size_t)a.T * nbx * 96 + (size_t)a.T * nbx * 4 + (size_t)a.T * (p.d / 32) * 4;
-    }
+    const size_t xbytes = (phase == 1) ? (size_t)pkg_layout(a.T, p.d).total : 0;
     int nw = MAX_WARPS;
-    while (nw > 1 && (size_t)nw * NS * STAGE + MAX_WARPS * NS * 8 + xbytes > (size_t)smem_max) --nw;
-    const size_t smem = (size_t)nw * NS * STAGE + MAX_WARPS * NS * 8 + xbytes;
+    while (nw > 1 && (size_t)nw * NS * STAGE + BAR_BYTES + xbytes > (size_t)smem_max) --nw;
+    const size_t smem = (size_t)nw * NS * STAGE + BAR_BYTES + xbytes;
     if (smem > (size_t)smem_max) return cudaErrorInvalidValue;
     cudaError_t e;
     if (phase == 1) {

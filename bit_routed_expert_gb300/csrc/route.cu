@@ -19,13 +19,41 @@ namespace bre {
 namespace {
 
 constexpr int SMALL_TT = 8;      // tokens per CTA, small-batch logits
-constexpr int SMALL_ET = 8;      // experts per CTA, small-batch logits
+constexpr int SMALL_ET = 4;      // experts per CTA, small-batch logits
+constexpr int SMALL_THREADS = SMALL_ET * 32;
 constexpr int TILE_T = 32;       // tokens per CTA, tiled logits
 constexpr int TILE_E = 32;       // experts per CTA, tiled logits
 constexpr int SMALL_T_MAX = 32;  // up to this many tokens use the small-batch kernel
 
+// s = 1 / (1 + exp(-z)) in float, every step one IEEE operation so that any conforming
+// machine gets the same bits: Cody-Waite range reduction n = rint(x log2 e), r = x - n ln2
+// (ln 2 split in two float parts, the first with few enough bits that n * LN2_HI is exact),
+// exp(r) by its degree-7 Taylor polynomial in Horner form, scaled by 2^n.  x = -z is clamped
+// below at -30 (there 1 + exp(x) == 1 in float); x > 88 gives 0.
 __device__ __forceinline__ float sigmoid_ref(float z) {
-  return (float)(1.0 / (1.0 + exp(-(double)z)));
+  const float LOG2E = 1.44269504088896341f;
+  const float LN2_HI = 0.693359375f;
+  const float LN2_LO = -2.12194440054690583e-4f;
+  float x = -z;
+  if (isnan(x)) return x;
+  if (x > 88.0f) return 0.0f;
+  x = fmaxf(x, -30.0f);
+  const float n = rintf(__fmul_rn(x, LOG2E));
+  float r = __fmaf_rn(-n, LN2_HI, x);
+  r = __fmaf_rn(-n, LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = __fmaf_rn(p, r, 1.0f / 720.0f);
+  p = __fmaf_rn(p, r, 1.0f / 120.0f);
+  p = __fmaf_rn(p, r, 1.0f / 24.0f);
+  p = __fmaf_rn(p, r, 1.0f / 6.0f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  // p * 2^n with n in [-44, 128): exact scaling (two steps so that 2^n itself never overflows)
+  const int ni = (int)n;
+  const int n1 = ni / 2, n2 = ni - n1;
+  const float e = __fmul_rn(__fmul_rn(p, __int_as_float((127 + n1) << 23)), __int_as_float((127 + n2) << 23));
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
 // Does (ka, ia) rank before (kb, ib)?  Larger key first, then lower id; NaN last.
@@ -111,60 +139,80 @@ __device__ void topk_warp(const float* __restrict__ s_row, const float* __restri
 }
 
 // Small batches: CTA = up to SMALL_TT tokens x SMALL_ET experts, all 32 partials.
-// Thread (e_l = tid & 7, j = tid >> 3) runs the fmaf chain of partial j of expert e_l
-// for every token of the CTA.  The last CTA to finish selects the top k of every token.
-__global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x,
+// Thread (e_l = tid % SMALL_ET, j = tid / SMALL_ET) runs the fmaf chain of partial j of expert e_l
+// for every token of the CTA.  With NI = d/32 known at compile time every W_r load of the
+// thread is issued before the first FMA (one memory round trip); x is staged once as FP32,
+// transposed to [c][token], so one row costs two 16-byte shared loads.  The last CTA to
+// finish selects the top k of every token.
+template <int NI>
+__global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ w_r,
                                                           const float* __restrict__ bias, int T, int d, int E,
                                                           int k, float* __restrict__ S, int* ticket,
                                                           int32_t* __restrict__ ids, float* __restrict__ wts) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);                             // [TT][d]
-  float* part = reinterpret_cast<float*>(smem_raw + (size_t)SMALL_TT * d * 2);      // [TT][32][8]
+  float* xs = reinterpret_cast<float*>(smem_raw);                                    // [d][TT]
+  float* part = reinterpret_cast<float*>(smem_raw + (size_t)SMALL_TT * d * 4);      // [TT][32][ET]
   __shared__ int is_last;
   pdl_wait();
   const int tid = threadIdx.x;
   const int e0 = blockIdx.x * SMALL_ET;
   const int t0 = blockIdx.y * SMALL_TT;
   const int nt = min(SMALL_TT, T - t0);
-  for (int i = tid; i < SMALL_TT * d / 8; i += 256) {
-    const int tt = i / (d / 8);
+  const int e_l = tid % SMALL_ET, j = tid / SMALL_ET;
+  const int e = e0 + e_l;
+  const float* wcol = w_r + (e < E ? e : 0);
+  float wv[NI > 0 ? NI : 1];
+  if (NI > 0) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) wv[i] = (e < E) ? __ldg(wcol + (size_t)(j + 32 * i) * E) : 0.0f;
+  }
+  // token index fastest across threads: the eight stores of a row land in eight consecutive words
+#pragma unroll 8
+  for (int i = tid; i < SMALL_TT * d / 8; i += SMALL_THREADS) {
+    const int tt = i % SMALL_TT, c = (i / SMALL_TT) * 8;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (tt < nt) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d) + (i % (d / 8)));
-    reinterpret_cast<uint4*>(xs)[i] = v;
+    if (tt < nt) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + c));
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      xs[(c + 2 * q) * SMALL_TT + tt] = bf16_bits_to_f32(w4[q] & 0xFFFFu);
+      xs[(c + 2 * q + 1) * SMALL_TT + tt] = bf16_bits_to_f32(w4[q] >> 16);
+    }
   }
   __syncthreads();
-  const int e_l = tid & 7, j = tid >> 3;
-  const int e = e0 + e_l;
   float acc[SMALL_TT];
 #pragma unroll
   for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = 0.0f;
-  const int n = d / 32;
-  const float* wcol = w_r + e;
-  constexpr int B = 16;
-  for (int i0 = 0; i0 < n; i0 += B) {
-    float wv[B];
+  auto fma_row = [&](int c, float wgt) {
+    const float4* xp = reinterpret_cast<const float4*>(xs + c * SMALL_TT);
+    const float4 a = xp[0], b = xp[1];
+    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const int c = j + 32 * (i0 + u);
-      wv[u] = (e < E && i0 + u < n) ? __ldg(wcol + (size_t)c * E) : 0.0f;
-    }
+    for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = fmaf(xv[tt], wgt, acc[tt]);
+  };
+  if (NI > 0) {
 #pragma unroll
-    for (int u = 0; u < B; ++u) {
-      if (i0 + u < n) {
-        const int c = j + 32 * (i0 + u);
+    for (int i = 0; i < NI; ++i) fma_row(j + 32 * i, wv[i]);
+  } else {
+    const int n = d / 32;
+    constexpr int B = 16;
+    for (int i0 = 0; i0 < n; i0 += B) {
+      float wb[B];
 #pragma unroll
-        for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = fmaf(bf16_bits_to_f32(xs[tt * d + c]), wv[u], acc[tt]);
-      }
+      for (int u = 0; u < B; ++u) wb[u] = (e < E && i0 + u < n) ? __ldg(wcol + (size_t)(j + 32 * (i0 + u)) * E) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < B; ++u)
+        if (i0 + u < n) fma_row(j + 32 * (i0 + u), wb[u]);
     }
   }
 #pragma unroll
-  for (int tt = 0; tt < SMALL_TT; ++tt) part[(tt * 32 + j) * 8 + e_l] = acc[tt];
+  for (int tt = 0; tt < SMALL_TT; ++tt) part[(tt * 32 + j) * SMALL_ET + e_l] = acc[tt];
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
-  for (int q = warp; q < SMALL_TT * SMALL_ET; q += 8) {
+  for (int q = warp; q < SMALL_TT * SMALL_ET; q += SMALL_THREADS / 32) {
     const int tt = q / SMALL_ET, el = q % SMALL_ET;
-    float v = part[(tt * 32 + lane) * 8 + el];
+    float v = part[(tt * 32 + lane) * SMALL_ET + el];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (lane == 0 && tt < nt && e0 + el < E) S[(size_t)(t0 + tt) * E + e0 + el] = sigmoid_ref(v);
@@ -179,7 +227,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int t = warp; t < T; t += 8) topk_warp(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
+  for (int t = warp; t < T; t += SMALL_THREADS / 32)
+    topk_warp(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
   if (tid == 0) *ticket = 0;
 }
 
@@ -402,22 +451,27 @@ cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias,
   // the ticket sits at a fixed offset so that calls with different T share it
   int* ticket = reinterpret_cast<int*>(ws);
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
-  if (T <= SMALL_T_MAX) {
-    const size_t smem = (size_t)SMALL_TT * d * 2 + SMALL_TT * 32 * 8 * sizeof(float);
-    static int configured_dev = -1;
-    static size_t configured_smem = 0;
-    int dev;
-    cudaGetDevice(&dev);
-    if (dev != configured_dev || smem > configured_smem) {
-      cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-      if (e != cudaSuccess) return e;
-      configured_dev = dev;
-      configured_smem = smem;
-    }
+  const size_t small_smem = (size_t)SMALL_TT * d * 4 + SMALL_TT * 32 * SMALL_ET * sizeof(float);
+  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin()) {
+    const size_t smem = small_smem;
     dim3 grid((E + SMALL_ET - 1) / SMALL_ET, (T + SMALL_TT - 1) / SMALL_TT);
-    route_small_kernel<<<grid, 256, smem, s>>>(x, w_r, bias, T, d, E, k, S, ticket, ids, w);
-    return cudaGetLastError();
+    auto launch = [&](auto kern) -> cudaError_t {
+      static int configured_dev = -1;
+      static size_t configured_smem = 0;
+      int dev;
+      cudaGetDevice(&dev);
+      if (dev != configured_dev || smem > configured_smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+        configured_smem = smem;
+      }
+      kern<<<grid, SMALL_THREADS, smem, s>>>(x, w_r, bias, T, d, E, k, S, ticket, ids, w);
+      return cudaGetLastError();
+    };
+    if (d == 4096) return launch(route_small_kernel<128>);
+    if (d == 512) return launch(route_small_kernel<16>);
+    return launch(route_small_kernel<0>);
   }
   dim3 grid((T + TILE_T - 1) / TILE_T, (E + TILE_E - 1) / TILE_E);
   route_tiled_kernel<<<grid, 512, 0, s>>>(x, w_r, T, d, E, S);

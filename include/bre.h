@@ -90,7 +90,10 @@ const char *bre_status_string(bre_status s);
  *   z = x[t,:] . w_r[:,e]  -- FP32, 32 partial sums (partial j takes fmaf over
  *       rows c = j, j+32, ... in ascending order, from +0), then a butterfly
  *       p_j += p_(j^o) for o = 16, 8, 4, 2, 1; z = p_0
- *   s = (float)(1 / (1 + exp(-(double)z)));  key = s + bias[e]  (float)
+ *   s = 1 / (1 + exp(-z)) in float by a fixed sequence of IEEE operations
+ *       (Cody-Waite range reduction, degree-7 Taylor polynomial of exp with fmaf,
+ *       exact scaling by 2^n; z < -88 gives s = 0), so it is reproducible bit for bit
+ *   key = s + bias[e]  (float)
  * ids[t,:] = the k experts with the largest key, ordered by key descending
  * then id ascending (a NaN key ranks last); w[t,j] = s_j / S with
  * S = (((s_0 + s_1) + s_2) ...) in slot order -- weights use the UNBIASED

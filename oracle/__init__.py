@@ -55,6 +55,8 @@ def lib():
         L.or_e4m3_to_f32.argtypes = [C.c_uint8]
         L.or_e8m0_to_f32.restype = C.c_float
         L.or_e8m0_to_f32.argtypes = [C.c_uint8]
+        L.or_sigmoid.restype = C.c_float
+        L.or_sigmoid.argtypes = [C.c_float]
         L.or_dequant_q2k.argtypes = [P, i64, P]
         L.or_dequant_q8_0.argtypes = [P, i64, P]
         L.or_engram_gather.argtypes = [P, P, i32, P, i32, i32, P, P]

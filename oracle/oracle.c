@@ -16,7 +16,12 @@
  *   R1  router logit order "LANE32": 32 partial sums, partial j accumulates
  *       fmaf over c = j, j+32, ... in ascending c from +0.0f, then a butterfly
  *       p_j <- p_j + p_(j xor o) for o = 16, 8, 4, 2, 1; z = p_0.
- *   R2  s = (float)(1 / (1 + exp(-(double)z))).
+ *   R2  s = 1 / (1 + e) in float, e = exp(-z) by Cody-Waite range reduction
+ *       (n = rint(x * log2 e), r = x - n*ln2 in two float parts) and the
+ *       degree-7 Taylor polynomial of exp(r) in Horner form with fmaf; x is
+ *       clamped below at -30 (there 1 + e == 1) and x > 88 gives s = 0.  Every
+ *       step is one IEEE float operation, so any conforming machine gets the
+ *       same bits.
  *   R3  key = s + b (float); order by key descending, id ascending; a NaN key
  *       ranks below every number.
  *   R4  S = (((s_0 + s_1) + s_2) + ...) in slot order; w_j = s_j / S.
@@ -208,6 +213,35 @@ static float lane32_dot(const uint16_t *x, const float *wr, int d, int E, int e)
     return p[0];
 }
 
+/* R2: the router's sigmoid (see the header comment). */
+float or_sigmoid(float z)
+{
+    const float LOG2E = 1.44269504088896341f;
+    const float LN2_HI = 0.693359375f;              /* 355/512: n * LN2_HI is exact */
+    const float LN2_LO = -2.12194440054690583e-4f;  /* ln 2 - LN2_HI */
+    float x = -z;
+    if (isnan(x))
+        return x;
+    if (x > 88.0f)
+        return 0.0f;
+    if (x < -30.0f)
+        x = -30.0f;
+    float n = rintf(x * LOG2E);
+    float r = fmaf(-n, LN2_HI, x);
+    r = fmaf(-n, LN2_LO, r);
+    /* exp(r) = sum r^k / k!, k = 0..7 */
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    float e = ldexpf(p, (int)n);
+    return 1.0f / (1.0f + e);
+}
+
 /* R3: does (ka, ia) rank before (kb, ib)? */
 static int ranks_before(float ka, int ia, float kb, int ib)
 {
@@ -229,7 +263,7 @@ void or_route(const uint16_t *x, const float *wr, const float *bias, int T, int 
         const uint16_t *xt = x + (int64_t)t * d;
         for (int e = 0; e < E; ++e) {
             float z = lane32_dot(xt, wr, d, E, e);
-            s[e] = (float)(1.0 / (1.0 + exp(-(double)z)));          /* R2 */
+            s[e] = or_sigmoid(z);                                        /* R2 */
             key[e] = s[e] + (bias ? bias[e] : 0.0f);                 /* R3 */
             used[e] = 0;
             if (z_out)

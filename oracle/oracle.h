@@ -12,6 +12,7 @@ uint16_t or_bf16_rne(float f);
 uint16_t or_bf16_rne_f64(double x);
 float or_e4m3_to_f32(uint8_t b);
 float or_e8m0_to_f32(uint8_t e);
+float or_sigmoid(float z);
 
 void or_dequant_q2k(const uint8_t *blk, int64_t nblk, float *out);
 void or_dequant_q8_0(const uint8_t *blk, int64_t nblk, float *out);
