@@ -120,8 +120,11 @@ cudaError_t launch_combine(const float* y_pairs, const float* topk_w, const int3
                            int E, const float* y_shared, int T, int k, int d, uint16_t* out, float* out_f32,
                            cudaStream_t s) {
   const long long n = (long long)T * (d / 8);
-  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y_pairs, topk_w, inv, offsets, E, y_shared, T, k, d,
-                                                            out, out_f32);
+  {
+    const cudaError_t le = launch_k(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y_pairs,
+                                    topk_w, inv, offsets, E, y_shared, T, k, d, out, out_f32);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -132,7 +135,11 @@ cudaError_t launch_residual_norm(const uint16_t* x, const uint16_t* moe, int T, 
     cudaError_t e = cudaFuncSetAttribute(residual_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  residual_norm_kernel<<<T, 256, smem, s>>>(x, moe, d, scale, eps, x_out, u_out);
+  {
+    const cudaError_t le = launch_k(residual_norm_kernel, dim3(T), dim3(256), smem, s, x, moe, d, scale, eps, x_out,
+                                    u_out);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -94,9 +94,17 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
   if (H == 1)
-    engram_gather_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(tabs, n_tables, ids, T, H, out, err);
+    {
+      const cudaError_t le = launch_k(engram_gather_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0, s, tabs,
+                                      n_tables, ids, T, H, out, err);
+      if (le != cudaSuccess) return le;
+    }
   else
-    engram_gather_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(tabs, n_tables, ids, T, H, out, err);
+    {
+      const cudaError_t le = launch_k(engram_gather_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, s, tabs,
+                                      n_tables, ids, T, H, out, err);
+      if (le != cudaSuccess) return le;
+    }
   return cudaGetLastError();
 }
 

@@ -5,11 +5,12 @@
 // against a dequantised F32 reference); SwiGLU from the V4-Flash description.
 //
 // Design (GB300): the path is bound by streaming 2-bit weights from HBM, so every
-// byte is read once.  Each warp owns a two-stage ring in shared memory that
-// bulk-copy (TMA) engines fill with 16-row tiles of an expert matrix; the warp
-// dequantises in registers straight into mma.sync A fragments and multiplies by
-// the expert's tokens (N = 8 columns).  Work items (expert, 16-row tile) are
-// handed out by an atomic counter so that busy SMs take fewer items.
+// byte is read once.  Each warp owns a two-stage ring in shared memory that the TMA
+// engine fills with 16-row chunks of one expert matrix (one tensor copy per chunk, or
+// one bulk copy when a whole 16-row tile fits a stage); the warp dequantises in
+// registers straight into mma.sync A fragments and multiplies by the expert's tokens
+// (N = 8 columns).  Work items (expert, 16-row tile) are handed out by an atomic
+// counter so that busy SMs take fewer items.
 //
 // Exactness: a Q2_K weight is (d*sc)*q - dmin*m.  The A fragment holds the
 // integer 128 + sc*q (exact in BF16), so one 256-weight block contributes
@@ -23,6 +24,9 @@
 // and B agree.  For Q2_K, step (jj, s) of thread t uses sub-block 4t+jj and codes
 // s, 4+s, 8+s, 12+s of it (the four codes of one byte lane after one shift), and the
 // activations are stored permuted to match.  Q8_0 uses natural order.
+#include <algorithm>
+#include <mutex>
+
 #include "bre_common.cuh"
 #include "kernels.h"
 
@@ -31,13 +35,29 @@ namespace bre {
 namespace {
 
 constexpr int NS = 2;                 // ring stages per warp
-constexpr int STAGE = 10752;          // bytes per stage (2 x 16 rows x 336 B)
-constexpr int MAX_WARPS = 8;
+constexpr int STAGE = 5376;           // bytes per stage: 16 rows x 336 B of one matrix
+constexpr int MAX_WARPS = 12;         // phase 1 (at most 170 registers a thread)
+constexpr int MAX_WARPS_P2 = 8;       // phase 2 (double-buffered B operand, up to 255 registers)
 constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
 constexpr int BAR_BYTES = 256;                  // mbarrier region: MAX_WARPS * NS ring barriers + package
+
+// n / d as a multiply and shift, for 0 <= n < 2^31 (round-up multiplier m = ceil(2^(31+l) / d),
+// 2^l >= d; the error n (m - 2^(31+l)/d) / 2^(31+l) stays below 1/d, so the floor is exact).
+struct FDiv {
+  uint32_t m;
+  int sh;
+};
+__host__ __device__ __forceinline__ int fdiv(int n, FDiv f) {
+  return (int)(((unsigned long long)(unsigned)n * f.m) >> f.sh);
+}
+static FDiv make_fdiv(unsigned d) {
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  return FDiv{(uint32_t)(((1ull << (31 + l)) + d - 1) / d), 31 + l};
+}
 
 struct DecParams {
   const uint8_t* rw0;  // routed: phase 1 gate, phase 2 down
@@ -67,6 +87,14 @@ struct DecParams {
   int32_t* err;
   int xstride;  // bytes per token row of the permuted activations in shared memory
   const unsigned char* pkg;  // activation package in global memory (phase 1)
+  uint32_t m43;              // 0x43004300: BF16 exponent pattern of 128 in both halves
+  int kp_r, kp_s;            // K parts per 16-row tile (phase 1): items are (tile, K part)
+  int C_r, C_s;              // chunks per matrix row of a routed / the shared expert
+  int cpi_r, cpi_s;          // chunks per matrix in one item (C / K parts)
+  FDiv fd_kps, fd_kpr, fd_trk, fd_k;   // divisors: K parts (shared, routed), routed tiles * K parts, k
+  float2* part_r;            // routed partial (gate, up) sums: [pair position][tile][K part][16 rows]
+  float2* part_s;            // shared partial sums: [token][tile][K part][16 rows]
+  int* tile_cnt;             // per tile count of finished K parts (zero between calls)
 };
 
 struct Item {
@@ -75,6 +103,10 @@ struct Item {
   int e, off, n;
   int tile;
   int nb, cb, C, whole, bb;
+  int KP, kp;   // K parts of the tile and this item's part
+  int cpi;      // chunks per matrix in this item (C / KP)
+  int nch;      // chunks of the item: cpi per matrix, gate then up in phase 1
+  int slot;     // tile index for the K-part fix-up
   const uint8_t* src0;
   const uint8_t* src1;
 };
@@ -84,9 +116,13 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
   Item it;
   it.id = id;
   if (id < 0) return it;
-  if (id < tiles_s) {
+  const int kps = (PHASE == 1) ? p.kp_s : 1, kpr = (PHASE == 1) ? p.kp_r : 1;
+  if (id < tiles_s * kps) {
     it.shared = true;
-    it.tile = id;
+    it.tile = fdiv(id, p.fd_kps);
+    it.KP = kps;
+    it.kp = id - it.tile * kps;
+    it.slot = it.tile;
     it.e = -1;
     it.off = 0;
     it.n = p.T;
@@ -97,13 +133,24 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
     it.src0 = p.sw0;
     it.src1 = p.sw1;
   } else {
-    const int r = id - tiles_s;
-    const int a = r / tiles_r;
+    const int r = id - tiles_s * kps;
+    const int a = fdiv(r, p.fd_trk), rt = r - a * (tiles_r * kpr);
     it.shared = false;
-    it.tile = r % tiles_r;
+    it.tile = fdiv(rt, p.fd_kpr);
+    it.KP = kpr;
+    it.kp = rt - it.tile * kpr;
+    it.slot = tiles_s + a * tiles_r + it.tile;
     it.e = __ldg(p.active + a);
-    it.off = __ldg(p.offsets + it.e);
-    it.n = __ldg(p.offsets + it.e + 1) - it.off;
+    if ((unsigned)it.e >= (unsigned)p.E) {
+      // an expert id the weights do not hold: no columns, and no copy outside the weights
+      set_err(p.err, BRE_DEVERR_EXPERT_ID);
+      it.e = 0;
+      it.off = 0;
+      it.n = 0;
+    } else {
+      it.off = __ldg(p.offsets + it.e);
+      it.n = __ldg(p.offsets + it.e + 1) - it.off;
+    }
     it.nb = p.nb_r;
     it.cb = p.cb_r;
     it.whole = p.whole_r;
@@ -111,31 +158,36 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
     it.src0 = p.rw0 + (long long)it.e * p.rs0;
     it.src1 = (PHASE == 1) ? p.rw1 + (long long)it.e * p.rs1 : nullptr;
   }
-  it.C = it.nb / it.cb;
+  it.C = it.shared ? p.C_s : p.C_r;
+  it.cpi = it.shared ? p.cpi_s : p.cpi_r;
+  it.nch = (PHASE == 1 ? 2 : 1) * it.cpi;
   return it;
 }
 
-// Issue the bulk copies of chunk c of `it` into `stage` (warp-wide; lane 0 arms the barrier).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Lane 0 issues the copy of chunk cc of `it` into `stage`: one bulk copy of a whole 16-row tile,
+// or one tensor copy of a 16-row x cb-block box (maps: [experts][rows][row words]).
 template <int PHASE>
-__device__ __forceinline__ void issue_chunk(const Item& it, int c, unsigned char* stage, uint64_t* bar, int lane) {
-  constexpr int NMAT = (PHASE == 1) ? 2 : 1;
-  const int row_bytes = it.nb * it.bb;
+__device__ __forceinline__ void issue_chunk(const Item& it, int cc, unsigned char* stage, uint64_t* bar, int lane,
+                                            const CUtensorMap* map0, const CUtensorMap* map1) {
+  if (lane != 0) return;
+  const int m = (PHASE == 1 && cc >= it.cpi) ? 1 : 0;
+  const int c = it.kp * it.cpi + (cc - m * it.cpi);
   const int chunk_bytes = it.cb * it.bb;
-  const uint32_t mat_bytes = 16u * chunk_bytes;
-  if (lane == 0) mbar_arrive_expect_tx(bar, NMAT * mat_bytes);
-  __syncwarp();
+  const uint32_t bytes = 16u * chunk_bytes;
+  mbar_arrive_expect_tx(bar, bytes);
   if (it.whole) {
-    if (lane < NMAT) {
-      const uint8_t* src = (lane == 0 ? it.src0 : it.src1) + (long long)it.tile * 16 * row_bytes;
-      bulk_g2s(stage + lane * mat_bytes, src, mat_bytes, bar);
-    }
+    const uint8_t* src = (m ? it.src1 : it.src0) + (long long)it.tile * 16 * chunk_bytes;
+    bulk_g2s(stage, src, bytes, bar);
   } else {
-    if (lane < 16 * NMAT) {
-      const int m = lane >> 4, r = lane & 15;
-      const uint8_t* src = (m == 0 ? it.src0 : it.src1) + (long long)(it.tile * 16 + r) * row_bytes +
-                           (long long)c * chunk_bytes;
-      bulk_g2s(stage + m * mat_bytes + r * chunk_bytes, src, chunk_bytes, bar);
-    }
+    tma_load_3d(stage, m ? map1 : map0, c * (chunk_bytes / 4), it.tile * 16, it.shared ? 0 : it.e, bar);
   }
 }
 
@@ -147,26 +199,20 @@ __device__ __forceinline__ uint32_t lds_u32_a2(const unsigned char* p) {  // 2-b
   return lds_u16(p) | (lds_u16(p + 2) << 16);
 }
 
-// Q2_K A fragment of one row for step s: 4 codes x sc as (128 + sc*q) bf16 pairs.
-__device__ __forceinline__ void q2k_frag(uint32_t qw, uint32_t sc, int s, uint32_t& lo, uint32_t& hi) {
-  const uint32_t v = ((qw >> (2 * s)) & 0x03030303u) * sc;
-  lo = prmt(v, C43, SEL_LO);
-  hi = prmt(v, C43, SEL_HI);
-}
-
 // Q2_K A fragments of one row for step s, codes left in place: one LOP3 per register gives the
 // BF16 pair 128 + c * 4^e (e = min(s, 2); the code occupies mantissa bits 2e, 2e+1).  lo holds
 // codes (s, 8+s) of the sub-block word (bytes 0 and 2), hi codes (4+s, 12+s) (bytes 1 and 3).
-__device__ __forceinline__ void q2k_pairs(uint32_t w, int s, uint32_t& lo, uint32_t& hi) {
-  constexpr uint32_t M43 = 0x43004300u;
+// m43 is the exponent pattern 0x43004300 held in a register (a kernel parameter, so that the
+// mask can be the instruction's immediate and the OR needs no second instruction).
+__device__ __forceinline__ void q2k_pairs(uint32_t w, int s, uint32_t m43, uint32_t& lo, uint32_t& hi) {
   if (s < 3) {
     const uint32_t m = 0x00030003u << (2 * s);
-    lo = (w & m) | M43;
-    hi = ((w >> 8) & m) | M43;
+    lo = (w & m) | m43;
+    hi = ((w >> 8) & m) | m43;
   } else {
     const uint32_t m = 0x00030003u << 4;
-    lo = ((w >> 2) & m) | M43;
-    hi = ((w >> 10) & m) | M43;
+    lo = ((w >> 2) & m) | m43;
+    hi = ((w >> 10) & m) | m43;
   }
 }
 
@@ -195,147 +241,19 @@ __device__ __forceinline__ void q80_frag(uint32_t w, uint32_t& lo01, uint32_t& l
 }
 
 // ----------------------------------------------------------------------------
-// phase 1, routed Q2_K: gate and up of 16 rows over one chunk
+// phase 1, routed Q2_K: 16 rows of one matrix (gate or up) over one chunk
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void p1_q2k_chunk(const unsigned char* stage, int cb, int c, int g, int t,
-                                             const unsigned char* xb_g,    // permuted x of column g (or null)
-                                             const unsigned char* xbm_g,   // XBm of column g (or null)
-                                             const float* xbM0, const float* xbM1,  // XbM rows of columns 2t, 2t+1
-                                             float (&acc)[2][4]) {
+// The block loop stays rolled (unrolled it outgrows the instruction cache); CB > 0 fixes the
+// chunk's block count at compile time so that addresses are base + immediate, CB == 0 takes cb_rt.
+template <int CB>
+__device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt, int c, int g, int t,
+                                           const unsigned char* xb_g,    // permuted x of column g
+                                           const unsigned char* xbm_g,   // XBm of column g
+                                           const float* xbM0, const float* xbM1,  // XbM rows of columns 2t, 2t+1
+                                           uint32_t m43, float (&acc)[4]) {
+  const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q2K_BB;
-  const int mat_bytes = 16 * chunk_bytes;
-  for (int bl = 0; bl < cb; ++bl) {
-    const int b = c * cb + bl;
-    uint32_t qw[2][2][4], sw[2][2], dd[2][2];
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const unsigned char* base = stage + m * mat_bytes + (g + 8 * rr) * chunk_bytes + bl * Q2K_BB;
-        sw[m][rr] = lds_u32(base + 4 * t);
-        dd[m][rr] = lds_u32(base + 80);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) qw[m][rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
-      }
-    // one accumulator per (matrix, jj): four independent MMA chains per matrix
-    float P[2][4][4], M[2][4];
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) P[m][jj][i] = 0.0f;
-        M[m][i] = 0.0f;
-      }
-    const unsigned char* xblk = xb_g ? xb_g + b * 512 : nullptr;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      uint32_t sc2[2][2], nsc2[2][2];
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) q2k_scale_pairs(sw[m][rr] & 0x0F0F0F0Fu, jj, sc2[m][rr], nsc2[m][rr]);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        uint2 bv = make_uint2(0u, 0u);
-        if (xblk) bv = *reinterpret_cast<const uint2*>(xblk + ((jj * 4 + s) * 4 + t) * 8);
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          uint32_t a0, a1, a2, a3;
-          q2k_pairs(qw[m][0][jj], s, a0, a2);
-          q2k_pairs(qw[m][1][jj], s, a1, a3);
-          a0 = bf16x2_fma(a0, sc2[m][0], nsc2[m][0]);
-          a2 = bf16x2_fma(a2, sc2[m][0], nsc2[m][0]);
-          a1 = bf16x2_fma(a1, sc2[m][1], nsc2[m][1]);
-          a3 = bf16x2_fma(a3, sc2[m][1], nsc2[m][1]);
-          mma_bf16_16816(P[m][jj], a0, a1, a2, a3, bv.x, bv.y);
-        }
-      }
-    }
-    // min term: M' = sum_j (128 + m_j) X_j over the 16 sub-blocks, X_j in three limbs
-#pragma unroll
-    for (int limb = 0; limb < 3; ++limb) {
-      uint2 bm = make_uint2(0u, 0u);
-      if (xbm_g) bm = *reinterpret_cast<const uint2*>(xbm_g + ((b * 4 + t) * 3 + limb) * 8);
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint32_t mg = (sw[m][0] >> 4) & 0x0F0F0F0Fu;
-        const uint32_t mg8 = (sw[m][1] >> 4) & 0x0F0F0F0Fu;
-        mma_bf16_16816(M[m], prmt(mg, C43, SEL_LO), prmt(mg8, C43, SEL_LO), prmt(mg, C43, SEL_HI),
-                       prmt(mg8, C43, SEL_HI), bm.x, bm.y);
-      }
-    }
-    const float x0 = xbM0 ? xbM0[b] : 0.0f, x1 = xbM1 ? xbM1[b] : 0.0f;
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t ddv = dd[m][i >> 1];
-        const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
-        const float xs = (i & 1) ? x1 : x0;
-        const float psum = (P[m][0][i] + P[m][1][i]) + (P[m][2][i] + P[m][3][i]);
-        const float mv = fmaf(-128.0f, xs, M[m][i]);
-        acc[m][i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[m][i]));
-      }
-  }
-}
-
-// ----------------------------------------------------------------------------
-// phase 1, shared Q8_0: gate and up of 16 rows over one chunk (natural k order)
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void p1_q80_chunk(const unsigned char* stage, int cb, int c, int g, int t,
-                                             const uint16_t* xrow_g,  // global x row of column g (or null)
-                                             const float* x32_0, const float* x32_1, float (&acc)[2][4]) {
-  const int chunk_bytes = cb * Q80_BB;
-  const int mat_bytes = 16 * chunk_bytes;
-  for (int bl = 0; bl < cb; ++bl) {
-    const int bq = c * cb + bl;
-    float Ph[2][4], Pl[2][4];
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        Ph[m][i] = 0.0f;
-        Pl[m][i] = 0.0f;
-      }
-    uint32_t dd[2][2];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint2 bv = make_uint2(0u, 0u);
-      if (xrow_g) bv = __ldg(reinterpret_cast<const uint2*>(xrow_g + 32 * bq + 16 * hf + 4 * t));
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        uint32_t l01[2], l23[2], h01[2], h23[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const unsigned char* base = stage + m * mat_bytes + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
-          if (hf == 0) dd[m][rr] = lds_u16(base);
-          q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), l01[rr], l23[rr], h01[rr], h23[rr]);
-        }
-        mma_bf16_16816(Pl[m], l01[0], l01[1], l23[0], l23[1], bv.x, bv.y);
-        mma_bf16_16816(Ph[m], h01[0], h01[1], h23[0], h23[1], bv.x, bv.y);
-      }
-    }
-    const float x0 = x32_0 ? x32_0[bq] : 0.0f, x1 = x32_1 ? x32_1[bq] : 0.0f;
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float dv = f16_bits_to_f32(dd[m][i >> 1]);
-        const float xs = (i & 1) ? x1 : x0;
-        const float v = fmaf(-2304.0f, xs, fmaf(16.0f, Ph[m][i], Pl[m][i]));
-        acc[m][i] = fmaf(dv, v, acc[m][i]);
-      }
-  }
-}
-
-// ----------------------------------------------------------------------------
-// phase 2, routed Q2_K down: 16 rows over one chunk; B = h limbs from global memory
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb, int c, int nb, int g, int t,
-                                             int pos_g, const uint16_t* __restrict__ hB,
-                                             const uint16_t* __restrict__ HBm, float (&acc)[4]) {
-  const int chunk_bytes = cb * Q2K_BB;
+#pragma unroll 1
   for (int bl = 0; bl < cb; ++bl) {
     const int b = c * cb + bl;
     uint32_t qw[2][4], sw[2], dd[2];
@@ -347,16 +265,9 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
     }
-    float P[4][4], M[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) P[jj][i] = 0.0f;
-    const uint16_t* hblk = (pos_g >= 0) ? hB + ((long long)pos_g * nb + b) * 512 : nullptr;
-    uint4 bvs[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      bvs[q] = hblk ? __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+    // one accumulator per jj: four independent MMA chains, each started by a C = 0 MMA
+    float P[4][4], M[4];
+    const unsigned char* xblk = xb_g + b * 512;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       uint32_t sc2[2], nsc2[2];
@@ -364,38 +275,35 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
       q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, jj, sc2[1], nsc2[1]);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const uint4 bv = bvs[jj * 4 + s];
+        const uint2 bv = *reinterpret_cast<const uint2*>(xblk + ((jj * 4 + s) * 4 + t) * 8);
         uint32_t a0, a1, a2, a3;
-        q2k_pairs(qw[0][jj], s, a0, a2);
-        q2k_pairs(qw[1][jj], s, a1, a3);
+        q2k_pairs(qw[0][jj], s, m43, a0, a2);
+        q2k_pairs(qw[1][jj], s, m43, a1, a3);
         a0 = bf16x2_fma(a0, sc2[0], nsc2[0]);
         a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
         a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
         a3 = bf16x2_fma(a3, sc2[1], nsc2[1]);
-        mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.x, bv.y);
-        mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.z, bv.w);
+        if (s == 0)
+          mma_bf16_16816_z(P[jj], a0, a1, a2, a3, bv.x, bv.y);
+        else
+          mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.x, bv.y);
       }
     }
-    float hsum = 0.0f;
+    // min term: M' = sum_j (128 + m_j) X_j over the 16 sub-blocks, X_j in three limbs
     {
       const uint32_t mg = (sw[0] >> 4) & 0x0F0F0F0Fu, mg8 = (sw[1] >> 4) & 0x0F0F0F0Fu;
       const uint32_t A0 = prmt(mg, C43, SEL_LO), A1 = prmt(mg8, C43, SEL_LO);
       const uint32_t A2 = prmt(mg, C43, SEL_HI), A3 = prmt(mg8, C43, SEL_HI);
-      const uint16_t* hm = (pos_g >= 0) ? HBm + (((long long)pos_g * nb + b) * 4 + t) * 12 : nullptr;
 #pragma unroll
       for (int limb = 0; limb < 3; ++limb) {
-        uint2 bm = make_uint2(0u, 0u);
-        if (hm) bm = __ldg(reinterpret_cast<const uint2*>(hm + limb * 4));
-        mma_bf16_16816(M, A0, A1, A2, A3, bm.x, bm.y);
-        hsum += bf16_bits_to_f32(bm.x & 0xFFFFu) + bf16_bits_to_f32(bm.x >> 16) +
-                bf16_bits_to_f32(bm.y & 0xFFFFu) + bf16_bits_to_f32(bm.y >> 16);
+        const uint2 bm = *reinterpret_cast<const uint2*>(xbm_g + ((b * 4 + t) * 3 + limb) * 8);
+        if (limb == 0)
+          mma_bf16_16816_z(M, A0, A1, A2, A3, bm.x, bm.y);
+        else
+          mma_bf16_16816(M, A0, A1, A2, A3, bm.x, bm.y);
       }
     }
-    // block sum of h for column g, then for the C-fragment columns 2t and 2t+1
-    hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
-    hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
-    const float x0 = __shfl_sync(0xffffffffu, hsum, (2 * t) * 4);
-    const float x1 = __shfl_sync(0xffffffffu, hsum, (2 * t + 1) * 4);
+    const float x0 = xbM0[b], x1 = xbM1[b];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t ddv = dd[i >> 1];
@@ -409,23 +317,28 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
 }
 
 // ----------------------------------------------------------------------------
-// phase 2, shared Q8_0 down: 16 rows over one chunk; B = h limbs (natural order)
+// phase 1, shared Q8_0: 16 rows of one matrix over one chunk (natural k order)
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb, int c, int g, int t, int Fs,
-                                             const uint16_t* hrow_g,  // hS[tok_g][0][:] or null
-                                             const float* hs16_0, const float* hs16_1, float (&acc)[4]) {
+__device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, int c, int g, int t,
+                                           const uint16_t* xrow_g,  // global x row of column g
+                                           const float* x32_0, const float* x32_1, float (&acc)[4]) {
   const int chunk_bytes = cb * Q80_BB;
+  // B (x from global memory) of block bl + 1 loads while block bl is processed
+  auto load_b = [&](int bq, uint2 (&b)[2]) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+      b[hf] = __ldg(reinterpret_cast<const uint2*>(xrow_g + 32 * bq + 16 * hf + 4 * t));
+  };
+  uint2 bcur[2], bnext[2];
+  load_b(c * cb, bcur);
   for (int bl = 0; bl < cb; ++bl) {
     const int bq = c * cb + bl;
-    float Ph[4] = {0.f, 0.f, 0.f, 0.f}, Pl[4] = {0.f, 0.f, 0.f, 0.f};
+    if (bl + 1 < cb) load_b(bq + 1, bnext);
+    float Ph[4], Pl[4];
     uint32_t dd[2];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      uint2 bh = make_uint2(0u, 0u), blo = make_uint2(0u, 0u);
-      if (hrow_g) {
-        bh = __ldg(reinterpret_cast<const uint2*>(hrow_g + 32 * bq + 16 * hf + 4 * t));
-        blo = __ldg(reinterpret_cast<const uint2*>(hrow_g + Fs + 32 * bq + 16 * hf + 4 * t));
-      }
+      const uint2 bv = bcur[hf];
       uint32_t l01[2], l23[2], h01[2], h23[2];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
@@ -433,13 +346,15 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb,
         if (hf == 0) dd[rr] = lds_u16(base);
         q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), l01[rr], l23[rr], h01[rr], h23[rr]);
       }
-      mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
-      mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], blo.x, blo.y);
-      mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
-      mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], blo.x, blo.y);
+      if (hf == 0) {
+        mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bv.x, bv.y);
+        mma_bf16_16816_z(Ph, h01[0], h01[1], h23[0], h23[1], bv.x, bv.y);
+      } else {
+        mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], bv.x, bv.y);
+        mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bv.x, bv.y);
+      }
     }
-    const float x0 = hs16_0 ? hs16_0[2 * bq] + hs16_0[2 * bq + 1] : 0.0f;
-    const float x1 = hs16_1 ? hs16_1[2 * bq] + hs16_1[2 * bq + 1] : 0.0f;
+    const float x0 = x32_0[bq], x1 = x32_1[bq];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float dv = f16_bits_to_f32(dd[i >> 1]);
@@ -447,6 +362,184 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb,
       const float v = fmaf(-2304.0f, xs, fmaf(16.0f, Ph[i], Pl[i]));
       acc[i] = fmaf(dv, v, acc[i]);
     }
+    bcur[0] = bnext[0];
+    bcur[1] = bnext[1];
+  }
+}
+
+// B operand of one block for column g: 16 uint4 (both limbs of h, fragment order) and the
+// three limbs of its sub-block sums.
+struct P2B {
+  uint4 v[16];
+  uint2 m[3];
+};
+
+__device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, const uint16_t* __restrict__ HBm,
+                                          int pos_g, int nb, int b, int t) {
+  const uint16_t* hblk = hB + ((long long)pos_g * nb + b) * 512;
+  const uint16_t* hm = HBm + (((long long)pos_g * nb + b) * 4 + t) * 12;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) B.v[q] = __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8));
+#pragma unroll
+  for (int limb = 0; limb < 3; ++limb) B.m[limb] = __ldg(reinterpret_cast<const uint2*>(hm + limb * 4));
+}
+
+// One 256-column block of 16 rows of the down projection.
+__device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_bytes, int g, int t, const P2B& B,
+                                             uint32_t m43, float (&acc)[4]) {
+  uint32_t qw[2][4], sw[2], dd[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const unsigned char* base = blk + (g + 8 * rr) * row_bytes;
+    sw[rr] = lds_u32(base + 4 * t);
+    dd[rr] = lds_u32(base + 80);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
+  }
+  float P[4][4], M[4];
+  // s outer, jj inner: consecutive MMAs go to different accumulators
+  uint32_t sc2[4][2], nsc2[4][2];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    q2k_scale_pairs(sw[0] & 0x0F0F0F0Fu, jj, sc2[jj][0], nsc2[jj][0]);
+    q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, jj, sc2[jj][1], nsc2[jj][1]);
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t A[4][4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      q2k_pairs(qw[0][jj], s, m43, A[jj][0], A[jj][2]);
+      q2k_pairs(qw[1][jj], s, m43, A[jj][1], A[jj][3]);
+      A[jj][0] = bf16x2_fma(A[jj][0], sc2[jj][0], nsc2[jj][0]);
+      A[jj][2] = bf16x2_fma(A[jj][2], sc2[jj][0], nsc2[jj][0]);
+      A[jj][1] = bf16x2_fma(A[jj][1], sc2[jj][1], nsc2[jj][1]);
+      A[jj][3] = bf16x2_fma(A[jj][3], sc2[jj][1], nsc2[jj][1]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint4 bv = B.v[jj * 4 + s];
+      if (s == 0)
+        mma_bf16_16816_z(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.x, bv.y);
+      else
+        mma_bf16_16816(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.x, bv.y);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint4 bv = B.v[jj * 4 + s];
+      mma_bf16_16816(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.z, bv.w);
+    }
+  }
+  float hsum = 0.0f;
+  {
+    const uint32_t mg = (sw[0] >> 4) & 0x0F0F0F0Fu, mg8 = (sw[1] >> 4) & 0x0F0F0F0Fu;
+    const uint32_t A0 = prmt(mg, C43, SEL_LO), A1 = prmt(mg8, C43, SEL_LO);
+    const uint32_t A2 = prmt(mg, C43, SEL_HI), A3 = prmt(mg8, C43, SEL_HI);
+#pragma unroll
+    for (int limb = 0; limb < 3; ++limb) {
+      const uint2 bm = B.m[limb];
+      if (limb == 0)
+        mma_bf16_16816_z(M, A0, A1, A2, A3, bm.x, bm.y);
+      else
+        mma_bf16_16816(M, A0, A1, A2, A3, bm.x, bm.y);
+      hsum += bf16_bits_to_f32(bm.x & 0xFFFFu) + bf16_bits_to_f32(bm.x >> 16) + bf16_bits_to_f32(bm.y & 0xFFFFu) +
+              bf16_bits_to_f32(bm.y >> 16);
+    }
+  }
+  // block sum of h for column g, then for the C-fragment columns 2t and 2t+1
+  hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
+  hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
+  const float x0 = __shfl_sync(0xffffffffu, hsum, (2 * t) * 4);
+  const float x1 = __shfl_sync(0xffffffffu, hsum, (2 * t + 1) * 4);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t ddv = dd[i >> 1];
+    const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
+    const float xs = (i & 1) ? x1 : x0;
+    const float psum = (P[0][i] + P[1][i]) + (P[2][i] + P[3][i]);
+    const float mv = fmaf(-128.0f, xs, M[i]);
+    acc[i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[i]));
+  }
+}
+
+// ----------------------------------------------------------------------------
+// phase 2, routed Q2_K down: 16 rows over one chunk; B = h limbs from global memory, loaded
+// one block ahead (two register sets) so that their latency hides behind a block of MMAs
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb, int c, int nb, int g, int t,
+                                             int pos_g, const uint16_t* __restrict__ hB,
+                                             const uint16_t* __restrict__ HBm, uint32_t m43, float (&acc)[4]) {
+  const int chunk_bytes = cb * Q2K_BB;
+  P2B B0, B1;
+  p2_load_b(B0, hB, HBm, pos_g, nb, c * cb, t);
+  for (int bl = 0; bl < cb; bl += 2) {
+    const int b = c * cb + bl;
+    if (bl + 1 < cb) p2_load_b(B1, hB, HBm, pos_g, nb, b + 1, t);
+    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B0, m43, acc);
+    if (bl + 1 < cb) {
+      if (bl + 2 < cb) p2_load_b(B0, hB, HBm, pos_g, nb, b + 2, t);
+      p2_q2k_block(stage + (bl + 1) * Q2K_BB, chunk_bytes, g, t, B1, m43, acc);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// phase 2, shared Q8_0 down: 16 rows over one chunk; B = h limbs (natural order)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb, int c, int g, int t, int Fs,
+                                             const uint16_t* hrow_g,  // hS[tok_g][0][:]
+                                             const float* hs16_0, const float* hs16_1, float (&acc)[4]) {
+  const int chunk_bytes = cb * Q80_BB;
+  // B (both limbs of h) and the 16-row sums of block bl + 1 load while block bl is processed
+  auto load_b = [&](int bq, uint2 (&b)[4], float (&xs2)[2]) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      b[2 * hf] = __ldg(reinterpret_cast<const uint2*>(hrow_g + 32 * bq + 16 * hf + 4 * t));
+      b[2 * hf + 1] = __ldg(reinterpret_cast<const uint2*>(hrow_g + Fs + 32 * bq + 16 * hf + 4 * t));
+    }
+    xs2[0] = hs16_0[2 * bq] + hs16_0[2 * bq + 1];
+    xs2[1] = hs16_1[2 * bq] + hs16_1[2 * bq + 1];
+  };
+  uint2 bcur[4], bnext[4];
+  float xcur[2], xnext[2];
+  load_b(c * cb, bcur, xcur);
+  for (int bl = 0; bl < cb; ++bl) {
+    const int bq = c * cb + bl;
+    if (bl + 1 < cb) load_b(bq + 1, bnext, xnext);
+    float Ph[4], Pl[4];
+    uint32_t dd[2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint2 bh = bcur[2 * hf], blo = bcur[2 * hf + 1];
+      uint32_t l01[2], l23[2], h01[2], h23[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const unsigned char* base = stage + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
+        if (hf == 0) dd[rr] = lds_u16(base);
+        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), l01[rr], l23[rr], h01[rr], h23[rr]);
+      }
+      if (hf == 0) {
+        mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
+        mma_bf16_16816_z(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
+      } else {
+        mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
+        mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
+      }
+      mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], blo.x, blo.y);
+      mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], blo.x, blo.y);
+    }
+    const float x0 = xcur[0], x1 = xcur[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float dv = f16_bits_to_f32(dd[i >> 1]);
+      const float xs = (i & 1) ? x1 : x0;
+      const float v = fmaf(-2304.0f, xs, fmaf(16.0f, Ph[i], Pl[i]));
+      acc[i] = fmaf(dv, v, acc[i]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bcur[q] = bnext[q];
+    xcur[0] = xnext[0];
+    xcur[1] = xnext[1];
   }
 }
 
@@ -527,7 +620,10 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
 // the kernel
 // ----------------------------------------------------------------------------
 template <int PHASE>
-__global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const DecParams p) {
+__global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 1)
+    ffn_decode_kernel(const DecParams p, const __grid_constant__ CUtensorMap map_r0,
+                      const __grid_constant__ CUtensorMap map_r1, const __grid_constant__ CUtensorMap map_s0,
+                      const __grid_constant__ CUtensorMap map_s1) {
   extern __shared__ __align__(128) unsigned char sm[];
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -552,7 +648,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
   const int n_act = *p.n_active;
   const int tiles_s = p.has_shared ? p.rows_s / 16 : 0;
   const int tiles_r = p.rows_r / 16;
-  const int n_items = tiles_s + n_act * tiles_r;
+  const int n_items = (PHASE == 1) ? tiles_s * p.kp_s + n_act * tiles_r * p.kp_r : tiles_s + n_act * tiles_r;
 
   unsigned char* my_stage = stages + warp * NS * STAGE;
   uint64_t* my_bar = bars + warp * NS;
@@ -564,19 +660,48 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
     return i < n_items ? i : -1;
   };
 
-  int queue[NS + 2];
+  // ids of the items whose chunks are issued but not yet consumed (at most NS + 1).  Phase 1
+  // keeps them in three registers (an indexed array would live in local memory); phase 2, at
+  // its register limit, keeps the array (touched once per item).
+  static_assert(NS + 1 <= 3, "item queue holds three ids");
+  int q0 = -1, q1 = -1, q2 = -1, qn = 0;
+  int qarr[4];
   int qh = 0, qt = 0;
+  auto q_push = [&](int v) {
+    if constexpr (PHASE == 1) {
+      if (qn == 0) q0 = v;
+      else if (qn == 1) q1 = v;
+      else q2 = v;
+      ++qn;
+    } else {
+      qarr[qt++ & 3] = v;
+    }
+  };
+  auto q_front = [&]() -> int {
+    if constexpr (PHASE == 1) return q0;
+    else return qarr[qh & 3];
+  };
+  auto q_pop = [&]() {
+    if constexpr (PHASE == 1) {
+      q0 = q1;
+      q1 = q2;
+      --qn;
+    } else {
+      ++qh;
+    }
+  };
   int ld_id = fetch();
-  queue[qt++ % (NS + 2)] = ld_id;
+  q_push(ld_id);
   Item ld_it = decode_item<PHASE>(p, ld_id, n_act, tiles_s, tiles_r);
   int ld_c = 0, ld_seq = 0;
   auto issue_next = [&]() {
     if (ld_it.id < 0) return;
-    issue_chunk<PHASE>(ld_it, ld_c, my_stage + (ld_seq % NS) * STAGE, &my_bar[ld_seq % NS], lane);
+    issue_chunk<PHASE>(ld_it, ld_c, my_stage + (ld_seq % NS) * STAGE, &my_bar[ld_seq % NS], lane,
+                       ld_it.shared ? &map_s0 : &map_r0, ld_it.shared ? &map_s1 : &map_r1);
     ++ld_seq;
-    if (++ld_c == ld_it.C) {
+    if (++ld_c == ld_it.nch) {
       ld_id = fetch();
-      queue[qt++ % (NS + 2)] = ld_id;
+      q_push(ld_id);
       ld_it = decode_item<PHASE>(p, ld_id, n_act, tiles_s, tiles_r);
       ld_c = 0;
     }
@@ -584,7 +709,6 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
   for (int i = 0; i < NS; ++i) issue_next();
 
   // ---- phase 1: the activation package arrives in shared memory by one bulk copy
-  const int T = p.T;
   const int d = p.d;
   const int nbx = d / 256;
   unsigned char* xB = xprep + PL.xB;                                   // [T][xstride]
@@ -602,7 +726,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
   int cs_seq = 0;
   const int Fnb = p.F / 256;
   while (true) {
-    const int id = queue[qh % (NS + 2)];
+    const int id = q_front();
     if (id < 0) break;
     const Item it = decode_item<PHASE>(p, id, n_act, tiles_s, tiles_r);
     const int r0 = it.tile * 16;
@@ -611,16 +735,21 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
       if (col >= it.n) return -1;
       if (it.shared) return col;                                  // token; phase-2 h row of the shared expert
       const int pos = it.off + col;
-      return (PHASE == 1) ? __ldg(p.perm + pos) / p.k : pos;
+      return (PHASE == 1) ? fdiv(__ldg(p.perm + pos), p.fd_k) : pos;
     };
     const int sg = col_src(g), sc0 = col_src(2 * t), sc1 = col_src(2 * t + 1);
+    // data sources: an absent column (>= n) reads column 0's data (or row 0), whose products
+    // land only in that column's outputs, which are never stored; this keeps the inner loops
+    // free of presence tests
+    const int src0 = it.n > 0 ? col_src(0) : 0;
+    const int dg = sg >= 0 ? sg : src0, d0 = sc0 >= 0 ? sc0 : src0, d1 = sc1 >= 0 ? sc1 : src0;
     float acc2[2][4];
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc2[m][i] = 0.0f;
 
-    for (int c = 0; c < it.C; ++c) {
+    for (int cc = 0; cc < it.nch; ++cc) {
       const int st = cs_seq % NS;
       if (!mbar_wait_bounded(&my_bar[st], (cs_seq / NS) & 1, WAIT_LIMIT)) {
         if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
@@ -629,21 +758,40 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
       }
       const unsigned char* stage = my_stage + st * STAGE;
       if (PHASE == 1) {
+        const int m = cc >= it.cpi ? 1 : 0;
+        const int c = it.kp * it.cpi + (cc - m * it.cpi);
+        // one call site per format (the matrix's accumulator is selected into accm), so that
+        // the hot loop's code stays small
+        float accm[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) accm[i] = m ? acc2[1][i] : acc2[0][i];
         if (it.shared) {
-          p1_q80_chunk(stage, it.cb, c, g, t, sg >= 0 ? p.x + (size_t)sg * d : nullptr,
-                       sc0 >= 0 ? X32 + sc0 * (d / 32) : nullptr, sc1 >= 0 ? X32 + sc1 * (d / 32) : nullptr, acc2);
+          const uint16_t* xr = p.x + (size_t)dg * d;
+          const float* x0 = X32 + d0 * (d / 32);
+          const float* x1 = X32 + d1 * (d / 32);
+          p1_q80_mat(stage, it.cb, c, g, t, xr, x0, x1, accm);
         } else {
-          p1_q2k_chunk(stage, it.cb, c, g, t, sg >= 0 ? xB + (size_t)sg * p.xstride : nullptr,
-                       sg >= 0 ? XBm + (size_t)sg * nbx * 96 : nullptr, sc0 >= 0 ? XbM + sc0 * nbx : nullptr,
-                       sc1 >= 0 ? XbM + sc1 * nbx : nullptr, acc2);
+          const unsigned char* xb = xB + (size_t)dg * p.xstride;
+          const unsigned char* xm = XBm + (size_t)dg * nbx * 96;
+          const float* x0 = XbM + d0 * nbx;
+          const float* x1 = XbM + d1 * nbx;
+          if (it.cb == 4)
+            p1_q2k_mat<4>(stage, 4, c, g, t, xb, xm, x0, x1, p.m43, accm);
+          else
+            p1_q2k_mat<0>(stage, it.cb, c, g, t, xb, xm, x0, x1, p.m43, accm);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc2[0][i] = m ? acc2[0][i] : accm[i];
+          acc2[1][i] = m ? accm[i] : acc2[1][i];
         }
       } else {
+        const int c = cc;
         if (it.shared) {
-          p2_q80_chunk(stage, it.cb, c, g, t, p.Fs, sg >= 0 ? p.hS + (size_t)sg * 2 * p.Fs : nullptr,
-                       sc0 >= 0 ? p.HS16 + (size_t)sc0 * (p.Fs / 16) : nullptr,
-                       sc1 >= 0 ? p.HS16 + (size_t)sc1 * (p.Fs / 16) : nullptr, acc2[0]);
+          p2_q80_chunk(stage, it.cb, c, g, t, p.Fs, p.hS + (size_t)dg * 2 * p.Fs, p.HS16 + (size_t)d0 * (p.Fs / 16),
+                       p.HS16 + (size_t)d1 * (p.Fs / 16), acc2[0]);
         } else {
-          p2_q2k_chunk(stage, it.cb, c, Fnb, g, t, sg, p.hB, p.HBm, acc2[0]);
+          p2_q2k_chunk(stage, it.cb, c, Fnb, g, t, dg, p.hB, p.HBm, p.m43, acc2[0]);
         }
       }
       fence_proxy_async_smem();
@@ -651,7 +799,44 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) ffn_decode_kernel(const Dec
       ++cs_seq;
       issue_next();
     }
-    ++qh;
+    q_pop();
+
+    // ---- K-part fix-up: the last part of a tile to finish adds the parts in order 0..KP-1
+    if (PHASE == 1 && it.KP > 1) {
+      // partials of column col: [col source][tile][K part][16 rows]
+      auto part_of = [&](int col) -> float2* {
+        return it.shared ? p.part_s + ((size_t)col * tiles_s + it.tile) * it.KP * 16
+                         : p.part_r + ((size_t)(it.off + col) * tiles_r + it.tile) * it.KP * 16;
+      };
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
+        if (col < it.n) part_of(col)[it.kp * 16 + row] = make_float2(acc2[0][i], acc2[1][i]);
+      }
+      // the warp barrier orders every lane's partial stores before lane 0's release; the
+      // finisher's acquire orders its reads of the other parts after it (then the warp barrier)
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) {
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.tile_cnt + it.slot) : "memory");
+        if (prev == it.KP - 1) p.tile_cnt[it.slot] = 0;   // ready for the next call
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev != it.KP - 1) continue;
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
+        if (col < it.n) {
+          const float2* pc = part_of(col);
+          for (int q = 0; q < it.KP; ++q) {
+            const float2 v = __ldcg(pc + q * 16 + row);
+            acc2[0][i] = q == 0 ? v.x : acc2[0][i] + v.x;
+            acc2[1][i] = q == 0 ? v.y : acc2[1][i] + v.y;
+          }
+        }
+      }
+    }
 
     // ---- epilogue
     if (PHASE == 1) {
@@ -738,18 +923,66 @@ int pick_chunk(int nb, int bb, int cap_per_mat, int align_blocks, int* whole) {
   return cb;
 }
 
+// Phase-1 K parts per tile: routed tiles split into one item per chunk; shared (Q8_0) tiles
+// into at most 4 parts (a divisor of their chunk count).
+void phase1_kparts(int d, bool has_shared, int* kpr, int* kps) {
+  int whole = 0;
+  const int cbr = pick_chunk(d / 256, Q2K_BB, STAGE, 4, &whole);
+  *kpr = cbr > 0 ? (d / 256) / cbr : 1;
+  *kps = 1;
+  if (has_shared) {
+    const int cbs = pick_chunk(d / 32, Q80_BB, STAGE, 8, &whole);
+    const int Cs = cbs > 0 ? (d / 32) / cbs : 1;
+    for (int q = Cs < 4 ? Cs : 4; q >= 1; --q)
+      if (Cs % q == 0) {
+        *kps = q;
+        break;
+      }
+  }
+}
+
+}  // namespace
+
+// 1 KB of work counters, then one K-part counter per phase-1 tile of the largest decode batch
+// (shared tiles + DECODE_T_MAX * k routed pairs' tiles).
+size_t ffn_reserved_bytes(int k, int F, int Fs) {
+  const size_t slots = (size_t)Fs / 16 + (size_t)DECODE_T_MAX * k * (F / 16);
+  return 1024 + ((slots * 4 + 255) & ~(size_t)255);
+}
+
+namespace {
+
+// Workspace of the decode path, in order.
+struct DecWs {
+  size_t pkg, hB, HBm, hS, HS16, cnt, part_r, part_s, total;
+};
+
+DecWs dec_ws_layout(int T, int k, int d, int F, int Fs) {
+  const size_t P = (size_t)T * k;
+  int kpr = 1, kps = 1;
+  phase1_kparts(d, Fs > 0, &kpr, &kps);
+  auto up256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  DecWs w;
+  w.cnt = 1024;                                                  // after the work counters
+  w.pkg = ffn_reserved_bytes(k, F, Fs);
+  w.hB = up256(w.pkg + pkg_layout(T, d).total);
+  w.HBm = up256(w.hB + P * (F / 256) * 512 * 2);
+  w.hS = up256(w.HBm + P * (F / 256) * 4 * 12 * 2);
+  w.HS16 = up256(w.hS + (size_t)T * 2 * Fs * 2);
+  w.part_r = up256(w.HS16 + (size_t)T * (Fs / 16) * 4);
+  w.part_s = up256(w.part_r + P * (F / 16) * kpr * 16 * 8);
+  w.total = up256(w.part_s + (size_t)T * (Fs / 16) * kps * 16 * 8);
+  return w;
+}
+
 }  // namespace
 
 size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs) {
   (void)E;
-  if (T > DECODE_T_MAX) return ffn_gemm_ws_bytes(T, k, d, F, Fs);
-  const size_t P = (size_t)T * k;
-  size_t s = 1024 + pkg_layout(T, d).total;              // counters, activation package
-  s += P * (F / 256) * 512 * 2;                          // hB
-  s += P * (F / 256) * 4 * 12 * 2;                       // HBm
-  s += (size_t)T * 2 * Fs * 2;                           // hS
-  s += (size_t)T * (Fs / 16) * 4;                        // HS16
-  return (s + 255) & ~(size_t)255;
+  // monotone in T: a workspace sized for T also serves every smaller batch (either path)
+  if (T > DECODE_T_MAX)
+    return std::max(ffn_gemm_ws_bytes(T, k, d, F, Fs), dec_ws_layout(DECODE_T_MAX, k, d, F, Fs).total);
+  return dec_ws_layout(T, k, d, F, Fs).total;
 }
 
 bre_status ffn_check_shapes(const bre_ffn_weights* r, const bre_ffn_weights* sh, int T) {
@@ -757,12 +990,49 @@ bre_status ffn_check_shapes(const bre_ffn_weights* r, const bre_ffn_weights* sh,
   if (d <= 0 || F <= 0 || d % 256 || F % 256) return BRE_ERR_UNSUPPORTED;
   if (sh && (sh->d != d || sh->d_ff <= 0 || sh->d_ff % 256)) return BRE_ERR_UNSUPPORTED;
   if (T <= DECODE_T_MAX) {
-    // Q2_K rows go to shared memory by 16-byte aligned bulk copies: whole 16-row tiles when
-    // they fit a stage, otherwise 4-block (336-byte) pieces of rows a multiple of 4 blocks long
+    // Q2_K rows go to shared memory as whole 16-row tiles when a tile fits a stage (rows of at
+    // most 4 blocks), otherwise as tensor copies of 4-block (336-byte) pieces, which needs rows
+    // a multiple of 4 blocks long (16-byte row pitch)
     if (!(d <= 1024 || d % 1024 == 0)) return BRE_ERR_UNSUPPORTED;
-    if (!(F <= 2048 || F % 1024 == 0)) return BRE_ERR_UNSUPPORTED;
+    if (!(F <= 1024 || F % 1024 == 0)) return BRE_ERR_UNSUPPORTED;
   }
   return BRE_OK;
+}
+
+// Tensor map over quantised expert matrices viewed as 32-bit words, [experts][rows][row words],
+// box = (chunk words, 16 rows, 1 expert).  Encodings are cached: decode calls repeat the same
+// few maps, and an encode costs host time on every call.
+static bool weight_map(CUtensorMap* m, const void* base, int n_exp, long long exp_stride, int rows, int row_bytes,
+                       int chunk_bytes) {
+  struct Entry {
+    const void* base;
+    long long n_exp, exp_stride, rows, row_bytes, chunk_bytes;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int n_cached = 0, next = 0;
+  if (n_exp <= 1 || exp_stride <= 0) exp_stride = (long long)rows * row_bytes;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cached; ++i) {
+    const Entry& c = cache[i];
+    if (c.base == base && c.n_exp == n_exp && c.exp_stride == exp_stride && c.rows == rows &&
+        c.row_bytes == row_bytes && c.chunk_bytes == chunk_bytes) {
+      *m = c.map;
+      return true;
+    }
+  }
+  const uint64_t dims[3] = {(uint64_t)(row_bytes / 4), (uint64_t)rows, (uint64_t)(n_exp > 0 ? n_exp : 1)};
+  const uint64_t strides[2] = {(uint64_t)row_bytes, (uint64_t)exp_stride};
+  const uint32_t box[3] = {(uint32_t)(chunk_bytes / 4), 16u, 1u};
+  if (row_bytes % 16 || chunk_bytes % 16 || exp_stride % 16) return false;
+  if (!encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return false;
+  Entry& slot = cache[next];
+  slot = Entry{base, n_exp, exp_stride, rows, row_bytes, chunk_bytes, *m};
+  next = (next + 1) % 32;
+  if (n_cached < 32) ++n_cached;
+  return true;
 }
 
 static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
@@ -784,31 +1054,34 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   p.y_pairs = a.y_pairs;
   p.y_shared = a.y_shared;
   p.err = a.err;
-  const size_t P = (size_t)a.T * a.k;
   char* w = reinterpret_cast<char*>(a.ws);
+  const DecWs L = dec_ws_layout(a.T, a.k, p.d, p.F, p.Fs);
   p.counters = reinterpret_cast<int*>(w);
-  w += 1024;
-  p.pkg = reinterpret_cast<const unsigned char*>(w);
-  unsigned char* pkg_w = reinterpret_cast<unsigned char*>(w);
-  w += pkg_layout(a.T, p.d).total;
-  p.hB = reinterpret_cast<uint16_t*>(w);
-  w += P * (p.F / 256) * 512 * 2;
-  p.HBm = reinterpret_cast<uint16_t*>(w);
-  w += P * (p.F / 256) * 4 * 12 * 2;
-  p.hS = reinterpret_cast<uint16_t*>(w);
-  w += (size_t)a.T * 2 * p.Fs * 2;
-  p.HS16 = reinterpret_cast<float*>(w);
+  p.pkg = reinterpret_cast<const unsigned char*>(w + L.pkg);
+  unsigned char* pkg_w = reinterpret_cast<unsigned char*>(w + L.pkg);
+  p.hB = reinterpret_cast<uint16_t*>(w + L.hB);
+  p.HBm = reinterpret_cast<uint16_t*>(w + L.HBm);
+  p.hS = reinterpret_cast<uint16_t*>(w + L.hS);
+  p.HS16 = reinterpret_cast<float*>(w + L.HS16);
+  p.tile_cnt = reinterpret_cast<int*>(w + L.cnt);
+  p.part_r = reinterpret_cast<float2*>(w + L.part_r);
+  p.part_s = reinterpret_cast<float2*>(w + L.part_s);
+  phase1_kparts(p.d, S != nullptr, &p.kp_r, &p.kp_s);
   p.xstride = p.d * 2 + 32;
+  p.m43 = 0x43004300u;
 
   const int sms = device_sm_count();
   const int smem_max = device_max_smem_optin();
-  ffn_prep_kernel<<<dim3(p.d / 256, a.T), 256, 0, s>>>(a.x, a.T, p.d, pkg_w);
+  const dim3 prep_grid(p.d / 256, a.T);
+  {
+    const cudaError_t le = launch_k(ffn_prep_kernel, dim3(prep_grid), dim3(256), 0, s, a.x, a.T, p.d, pkg_w);
+    if (le != cudaSuccess) return le;
+  }
   {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   for (int phase = 1; phase <= 2; ++phase) {
-    const int cap = (phase == 1) ? STAGE / 2 : STAGE;
     if (phase == 1) {
       p.rw0 = static_cast<const uint8_t*>(R->gate);
       p.rw1 = static_cast<const uint8_t*>(R->up);
@@ -832,11 +1105,36 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
       p.nb_r = p.F / 256;
       p.nb_s = p.Fs / 32;
     }
-    p.cb_r = pick_chunk(p.nb_r, Q2K_BB, cap, 4, &p.whole_r);
-    p.cb_s = S ? pick_chunk(p.nb_s, Q80_BB, cap, 8, &p.whole_s) : 1;
+    p.cb_r = pick_chunk(p.nb_r, Q2K_BB, STAGE, 4, &p.whole_r);
+    p.cb_s = S ? pick_chunk(p.nb_s, Q80_BB, STAGE, 8, &p.whole_s) : 1;
     if (p.cb_r <= 0 || p.cb_s <= 0) return cudaErrorInvalidValue;
+    p.C_r = p.nb_r / p.cb_r;
+    p.C_s = S ? p.nb_s / p.cb_s : 1;
+    {
+      const int kpr = phase == 1 ? p.kp_r : 1, kps = phase == 1 ? p.kp_s : 1;
+      p.fd_kpr = make_fdiv(kpr);
+      p.fd_kps = make_fdiv(kps);
+      p.fd_trk = make_fdiv((unsigned)(p.rows_r / 16 * kpr));
+      p.fd_k = make_fdiv((unsigned)a.k);
+      p.cpi_r = p.C_r / kpr;
+      p.cpi_s = p.C_s / kps;
+      if (p.cpi_r * kpr != p.C_r || p.cpi_s * kps != p.C_s) return cudaErrorInvalidValue;
+    }
+    // tensor maps for chunked rows (unused when whole tiles fit a stage)
+    CUtensorMap mr0{}, mr1{}, ms0{}, ms1{};
+    if (!p.whole_r) {
+      if (!weight_map(&mr0, p.rw0, R->n_experts, p.rs0, p.rows_r, p.nb_r * Q2K_BB, p.cb_r * Q2K_BB)) return cudaErrorInvalidValue;
+      if (phase == 1 &&
+          !weight_map(&mr1, p.rw1, R->n_experts, p.rs1, p.rows_r, p.nb_r * Q2K_BB, p.cb_r * Q2K_BB))
+        return cudaErrorInvalidValue;
+    }
+    if (S && !p.whole_s) {
+      if (!weight_map(&ms0, p.sw0, 1, 0, p.rows_s, p.nb_s * Q80_BB, p.cb_s * Q80_BB)) return cudaErrorInvalidValue;
+      if (phase == 1 && !weight_map(&ms1, p.sw1, 1, 0, p.rows_s, p.nb_s * Q80_BB, p.cb_s * Q80_BB))
+        return cudaErrorInvalidValue;
+    }
     const size_t xbytes = (phase == 1) ? (size_t)pkg_layout(a.T, p.d).total : 0;
-    int nw = MAX_WARPS;
+    int nw = (phase == 1) ? MAX_WARPS : MAX_WARPS_P2;
     while (nw > 1 && (size_t)nw * NS * STAGE + BAR_BYTES + xbytes > (size_t)smem_max) --nw;
     const size_t smem = (size_t)nw * NS * STAGE + BAR_BYTES + xbytes;
     if (smem > (size_t)smem_max) return cudaErrorInvalidValue;
@@ -844,11 +1142,19 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     if (phase == 1) {
       e = cudaFuncSetAttribute(ffn_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      ffn_decode_kernel<1><<<sms, nw * 32, smem, s>>>(p);
+      {
+        const cudaError_t le = launch_k(ffn_decode_kernel<1>, dim3(sms), dim3(nw * 32), smem, s, p, mr0, mr1, ms0,
+                                        ms1);
+        if (le != cudaSuccess) return le;
+      }
     } else {
       e = cudaFuncSetAttribute(ffn_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      ffn_decode_kernel<2><<<sms, nw * 32, smem, s>>>(p);
+      {
+        const cudaError_t le = launch_k(ffn_decode_kernel<2>, dim3(sms), dim3(nw * 32), smem, s, p, mr0, mr1, ms0,
+                                        ms1);
+        if (le != cudaSuccess) return le;
+      }
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -46,13 +46,17 @@ struct Plan {
 
 __global__ void plan_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ active,
                             const int32_t* __restrict__ n_active, int has_shared, int T, int P, int nt1_r, int nt1_s,
-                            int nt2, Plan* plan) {
+                            int nt2, int E, int32_t* err, Plan* plan) {
   pdl_wait();
   if (threadIdx.x != 0) return;
-  const int na = *n_active;
+  const int na = min(*n_active, G_MAX_GROUPS - 1);
   int g = 0, t1 = 0, t2 = 0;
-  for (int a = 0; a < na; ++a, ++g) {
+  for (int a = 0; a < na; ++a) {
     const int e = active[a];
+    if ((unsigned)e >= (unsigned)E) {   // an expert the weights do not hold: its pairs stay zero
+      set_err(err, BRE_DEVERR_EXPERT_ID);
+      continue;
+    }
     const int off = offsets[e], n = offsets[e + 1] - off;
     const int mt = (n + G_BM - 1) / G_BM;
     plan->a_row0[g] = off;
@@ -62,6 +66,7 @@ __global__ void plan_kernel(const int32_t* __restrict__ offsets, const int32_t* 
     plan->tile2[g] = t2;
     t1 += mt * nt1_r;
     t2 += mt * nt2;
+    ++g;
   }
   if (has_shared) {
     const int mt = (T + G_BM - 1) / G_BM;
@@ -167,13 +172,21 @@ struct RawQ2K {
   uint32_t sw, dd, q[4];
 };
 
-__device__ __forceinline__ void load_raw_q2k(const uint8_t* row, int ks, RawQ2K& r) {
-  const uint8_t* blk = row + (ks >> 2) * Q2K_BB;
-  const int j0 = (ks & 3) * 4;
-  r.sw = __ldg(reinterpret_cast<const uint32_t*>(blk + j0));
-  r.dd = __ldg(reinterpret_cast<const uint32_t*>(blk + 80));
+// A whole Q2_K block of one row (21 words: scales, codes, d and dmin); the producers hold the
+// next block while dequantising the current one, so the load has four K steps to land.
+struct RawBlk {
+  uint32_t w[21];
+};
+
+
+// The quarter kq (64 values, sub-blocks 4kq .. 4kq+3) of a held block.
+__device__ __forceinline__ RawQ2K quarter(const RawBlk& b, int kq) {
+  RawQ2K r;
+  r.sw = b.w[kq];
+  r.dd = b.w[20];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) r.q[jj] = __ldg(reinterpret_cast<const uint32_t*>(blk + 16 + 4 * (j0 + jj)));
+  for (int jj = 0; jj < 4; ++jj) r.q[jj] = b.w[4 + 4 * kq + jj];
+  return r;
 }
 
 // 4-entry BF16 table of one sub-block: value of code q is bf16_rne((d*sc)*q - dmin*m).
@@ -313,6 +326,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   uint64_t* tempty = tfull + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  unsigned char* stage_raw = reinterpret_cast<unsigned char*>(full) + 256;   // [4 warps][64 rows][84 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
@@ -378,23 +392,58 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           rowA = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + i) * rb;
           rowB = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + 128 + i) * rb;
         }
-        RawQ2K ca, cb, na, nb;
-        load_raw_q2k(rowA, 0, ca);
-        load_raw_q2k(rowB, 0, cb);
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          if (ks + 1 < KS) {
-            load_raw_q2k(rowA, ks + 1, na);
-            load_raw_q2k(rowB, ks + 1, nb);
+        // Whole blocks (4 K steps each) reach the warp's staging area by coalesced copies: lanes
+        // 0..20 copy the 21 words of one row per instruction (a row pointer that advances by the
+        // row pitch), 64 rows per warp.  Each thread then reads its two rows into registers, and
+        // the copy of the next block runs while this one is dequantised.
+        const int NBK = KS / 4;
+        const int pw = warp - 4;
+        unsigned char* stg = stage_raw + pw * 64 * Q2K_BB;
+        const uint8_t* pa0 = rowA - (long long)lane * rb + 4 * lane;   // row 32*pw of the A set
+        const uint8_t* pb0 = rowB - (long long)lane * rb + 4 * lane;   // row 32*pw of the B set
+        auto stage_copy = [&](int blk) {
+          if (lane < 21) {
+            const uint8_t* pa = pa0 + blk * Q2K_BB;
+            const uint8_t* pb = pb0 + blk * Q2K_BB;
+            unsigned char* dst = stg + 4 * lane;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) cp_async4(dst + r * Q2K_BB, pa + (long long)r * rb, 4);
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) cp_async4(dst + (32 + r) * Q2K_BB, pb + (long long)r * rb, 4);
           }
-          const int s = it % G_STAGES;
-          if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) { fail(); break; }
-          store_q2k_row(ca, b_st + s * G_B_BYTES, i);
-          store_q2k_row(cb, b_st + s * G_B_BYTES, i + 128);
-          fence_proxy_async_smem();
-          mbar_arrive(&full[s]);
-          ca = na;
-          cb = nb;
+          cp_async_commit();
+        };
+        auto stage_read = [&](RawBlk& a, RawBlk& b) {
+          cp_async_wait<0>();
+          __syncwarp();
+#pragma unroll
+          for (int w = 0; w < 21; ++w) {
+            a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * Q2K_BB + 4 * w);
+            b.w[w] = *reinterpret_cast<const uint32_t*>(stg + (32 + lane) * Q2K_BB + 4 * w);
+          }
+          __syncwarp();
+        };
+        RawBlk ca, cb;
+        stage_copy(0);
+        bool ok = true;
+        for (int bk = 0; bk < NBK && ok; ++bk) {
+          stage_read(ca, cb);
+          if (bk + 1 < NBK) stage_copy(bk + 1);
+#pragma unroll
+          for (int kq = 0; kq < 4; ++kq, ++it) {
+            const int s = it % G_STAGES;
+            if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) {
+              fail();
+              ok = false;
+              break;
+            }
+            store_q2k_row(quarter(ca, kq), b_st + s * G_B_BYTES, i);
+            store_q2k_row(quarter(cb, kq), b_st + s * G_B_BYTES, i + 128);
+            fence_proxy_async_smem();
+            mbar_arrive(&full[s]);
+          }
         }
+        cp_async_wait<0>();   // no copy stays in flight past the tile
       } else {
         const int rb = (p.K_s / 32) * Q80_BB;
         if (PHASE == 1) {
@@ -404,16 +453,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           rowA = p.s0 + (long long)(ti.nt * 256 + i) * rb;
           rowB = p.s0 + (long long)(ti.nt * 256 + 128 + i) * rb;
         }
-        RawQ80 ca, cb;
+        RawQ80 ca, cb, na, nb;
+        load_raw_q80(rowA, 0, ca);
+        load_raw_q80(rowB, 0, cb);
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          load_raw_q80(rowA, ks, ca);
-          load_raw_q80(rowB, ks, cb);
+          if (ks + 1 < KS) {   // one K step ahead
+            load_raw_q80(rowA, ks + 1, na);
+            load_raw_q80(rowB, ks + 1, nb);
+          }
           const int s = it % G_STAGES;
           if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) { fail(); break; }
           store_q80_row(ca, b_st + s * G_B_BYTES, i);
           store_q80_row(cb, b_st + s * G_B_BYTES, i + 128);
           fence_proxy_async_smem();
           mbar_arrive(&full[s]);
+          ca = na;
+          cb = nb;
         }
       }
     }
@@ -505,41 +560,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
 // 2-D BF16 tensor [rows][K], box 64 x 128, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, long long rows, int K) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)(rows > 0 ? rows : 1)};
+  const uint64_t strides[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {64, 128};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
 
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
-  // the first 1 KB stays with the decode path's work counters, which must keep their zeros
-  size_t s = 1024 + ((sizeof(Plan) + 1023) & ~(size_t)1023);
+  // the reserved prefix stays with the decode path's counters, which must keep their zeros
+  size_t s = ffn_reserved_bytes(k, F, Fs) + ((sizeof(Plan) + 1023) & ~(size_t)1023);
   s += ((P + T) * d * 2 + 1023) & ~(size_t)1023;     // gathered activations
   s += (P * F * 2 + 1023) & ~(size_t)1023;           // routed intermediate
   s += ((size_t)T * Fs * 2 + 1023) & ~(size_t)1023;  // shared intermediate
@@ -551,7 +585,7 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   const bre_ffn_weights* S = a.shared;
   const int T = a.T, k = a.k, d = R->d, F = R->d_ff, Fs = S ? S->d_ff : 0, E = R->n_experts;
   const size_t P = (size_t)T * k;
-  char* w = static_cast<char*>(a.ws) + 1024;
+  char* w = static_cast<char*>(a.ws) + ffn_reserved_bytes(k, F, Fs);
   Plan* plan = reinterpret_cast<Plan*>(w);
   w += (sizeof(Plan) + 1023) & ~(size_t)1023;
   uint16_t* xp = reinterpret_cast<uint16_t*>(w);
@@ -560,14 +594,22 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   w += (P * F * 2 + 1023) & ~(size_t)1023;
   uint16_t* h_s = reinterpret_cast<uint16_t*>(w);
 
-  plan_kernel<<<1, 32, 0, s>>>(a.offsets, a.active, a.n_active, S ? 1 : 0, T, (int)P, F / 128, Fs / 128, d / 256, plan);
+  {
+    const cudaError_t le = launch_k(plan_kernel, dim3(1), dim3(32), 0, s, a.offsets, a.active, a.n_active,
+                                    S ? 1 : 0, T, (int)P, F / 128, Fs / 128, d / 256, E, a.err, plan);
+    if (le != cudaSuccess) return le;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
-  gather_kernel<<<sms * 4, 256, 0, s>>>(a.x, a.perm, a.offsets, E, k, T, (int)P, d, xp, S ? 1 : 0);
+  {
+    const cudaError_t le = launch_k(gather_kernel, dim3(sms * 4), dim3(256), 0, s, a.x, a.perm, a.offsets, E, k, T,
+                                    (int)P, d, xp, S ? 1 : 0);
+    if (le != cudaSuccess) return le;
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const size_t smem = G_STAGES * (G_A_BYTES + G_B_BYTES) + 1024 + 256;
+  const size_t smem = G_STAGES * (G_A_BYTES + G_B_BYTES) + 1024 + 256 + 4 * 64 * Q2K_BB;
   static int configured = -1;
   int dev;
   cudaGetDevice(&dev);
@@ -606,7 +648,10 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   g.h_s = h_s;
   g.out_ld_r = F;
   g.out_ld_s = Fs;
-  ffn_gemm_kernel<1><<<sms, G_THREADS, smem, s>>>(m_x, m_x, g);
+  {
+    const cudaError_t le = launch_k(ffn_gemm_kernel<1>, dim3(sms), dim3(G_THREADS), smem, s, m_x, m_x, g);
+    if (le != cudaSuccess) return le;
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // phase 2: down -> y
   g.r0 = static_cast<const uint8_t*>(R->down);
@@ -625,7 +670,10 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   g.y_s = a.y_shared;
   g.out_ld_r = d;
   g.out_ld_s = d;
-  ffn_gemm_kernel<2><<<sms, G_THREADS, smem, s>>>(m_hr, m_hs, g);
+  {
+    const cudaError_t le = launch_k(ffn_gemm_kernel<2>, dim3(sms), dim3(G_THREADS), smem, s, m_hr, m_hs, g);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // Internal launcher declarations of libbre (host side).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,9 @@ struct FfnArgs {
   int32_t* err;
 };
 constexpr int DECODE_T_MAX = 8;   // larger batches take the grouped-GEMM path
+// Leading bytes of the FFN workspace that hold the decode path's counters; they keep their
+// zeros between calls whatever T, so both paths place everything else after them.
+size_t ffn_reserved_bytes(int k, int F, int Fs);
 size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs);
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs);
 bre_status ffn_check_shapes(const bre_ffn_weights* routed, const bre_ffn_weights* shared, int T);
@@ -51,6 +55,30 @@ cudaError_t launch_combine(const float* y_pairs, const float* topk_w, const int3
 cudaError_t launch_residual_norm(const uint16_t* x, const uint16_t* moe, int T, int d, float scale, float eps,
                                  uint16_t* x_out, uint16_t* u_out, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t n_blocks, float* out, cudaStream_t s);
+
+// tiled tensor map over global memory: dims innermost first, strides (bytes) of dims 1..rank-1
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Launch with programmatic dependent launch allowed (unless BRE_PDL=0 in the environment): the
+// kernel may be scheduled while the previous kernel on the stream drains, so every kernel
+// launched this way calls pdl_wait() before it reads another kernel's results or writes
+// memory an earlier kernel may still read.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // device attributes (cached per device)
 int device_sm_count();

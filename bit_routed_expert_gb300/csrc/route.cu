@@ -11,6 +11,8 @@
 // bit for bit: 32 partial sums, partial j takes fmaf over rows c = j, j+32, ... in
 // ascending order starting from +0, then a butterfly p_j + p_(j^o) for
 // o = 16, 8, 4, 2, 1.  Any thread mapping computes exactly this.
+#include <algorithm>
+
 #include "bre_common.cuh"
 #include "kernels.h"
 
@@ -18,9 +20,7 @@ namespace bre {
 
 namespace {
 
-constexpr int SMALL_TT = 8;      // tokens per CTA, small-batch logits
-constexpr int SMALL_ET = 4;      // experts per CTA, small-batch logits
-constexpr int SMALL_THREADS = SMALL_ET * 32;
+constexpr int SMALL_TT = 8;      // tokens per token group, small-batch logits
 constexpr int TILE_T = 32;       // tokens per CTA, tiled logits
 constexpr int TILE_E = 32;       // experts per CTA, tiled logits
 constexpr int SMALL_T_MAX = 32;  // up to this many tokens use the small-batch kernel
@@ -64,13 +64,15 @@ __device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib)
   return ia < ib;
 }
 
-// One warp selects the top k of the E scores of one token and writes ids and weights.
+// One warp selects the top k of the E scores of one token and writes ids and weights; lane l
+// holds scores l, l+32, ... (NI >= ceil(E/32) of them, a compile-time count).
+template <int NI>
 __device__ void topk_warp(const float* __restrict__ s_row, const float* __restrict__ bias, int E, int k,
                           int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
   const int lane = threadIdx.x & 31;
-  float sv[32], kv[32];
+  float sv[NI], kv[NI];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
       sv[i] = __ldcg(s_row + e);
@@ -87,7 +89,7 @@ __device__ void topk_warp(const float* __restrict__ s_row, const float* __restri
     float bk = 0.0f, bs = 0.0f;
     int bid = -1;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NI; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((used >> i) & 1u)) {
         if (bid < 0 || ranks_before(kv[i], e, bk, bid)) {
@@ -138,153 +140,317 @@ __device__ void topk_warp(const float* __restrict__ s_row, const float* __restri
   }
 }
 
-// Small batches: CTA = up to SMALL_TT tokens x SMALL_ET experts, all 32 partials.
-// Thread (e_l = tid % SMALL_ET, j = tid / SMALL_ET) runs the fmaf chain of partial j of expert e_l
-// for every token of the CTA.  With NI = d/32 known at compile time every W_r load of the
-// thread is issued before the first FMA (one memory round trip); x is staged once as FP32,
-// transposed to [c][token], so one row costs two 16-byte shared loads.  The last CTA to
-// finish selects the top k of every token.
-template <int NI>
-__global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(const uint16_t* __restrict__ x,
-                                                          const float* __restrict__ w_r,
-                                                          const float* __restrict__ bias, int T, int d, int E,
-                                                          int k, float* __restrict__ S, int* ticket,
-                                                          int32_t* __restrict__ ids, float* __restrict__ wts) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* xs = reinterpret_cast<float*>(smem_raw);                                    // [d][TT]
-  float* part = reinterpret_cast<float*>(smem_raw + (size_t)SMALL_TT * d * 4);      // [TT][32][ET]
-  __shared__ int is_last;
-  pdl_wait();
-  const int tid = threadIdx.x;
-  const int e0 = blockIdx.x * SMALL_ET;
-  const int t0 = blockIdx.y * SMALL_TT;
-  const int nt = min(SMALL_TT, T - t0);
-  const int e_l = tid % SMALL_ET, j = tid / SMALL_ET;
-  const int e = e0 + e_l;
-  const float* wcol = w_r + (e < E ? e : 0);
-  float wv[NI > 0 ? NI : 1];
-  if (NI > 0) {
-#pragma unroll
-    for (int i = 0; i < NI; ++i) wv[i] = (e < E) ? __ldg(wcol + (size_t)(j + 32 * i) * E) : 0.0f;
-  }
-  // token index fastest across threads: the eight stores of a row land in eight consecutive words
-#pragma unroll 8
-  for (int i = tid; i < SMALL_TT * d / 8; i += SMALL_THREADS) {
-    const int tt = i % SMALL_TT, c = (i / SMALL_TT) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (tt < nt) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + c));
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      xs[(c + 2 * q) * SMALL_TT + tt] = bf16_bits_to_f32(w4[q] & 0xFFFFu);
-      xs[(c + 2 * q + 1) * SMALL_TT + tt] = bf16_bits_to_f32(w4[q] >> 16);
+// Small batches (decode): one warp per (partial j, block of 32 experts), lane = expert.  A
+// CTA holds four consecutive j; the eight CTAs that hold j = 0..31 of one expert block form
+// a cluster and add their partials in the butterfly order through distributed shared memory.
+// The CTA's W_r slice (rows c = j (mod 32) of its 32 experts) is copied to shared memory
+// with cp.async (coalesced 128-byte rows, all in flight at once, issued before the wait on
+// the producing kernel: W_r is a weight); x is staged once as FP32 in [j][i][token] order.
+// Every loop stays rolled: each SM runs this code once, so its size, not its arithmetic,
+// would set the time.  Each cluster then selects a local top k of its 32 experts per token;
+// the last block to deliver a token's candidates merges them (the global top k of a token is
+// contained in the union of the per-block top k).
+constexpr int RC_J = 4;                   // partials (warps) per CTA
+constexpr int RC_CLUSTER = 32 / RC_J;     // CTAs per cluster
+constexpr int RC_THREADS = RC_J * 32;
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// Warp arg-best of one candidate per lane: the (key, id) that ranks first among lanes with has.
+// Returns the winner's id (0x7FFFFFFF when no lane has a candidate) and its key.
+__device__ __forceinline__ int warp_best(float key, int id, bool has, float& wkey) {
+  float wk = key;
+  int wid = has ? id : 0x7FFFFFFF;
+  bool wh = has;
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ok = __shfl_xor_sync(0xffffffffu, wk, o);
+    const int oid = __shfl_xor_sync(0xffffffffu, wid, o);
+    const bool oh = __shfl_xor_sync(0xffffffffu, (int)wh, o) != 0;
+    bool take;
+    if (wh != oh)
+      take = oh;
+    else if (!wh)
+      take = oid < wid;
+    else
+      take = ranks_before(ok, oid, wk, wid);
+    if (take) {
+      wk = ok;
+      wid = oid;
+      wh = oh;
     }
   }
+  wkey = wk;
+  return wid;
+}
+
+// Candidates of one token: kc slots per expert block, (s, id) with id = -1 for an empty slot.
+__host__ __device__ __forceinline__ int rc_slots(int E, int k) { return ((E + 31) / 32) * (k < 32 ? k : 32); }
+
+__global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
+    route_cluster_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w_r,
+                         const float* __restrict__ bias, int T, int d, int E, int k, float* __restrict__ cand_k,
+                         float* __restrict__ cand_s, int* __restrict__ cand_id, int* tickets,
+                         int32_t* __restrict__ ids, float* __restrict__ wts) {
+  extern __shared__ __align__(16) float rc_smem[];
+  __shared__ float part[SMALL_TT][RC_J][33];     // partial sums of this CTA's j, padded
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = d / 32;
+  float* Ws = rc_smem;                           // [n][RC_J][32]
+  float* xs = rc_smem + (size_t)n * RC_J * 32;   // [RC_J][n][SMALL_TT]
+  const int e = blockIdx.x * 32 + lane;
+  const int jb = blockIdx.y;                     // j block = rank in the cluster
+  const int j = jb * RC_J + warp;
+  const int t0 = blockIdx.z * SMALL_TT;
+  const int nt = min(SMALL_TT, T - t0);
+  const int kc = min(k, 32);
+  const int slots = rc_slots(E, k);
+  if ((E & 3) == 0) {
+    // 16-byte pieces: row (i, jj) of the slice is 8 pieces of the W_r row 32 i + RC_J jb + jj
+    for (int q = tid; q < n * RC_J * 8; q += RC_THREADS) {
+      const int pc = q & 7, row = q >> 3;           // row = i * RC_J + jj
+      const int i = row / RC_J, jj = row % RC_J;
+      const int ee = blockIdx.x * 32 + pc * 4;
+      const bool ok = ee < E;
+      const float* src = ok ? w_r + (size_t)(32 * i + jb * RC_J + jj) * E + ee : w_r;
+      cp_async16(Ws + (size_t)row * 32 + pc * 4, src, ok ? 16 : 0);
+    }
+  } else {
+    const float* src = w_r + (size_t)j * E + (e < E ? e : 0);
+    const size_t rstride = (size_t)32 * E;
+    float* dst = Ws + warp * 32 + lane;
+    for (int i = 0; i < n; ++i) cp_async4(dst + (size_t)i * RC_J * 32, src + i * rstride, e < E ? 4 : 0);
+  }
+  pdl_wait();
+  // stage x: item q = (i, tt) reads the RC_J values x[t0+tt][32 i + RC_J jb ...] (8 bytes)
+  for (int q = tid; q < n * SMALL_TT; q += RC_THREADS) {
+    const int tt = q & (SMALL_TT - 1), i = q / SMALL_TT;
+    uint2 v = make_uint2(0u, 0u);
+    if (tt < nt) v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * d + 32 * i + RC_J * jb));
+    xs[(0 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.x & 0xFFFFu);
+    xs[(1 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.x >> 16);
+    xs[(2 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.y & 0xFFFFu);
+    xs[(3 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.y >> 16);
+  }
+  cp_async_wait_all();
   __syncthreads();
+  // partial j of expert e: rows c = j + 32 i in ascending i, fmaf from +0
   float acc[SMALL_TT];
 #pragma unroll
   for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = 0.0f;
-  auto fma_row = [&](int c, float wgt) {
-    const float4* xp = reinterpret_cast<const float4*>(xs + c * SMALL_TT);
-    const float4 a = xp[0], b = xp[1];
-    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const float4* xw = reinterpret_cast<const float4*>(xs + (size_t)warp * n * SMALL_TT);
+  const float* wp = Ws + warp * 32 + lane;
+#pragma unroll 4
+  for (int i = 0; i < n; ++i) {
+    const float wgt = wp[(size_t)i * RC_J * 32];
+    const float4 a = xw[2 * i], b = xw[2 * i + 1];
+    acc[0] = fmaf(a.x, wgt, acc[0]);
+    acc[1] = fmaf(a.y, wgt, acc[1]);
+    acc[2] = fmaf(a.z, wgt, acc[2]);
+    acc[3] = fmaf(a.w, wgt, acc[3]);
+    acc[4] = fmaf(b.x, wgt, acc[4]);
+    acc[5] = fmaf(b.y, wgt, acc[5]);
+    acc[6] = fmaf(b.z, wgt, acc[6]);
+    acc[7] = fmaf(b.w, wgt, acc[7]);
+  }
 #pragma unroll
-    for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = fmaf(xv[tt], wgt, acc[tt]);
-  };
-  if (NI > 0) {
+  for (int tt = 0; tt < SMALL_TT; ++tt) part[tt][warp][lane] = acc[tt];
+  cluster_sync_all();
+  // CTA of rank r adds the 32 partials of token t0 + r for the 32 experts of the block, then
+  // selects the block's top kc of that token; the last block to deliver a token's candidates
+  // (per-token ticket, reset by it) merges them, so the tokens' merges run in parallel
+  const uint32_t r = cluster_ctarank();
+  bool merge = false;
+  if (warp == 0 && (int)r < nt) {
+    float v[32];
 #pragma unroll
-    for (int i = 0; i < NI; ++i) fma_row(j + 32 * i, wv[i]);
-  } else {
-    const int n = d / 32;
-    constexpr int B = 16;
-    for (int i0 = 0; i0 < n; i0 += B) {
-      float wb[B];
+    for (int b = 0; b < RC_CLUSTER; ++b)
 #pragma unroll
-      for (int u = 0; u < B; ++u) wb[u] = (e < E && i0 + u < n) ? __ldg(wcol + (size_t)(j + 32 * (i0 + u)) * E) : 0.0f;
+      for (int w = 0; w < RC_J; ++w) v[b * RC_J + w] = ld_cluster_f32(&part[r][w][lane], (uint32_t)b);
 #pragma unroll
-      for (int u = 0; u < B; ++u)
-        if (i0 + u < n) fma_row(j + 32 * (i0 + u), wb[u]);
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < o; ++q) v[q] = __fadd_rn(v[q], v[q + o]);
+    const bool valid = e < E;
+    const float sv = valid ? sigmoid_ref(v[0]) : 0.0f;
+    const float key = __fadd_rn(sv, (bias && valid) ? __ldg(bias + e) : 0.0f);
+    bool has = valid;
+    const size_t cbase = (size_t)(t0 + r) * slots + (size_t)blockIdx.x * kc;
+    for (int q = 0; q < kc; ++q) {
+      float wk;
+      const int wid = warp_best(key, e, has, wk);
+      if (has && wid == e) {
+        has = false;
+        cand_k[cbase + q] = key;
+        cand_s[cbase + q] = sv;
+        cand_id[cbase + q] = e;
+      }
+      if (wid == 0x7FFFFFFF && lane == 0) cand_id[cbase + q] = -1;   // block has fewer than kc experts
     }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(tickets + t0 + r, 1) == (int)gridDim.x - 1;
+    merge = __shfl_sync(0xffffffffu, last, 0) != 0;
   }
-#pragma unroll
-  for (int tt = 0; tt < SMALL_TT; ++tt) part[(tt * 32 + j) * SMALL_ET + e_l] = acc[tt];
-  __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int q = warp; q < SMALL_TT * SMALL_ET; q += SMALL_THREADS / 32) {
-    const int tt = q / SMALL_ET, el = q % SMALL_ET;
-    float v = part[(tt * 32 + lane) * SMALL_ET + el];
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0 && tt < nt && e0 + el < E) S[(size_t)(t0 + tt) * E + e0 + el] = sigmoid_ref(v);
-  }
-  // the last CTA selects
+  cluster_sync_all();  // no CTA leaves, or reuses its shared memory, while another reads its partials
+  if (!merge) return;
+  // merge (warp 0): the token's candidates, read once into shared memory (reusing the W slice)
+  // as (key, s, id); a selected candidate's id becomes -1
   __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int total = gridDim.x * gridDim.y;
-    is_last = (atomicAdd(ticket, 1) == total - 1);
+  const int t = t0 + (int)r;
+  float* mk = Ws;
+  float* ms = mk + slots;
+  int* mid = reinterpret_cast<int*>(ms + slots);
+  const size_t cb = (size_t)t * slots;
+#pragma unroll 4
+  for (int c = lane; c < slots; c += 32) {
+    mk[c] = __ldcg(cand_k + cb + c);
+    ms[c] = __ldcg(cand_s + cb + c);
+    mid[c] = __ldcg(cand_id + cb + c);
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int t = warp; t < T; t += SMALL_THREADS / 32)
-    topk_warp(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
-  if (tid == 0) *ticket = 0;
+  if (lane == 0) tickets[t] = 0;   // ready for the next call
+  __syncwarp();
+  float my_s = 0.0f;
+  int my_id = 0;
+  for (int q = 0; q < k; ++q) {
+    float bk = 0.0f, bs = 0.0f;
+    int bid = -1, bc = -1;
+    for (int c = lane; c < slots; c += 32) {
+      const int id = mid[c];
+      if (id < 0) continue;
+      const float kv = mk[c];
+      if (bid < 0 || ranks_before(kv, id, bk, bid)) {
+        bk = kv;
+        bid = id;
+        bs = ms[c];
+        bc = c;
+      }
+    }
+    float wk;
+    const int wid = warp_best(bk, bid, bid >= 0, wk);
+    const bool mine = bid >= 0 && bid == wid;
+    if (mine) mid[bc] = -1;
+    const int owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    const float ws = __shfl_sync(0xffffffffu, bs, owner < 0 ? 0 : owner);
+    if (lane == q) {
+      my_s = ws;
+      my_id = wid;
+    }
+    __syncwarp();
+  }
+  float S = 0.0f;
+  for (int q = 0; q < k; ++q) {
+    const float sq = __shfl_sync(0xffffffffu, my_s, q);
+    S = (q == 0) ? sq : __fadd_rn(S, sq);
+  }
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    wts[(size_t)t * k + lane] = __fdiv_rn(my_s, S);
+  }
 }
 
 // Large batches: CTA = TILE_T tokens x TILE_E experts, 16 warps.  Lane = partial j; warp q
-// owns tokens 8*(q/4) .. +8 and experts 8*(q%4) .. +8 of the tile.  Rows are staged 32 at a
-// time through shared memory (lane j uses row c0 + j).
-__global__ void __launch_bounds__(512, 1) route_tiled_kernel(const uint16_t* __restrict__ x,
-                                                             const float* __restrict__ w_r, int T, int d, int E,
-                                                             float* __restrict__ S) {
-  __shared__ __align__(16) float Wt[32][TILE_E + 4];
-  __shared__ __align__(16) float Xt[32][TILE_T + 4];
-  pdl_wait();
+// owns tokens 8*(q/4) .. +8 and experts 8*(q%4) .. +8 of the tile.  Rows arrive TR at a time
+// through a TSTAGES-deep cp.async ring: W_r rows as FP32 (padded to 36 words so that the 32
+// lanes' 16-byte loads of 32 different rows spread over the banks), x as the raw BF16 tile
+// [token][row], which lane j reads at row c0 + j (consecutive lanes, consecutive addresses)
+// and widens in registers.  One barrier per stage.  (Measured on GB300: an 8-token x 16-expert
+// tile per thread with 8 warps, and widening x once per stage into a transposed FP32 tile, were
+// both slower than this.)
+constexpr int TR = 128;
+constexpr int TSTAGES = 3;
+constexpr int TTHREADS = 512;
+constexpr int TW = TILE_E + 4;   // padded W row (words)
+constexpr size_t TILED_SMEM = (size_t)TSTAGES * (TR * TW * 4 + TILE_T * TR * 2);
+
+
+__global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                  const float* __restrict__ w_r, int T, int d,
+                                                                  int E, float* __restrict__ S) {
+  extern __shared__ __align__(16) unsigned char tsm[];
+  float* Wst = reinterpret_cast<float*>(tsm);                                          // [TSTAGES][TR][TW]
+  uint16_t* Xst = reinterpret_cast<uint16_t*>(tsm + (size_t)TSTAGES * TR * TW * 4);    // [TSTAGES][TILE_T][TR]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * TILE_T, e0 = blockIdx.y * TILE_E;
   const int tsub = (warp >> 2) * 8, esub = (warp & 3) * 8;
+  const int nst = (d + TR - 1) / TR;
   float acc[8][8];
 #pragma unroll
   for (int a = 0; a < 8; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
 
-  // register staging: W 32x32 floats = 2 per thread; X 32 tokens x 32 values = 2 per thread
-  const int wr_r = tid >> 4, wr_c = (tid & 15) * 2;
-  const int xr_t = tid >> 4, xr_c = (tid & 15) * 2;
-  float2 wreg;
-  uint32_t xreg;
-  auto load = [&](int c0) {
-    const int e = e0 + wr_c;
-    const float* wp = w_r + (size_t)(c0 + wr_r) * E + e;
-    wreg.x = (e < E) ? __ldg(wp) : 0.0f;
-    wreg.y = (e + 1 < E) ? __ldg(wp + 1) : 0.0f;
-    const int t = t0 + xr_t;
-    xreg = (t < T) ? __ldg(reinterpret_cast<const uint32_t*>(x + (size_t)t * d + c0 + xr_c)) : 0u;
+  auto issue = [&](int st) {
+    const int c0 = st * TR;
+    float* W = Wst + (size_t)(st % TSTAGES) * TR * TW;
+    uint16_t* X = Xst + (size_t)(st % TSTAGES) * TILE_T * TR;
+    // W: TR rows x 32 experts (zeros past E or d); 16-byte pieces when rows are 16-byte aligned
+    if ((E & 3) == 0) {
+      for (int q = tid; q < TR * (TILE_E / 4); q += TTHREADS) {
+        const int r = q >> 3, ee = (q & 7) * 4;
+        const bool ok = (c0 + r < d) && (e0 + ee < E);
+        const float* src = ok ? w_r + (size_t)(c0 + r) * E + e0 + ee : w_r;
+        cp_async16(W + r * TW + ee, src, ok ? 16 : 0);
+      }
+    } else {
+      for (int q = tid; q < TR * TILE_E; q += TTHREADS) {
+        const int r = q >> 5, ee = q & 31;
+        const bool ok = (c0 + r < d) && (e0 + ee < E);
+        const float* src = ok ? w_r + (size_t)(c0 + r) * E + e0 + ee : w_r;
+        cp_async4(W + r * TW + ee, src, ok ? 4 : 0);
+      }
+    }
+    // x: TILE_T tokens x TR values, 16-byte pieces (zeros past T or d)
+    for (int q = tid; q < TILE_T * (TR / 8); q += TTHREADS) {
+      const int tt = q / (TR / 8), pc = (q % (TR / 8)) * 8;
+      const bool ok = (t0 + tt < T) && (c0 + pc < d);
+      const uint16_t* src = ok ? x + (size_t)(t0 + tt) * d + c0 + pc : x;
+      cp_async16(X + tt * TR + pc, src, ok ? 16 : 0);
+    }
   };
-  load(0);
-  for (int c0 = 0; c0 < d; c0 += 32) {
-    __syncthreads();
-    Wt[wr_r][wr_c] = wreg.x;
-    Wt[wr_r][wr_c + 1] = wreg.y;
-    Xt[xr_c + 0][xr_t] = bf16_bits_to_f32(xreg & 0xFFFFu);
-    Xt[xr_c + 1][xr_t] = bf16_bits_to_f32(xreg >> 16);
-    __syncthreads();
-    if (c0 + 32 < d) load(c0 + 32);
-    float xv[8], wv[8];
-    const float4* xp = reinterpret_cast<const float4*>(&Xt[lane][tsub]);
-    const float4* wp = reinterpret_cast<const float4*>(&Wt[lane][esub]);
-    float4 t4 = xp[0], u4 = xp[1];
-    xv[0] = t4.x; xv[1] = t4.y; xv[2] = t4.z; xv[3] = t4.w;
-    xv[4] = u4.x; xv[5] = u4.y; xv[6] = u4.z; xv[7] = u4.w;
-    float4 w4 = wp[0], v4 = wp[1];
-    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-    wv[4] = v4.x; wv[5] = v4.y; wv[6] = v4.z; wv[7] = v4.w;
+
+  pdl_wait();
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+  for (int st = 0; st < TSTAGES - 1; ++st) {
+    if (st < nst) issue(st);
+    cp_async_commit();
+  }
+  for (int st = 0; st < nst; ++st) {
+    cp_async_wait<TSTAGES - 2>();
+    __syncthreads();   // stage st landed for every thread; stage st-1 is no longer read
+    if (st + TSTAGES - 1 < nst) issue(st + TSTAGES - 1);
+    cp_async_commit();
+    const float* W = Wst + (size_t)(st % TSTAGES) * TR * TW;
+    const uint16_t* X = Xst + (size_t)(st % TSTAGES) * TILE_T * TR;
+    const int rows = min(TR, d - st * TR);
+    for (int u = 0; u < rows; u += 32) {
+      const int c = u + lane;
+      float xv[8], wv[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+      for (int a = 0; a < 8; ++a) xv[a] = bf16_bits_to_f32(X[(tsub + a) * TR + c]);
+      const float4 w4 = *reinterpret_cast<const float4*>(W + c * TW + esub);
+      const float4 v4 = *reinterpret_cast<const float4*>(W + c * TW + esub + 4);
+      wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+      wv[4] = v4.x; wv[5] = v4.y; wv[6] = v4.z; wv[7] = v4.w;
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+    }
   }
   // butterfly over the 32 partials (lanes); every lane ends with the same sums
 #pragma unroll
@@ -307,13 +473,14 @@ __global__ void __launch_bounds__(512, 1) route_tiled_kernel(const uint16_t* __r
     }
 }
 
+template <int NI>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ S, const float* __restrict__ bias,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ wts) {
   pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_warp(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
+  topk_warp<NI>(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
 }
 
 // Stable counting sort of pair ids by expert, one CTA of 1024 threads.  Pairs are taken
@@ -441,43 +608,66 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) permute_kernel(const int32_t*
 }  // namespace
 
 size_t route_ws_bytes(int T, int E) {
+  // scores (T x E) for the large-batch path; candidates (s, id) for the small-batch path
   size_t s = (size_t)T * E * sizeof(float);
+  if (T <= SMALL_T_MAX) s = std::max(s, (size_t)T * rc_slots(E, 32) * 12);
   s = (s + 255) & ~(size_t)255;
   return s + 256;
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                          int32_t* ids, float* w, void* ws, cudaStream_t s) {
-  // the ticket sits at a fixed offset so that calls with different T share it
+  // one ticket per token of the small-batch kernel, at fixed offsets so that calls with
+  // different T share them
   int* ticket = reinterpret_cast<int*>(ws);
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
-  const size_t small_smem = (size_t)SMALL_TT * d * 4 + SMALL_TT * 32 * SMALL_ET * sizeof(float);
-  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin()) {
+  const size_t small_smem = (size_t)(d / 32) * (RC_J * 32 + RC_J * SMALL_TT) * sizeof(float);
+  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() &&
+      small_smem >= (size_t)rc_slots(E, k) * 12) {
     const size_t smem = small_smem;
-    dim3 grid((E + SMALL_ET - 1) / SMALL_ET, (T + SMALL_TT - 1) / SMALL_TT);
-    auto launch = [&](auto kern) -> cudaError_t {
-      static int configured_dev = -1;
-      static size_t configured_smem = 0;
-      int dev;
-      cudaGetDevice(&dev);
-      if (dev != configured_dev || smem > configured_smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-        configured_smem = smem;
-      }
-      kern<<<grid, SMALL_THREADS, smem, s>>>(x, w_r, bias, T, d, E, k, S, ticket, ids, w);
-      return cudaGetLastError();
-    };
-    if (d == 4096) return launch(route_small_kernel<128>);
-    if (d == 512) return launch(route_small_kernel<16>);
-    return launch(route_small_kernel<0>);
+    static int configured_dev = -1;
+    static size_t configured_smem = 0;
+    int dev;
+    cudaGetDevice(&dev);
+    if (dev != configured_dev || smem > configured_smem) {
+      cudaError_t e = cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      configured_dev = dev;
+      configured_smem = smem;
+    }
+    const int slots = rc_slots(E, k);
+    float* cand_k = S;
+    float* cand_s = S + (size_t)T * slots;
+    int* cand_id = reinterpret_cast<int*>(S + (size_t)2 * T * slots);
+    dim3 grid((E + 31) / 32, RC_CLUSTER, (T + SMALL_TT - 1) / SMALL_TT);
+    {
+      const cudaError_t le = launch_k(route_cluster_kernel, dim3(grid), dim3(RC_THREADS), smem, s, x, w_r, bias, T,
+                                      d, E, k, cand_k, cand_s, cand_id, ticket, ids, w);
+      if (le != cudaSuccess) return le;
+    }
+    return cudaGetLastError();
+  }
+  static int tiled_dev = -1;
+  int dev;
+  cudaGetDevice(&dev);
+  if (dev != tiled_dev) {
+    cudaError_t e = cudaFuncSetAttribute(route_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)TILED_SMEM);
+    if (e != cudaSuccess) return e;
+    tiled_dev = dev;
   }
   dim3 grid((T + TILE_T - 1) / TILE_T, (E + TILE_E - 1) / TILE_E);
-  route_tiled_kernel<<<grid, 512, 0, s>>>(x, w_r, T, d, E, S);
+  {
+    const cudaError_t le = launch_k(route_tiled_kernel, dim3(grid), dim3(TTHREADS), TILED_SMEM, s, x, w_r, T, d, E, S);
+    if (le != cudaSuccess) return le;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(S, bias, T, E, k, ids, w);
+  {
+    auto kern = E <= 32 ? topk_kernel<1> : E <= 128 ? topk_kernel<4> : E <= 384 ? topk_kernel<12> : topk_kernel<32>;
+    const cudaError_t le = launch_k(kern, dim3((T + 7) / 8), dim3(256), 0, s, S, bias, T, E, k, ids, w);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -493,7 +683,11 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  permute_kernel<<<1, PERM_THREADS, smem, s>>>(ids, T * k, E, offsets, perm, inv, active, n_active, err);
+  {
+    const cudaError_t le = launch_k(permute_kernel, dim3(1), dim3(PERM_THREADS), smem, s, ids, T * k, E, offsets,
+                                    perm, inv, active, n_active, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -7,11 +7,11 @@
 // input and output buffers with no access to an allocator.  This call allocates nothing:
 // it neither calls cudaMalloc/cudaFree nor any library routine that allocates.
 //
-// The scratch is one file-scope device array of ROUTE_STATIC_SCRATCH bytes, loaded with the
-// library and held by every GPU that loads it until the process exits.  All calls share
+// The scratch is one file-scope device array of ROUTE_STATIC_SCRATCH bytes (about 384 KB),
+// loaded with the library and held by every GPU that loads it until the process exits.  All calls share
 // it, so calls that overlap on the GPU (other streams, other host threads) race and must be
-// ordered by the caller.  The selection ticket at its start must be zero before a call; it
-// is cleared with a memset on the caller's stream at every call.
+// ordered by the caller.  The selection tickets at its start must be zero before a call; they are
+// cleared with a memset on the caller's stream at every call.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,8 +21,12 @@
 
 namespace {
 
+// tickets, then either the scores of a large batch (T*E floats) or the selection candidates
+// of a small batch (at most 32 tokens x 1024 expert slots x 12 bytes)
 constexpr size_t ROUTE_STATIC_SCORES = (size_t)BRE_ROUTE_STATIC_MAX_TE * sizeof(float);
-constexpr size_t ROUTE_STATIC_SCRATCH = 256 + ROUTE_STATIC_SCORES;   // ticket + scores
+constexpr size_t ROUTE_STATIC_CANDIDATES = (size_t)32 * 1024 * 12;
+constexpr size_t ROUTE_STATIC_SCRATCH =
+    256 + (ROUTE_STATIC_SCORES > ROUTE_STATIC_CANDIDATES ? ROUTE_STATIC_SCORES : ROUTE_STATIC_CANDIDATES);
 
 static __device__ __align__(256) unsigned char g_route_scratch[ROUTE_STATIC_SCRATCH];
 
@@ -55,6 +59,7 @@ extern "C" bre_status moe_route_static(const void* x_bf16, const float* w_r, con
   if (k > E || k > 32 || E > 1024 || d % 32 != 0) return BRE_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(x_bf16) % 16 || reinterpret_cast<uintptr_t>(w_r) % 16) return BRE_ERR_ARG;
   if ((long long)T * E > BRE_ROUTE_STATIC_MAX_TE) return BRE_ERR_WORKSPACE;   // beyond the fixed scratch
+  if (bre::route_ws_bytes(T, E) > ROUTE_STATIC_SCRATCH) return BRE_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return BRE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

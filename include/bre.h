@@ -112,9 +112,10 @@ bre_status moe_route(const void *x_bf16, const float *w_r, const float *bias, in
  * loops that must not call cudaMalloc because it may synchronise the device; integrations
  * handed only pre-allocated buffers).  The pages have no counterpart: it is an interface
  * convenience of this library.  It computes exactly what moe_route computes.
- *   Scratch: one fixed device array inside the library (256 + 4 * BRE_ROUTE_STATIC_MAX_TE
- *   bytes), held by every GPU that loads the library until the process exits.  T * E above
- *   BRE_ROUTE_STATIC_MAX_TE returns BRE_ERR_WORKSPACE.  Allocates nothing.
+ *   Scratch: one fixed device array inside the library (256 bytes plus the larger of
+ *   4 * BRE_ROUTE_STATIC_MAX_TE and 384 KB), held by every GPU that loads the library until
+ *   the process exits.  T * E above BRE_ROUTE_STATIC_MAX_TE, or a shape whose
+ *   moe_route_workspace exceeds the array, returns BRE_ERR_WORKSPACE.  Allocates nothing.
  *   The first call on a device looks up the array's device address (and may load the
  *   library's device code); make that first call before any stream capture.
  *   Every call shares the array: calls that overlap on the GPU (different streams or host
@@ -148,10 +149,13 @@ bre_status moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *of
  *   x_bf16 [T][d]; offsets/perm/active/n_active from moe_permute (k pairs per
  *   token); y_pairs [T*k][d] FP32 out, row q = permuted position q (rows of
  *   pairs with an invalid id are not written); y_shared [T][d] FP32 out.
- *   ws: moe_expert_ffn_workspace(...) bytes, zero-filled once after allocation.
- * Shapes: d and d_ff multiples of 256; each of d, d_ff either <= 2048 or a
- * multiple of 1024 (Q2_K rows are copied to shared memory with 16-byte
- * aligned bulk copies). */
+ *   ws: moe_expert_ffn_workspace(T, ...) bytes, zero-filled once after allocation.
+ *   Its leading part holds counters that each call leaves at zero again; a
+ *   workspace sized for T serves every call with T' <= T (same k, d, d_ff,
+ *   d_ff_shared).  Calls sharing one workspace must be ordered.
+ * Shapes: d and d_ff multiples of 256; for T <= 8 each of d, d_ff either
+ * <= 1024 or a multiple of 1024 (Q2_K rows reach shared memory as whole
+ * 16-row tiles or as 4-block tensor-copy pieces with a 16-byte row pitch). */
 size_t moe_expert_ffn_workspace(int T, int k, int E, int d, int d_ff, int d_ff_shared);
 bre_status moe_expert_ffn(const bre_ffn_weights *routed, const bre_ffn_weights *shared, const void *x_bf16,
                           int T, int k, const int32_t *offsets, const int32_t *perm, const int32_t *active,

@@ -137,7 +137,8 @@ def test_engram_full_size_sampled(cuda_dev):
 # --------------------------------------------------------------------------- #
 
 @pytest.mark.parametrize("shape,T", [(synth.TINY, 4), (synth.V41, 1), (synth.V41, 2), (synth.V41, 4), (synth.V41, 8),
-                                     (synth.V41, 5), (synth.TINY, 33), (synth.TINY, 300)])
+                                     (synth.V41, 5), (synth.V41, 17), (synth.V41, 32), (synth.TINY, 9),
+                                     (synth.TINY, 33), (synth.TINY, 300)])
 def test_route_bit_exact(cuda_dev, shape, T):
     for tset in range(2):
         x = synth.x_bf16(SEED, 0, tset, T, shape.d)
@@ -159,6 +160,20 @@ def test_route_prefill_zipf_sampled(cuda_dev):
     ids_ref, w_ref = oracle.route(x[sample], w_r, b, shape.k)
     assert np.array_equal(ids.cpu().numpy()[sample], ids_ref)
     assert np.array_equal(w.cpu().numpy()[sample].view(np.uint32), w_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("T,d,E,k", [(3, 96, 40, 32), (12, 64, 33, 7), (2, 32, 1, 1), (20, 160, 70, 9),
+                                     (40, 96, 33, 7), (100, 224, 70, 9), (77, 4096, 384, 6)])
+def test_route_odd_shapes(cuda_dev, T, d, E, k):
+    """Expert counts that leave a partial block of 32, k up to 32, several token groups; above
+    32 tokens the large-batch kernel, with rows not a multiple of its 128-row stage."""
+    x = synth.x_bf16(SEED + d, 0, 0, T, d)
+    w_r = synth.router_weight(SEED + E, 0, d, E)
+    b = synth.route_bias(SEED + k, 0, E, 0.3)
+    ids_ref, w_ref = oracle.route(x, w_r, b, k)
+    ids, w = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
 
 
 def test_route_ties_and_zero_bias(cuda_dev):
@@ -252,6 +267,23 @@ def test_layer_decode_full_shape(cuda_dev):
         assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
         assert_layer_close(out, of, ref)
         assert int(layer.dev_err) == 0
+
+
+def test_layer_workspace_shared_across_paths(cuda_dev):
+    """One workspace serves decode calls (which keep K-part counters in it between calls) and a
+    grouped-GEMM call in between; the repeated decode call is bit-identical."""
+    shape = synth.V41
+    layer = device_layer(SEED, 0, shape, 64, cuda_dev)
+    x8 = synth.x_bf16(SEED, 0, 41, 8, shape.d).to(cuda_dev)
+    x2 = synth.x_bf16(SEED, 0, 42, 2, shape.d).to(cuda_dev)
+    x64 = synth.x_bf16(SEED, 0, 43, 64, shape.d).to(cuda_dev)
+    a, _ = layer.forward(x8)
+    a = a.clone()
+    layer.forward(x2)
+    layer.forward(x64)
+    b, _ = layer.forward(x8)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert int(layer.dev_err) == 0
 
 
 def test_layer_repeatable(cuda_dev):
