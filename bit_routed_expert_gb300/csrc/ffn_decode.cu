@@ -37,7 +37,7 @@ namespace {
 constexpr int NS = 2;                 // ring stages per warp
 constexpr int STAGE = 5376;           // bytes per stage: 16 rows x 336 B of one matrix
 constexpr int MAX_WARPS = 12;         // phase 1 (at most 170 registers a thread)
-constexpr int MAX_WARPS_P2 = 8;       // phase 2 (double-buffered B operand, up to 255 registers)
+constexpr int MAX_WARPS_P2 = 8;       // phase 2 (at most 255 registers a thread)
 constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
@@ -88,12 +88,13 @@ struct DecParams {
   int xstride;  // bytes per token row of the permuted activations in shared memory
   const unsigned char* pkg;  // activation package in global memory (phase 1)
   uint32_t m43;              // 0x43004300: BF16 exponent pattern of 128 in both halves
-  int kp_r, kp_s;            // K parts per 16-row tile (phase 1): items are (tile, K part)
+  int kp_r, kp_s;            // K parts per 16-row tile: items are (tile, K part)
   int C_r, C_s;              // chunks per matrix row of a routed / the shared expert
   int cpi_r, cpi_s;          // chunks per matrix in one item (C / K parts)
   FDiv fd_kps, fd_kpr, fd_trk, fd_k;   // divisors: K parts (shared, routed), routed tiles * K parts, k
-  float2* part_r;            // routed partial (gate, up) sums: [pair position][tile][K part][16 rows]
-  float2* part_s;            // shared partial sums: [token][tile][K part][16 rows]
+  float* part_r;             // routed partial sums: [pair position][tile][K part][16 rows] x (gate, up)
+                             // in phase 1, x (y) in phase 2
+  float* part_s;             // shared partial sums: [token][tile][K part][16 rows] x (2 | 1)
   int* tile_cnt;             // per tile count of finished K parts (zero between calls)
 };
 
@@ -116,7 +117,7 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
   Item it;
   it.id = id;
   if (id < 0) return it;
-  const int kps = (PHASE == 1) ? p.kp_s : 1, kpr = (PHASE == 1) ? p.kp_r : 1;
+  const int kps = (PHASE == 1) ? p.kp_s : 1, kpr = (PHASE == 1) ? p.kp_r : 1;   // phase 2 is not split
   if (id < tiles_s * kps) {
     it.shared = true;
     it.tile = fdiv(id, p.fd_kps);
@@ -367,26 +368,25 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
   }
 }
 
-// B operand of one block for column g: 16 uint4 (both limbs of h, fragment order) and the
-// three limbs of its sub-block sums.
+// B operand of one block for column g: 16 uint4 (both limbs of h, fragment order).
 struct P2B {
   uint4 v[16];
-  uint2 m[3];
 };
 
-__device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, const uint16_t* __restrict__ HBm,
+__device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, const uint16_t* __restrict__,
                                           int pos_g, int nb, int b, int t) {
   const uint16_t* hblk = hB + ((long long)pos_g * nb + b) * 512;
-  const uint16_t* hm = HBm + (((long long)pos_g * nb + b) * 4 + t) * 12;
 #pragma unroll
   for (int q = 0; q < 16; ++q) B.v[q] = __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8));
-#pragma unroll
-  for (int limb = 0; limb < 3; ++limb) B.m[limb] = __ldg(reinterpret_cast<const uint2*>(hm + limb * 4));
 }
 
 // One 256-column block of 16 rows of the down projection.
 __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_bytes, int g, int t, const P2B& B,
-                                             uint32_t m43, float (&acc)[4]) {
+                                             const uint16_t* __restrict__ hm, uint32_t m43, float (&acc)[4]) {
+  // the three limbs of the sub-block sums are first needed at the block's end: loaded here
+  uint2 bm[3];
+#pragma unroll
+  for (int limb = 0; limb < 3; ++limb) bm[limb] = __ldg(reinterpret_cast<const uint2*>(hm + limb * 4));
   uint32_t qw[2][4], sw[2], dd[2];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
@@ -437,13 +437,13 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
     const uint32_t A2 = prmt(mg, C43, SEL_HI), A3 = prmt(mg8, C43, SEL_HI);
 #pragma unroll
     for (int limb = 0; limb < 3; ++limb) {
-      const uint2 bm = B.m[limb];
+      const uint2 b2 = bm[limb];
       if (limb == 0)
-        mma_bf16_16816_z(M, A0, A1, A2, A3, bm.x, bm.y);
+        mma_bf16_16816_z(M, A0, A1, A2, A3, b2.x, b2.y);
       else
-        mma_bf16_16816(M, A0, A1, A2, A3, bm.x, bm.y);
-      hsum += bf16_bits_to_f32(bm.x & 0xFFFFu) + bf16_bits_to_f32(bm.x >> 16) + bf16_bits_to_f32(bm.y & 0xFFFFu) +
-              bf16_bits_to_f32(bm.y >> 16);
+        mma_bf16_16816(M, A0, A1, A2, A3, b2.x, b2.y);
+      hsum += bf16_bits_to_f32(b2.x & 0xFFFFu) + bf16_bits_to_f32(b2.x >> 16) + bf16_bits_to_f32(b2.y & 0xFFFFu) +
+              bf16_bits_to_f32(b2.y >> 16);
     }
   }
   // block sum of h for column g, then for the C-fragment columns 2t and 2t+1
@@ -475,10 +475,11 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
   for (int bl = 0; bl < cb; bl += 2) {
     const int b = c * cb + bl;
     if (bl + 1 < cb) p2_load_b(B1, hB, HBm, pos_g, nb, b + 1, t);
-    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B0, m43, acc);
+    const uint16_t* hm = HBm + (((long long)pos_g * nb + b) * 4 + t) * 12;   // limbs of block b
+    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B0, hm, m43, acc);
     if (bl + 1 < cb) {
       if (bl + 2 < cb) p2_load_b(B0, hB, HBm, pos_g, nb, b + 2, t);
-      p2_q2k_block(stage + (bl + 1) * Q2K_BB, chunk_bytes, g, t, B1, m43, acc);
+      p2_q2k_block(stage + (bl + 1) * Q2K_BB, chunk_bytes, g, t, B1, hm + 48, m43, acc);
     }
   }
 }
@@ -786,7 +787,7 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
           acc2[1][i] = m ? accm[i] : acc2[1][i];
         }
       } else {
-        const int c = cc;
+        const int c = it.kp * it.cpi + cc;
         if (it.shared) {
           p2_q80_chunk(stage, it.cb, c, g, t, p.Fs, p.hS + (size_t)dg * 2 * p.Fs, p.HS16 + (size_t)d0 * (p.Fs / 16),
                        p.HS16 + (size_t)d1 * (p.Fs / 16), acc2[0]);
@@ -803,15 +804,22 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
 
     // ---- K-part fix-up: the last part of a tile to finish adds the parts in order 0..KP-1
     if (PHASE == 1 && it.KP > 1) {
-      // partials of column col: [col source][tile][K part][16 rows]
-      auto part_of = [&](int col) -> float2* {
-        return it.shared ? p.part_s + ((size_t)col * tiles_s + it.tile) * it.KP * 16
-                         : p.part_r + ((size_t)(it.off + col) * tiles_r + it.tile) * it.KP * 16;
+      constexpr int NV = (PHASE == 1) ? 2 : 1;   // values per (row, column): (gate, up) or y
+      // partials of column col: [col source][tile][K part][16 rows][NV]
+      auto part_of = [&](int col) -> float* {
+        return it.shared ? p.part_s + ((size_t)col * tiles_s + it.tile) * it.KP * 16 * NV
+                         : p.part_r + ((size_t)(it.off + col) * tiles_r + it.tile) * it.KP * 16 * NV;
       };
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
-        if (col < it.n) part_of(col)[it.kp * 16 + row] = make_float2(acc2[0][i], acc2[1][i]);
+        if (col < it.n) {
+          float* pc = part_of(col) + (it.kp * 16 + row) * NV;
+          if (PHASE == 1)
+            *reinterpret_cast<float2*>(pc) = make_float2(acc2[0][i], acc2[1][i]);
+          else
+            *pc = acc2[0][i];
+        }
       }
       // the warp barrier orders every lane's partial stores before lane 0's release; the
       // finisher's acquire orders its reads of the other parts after it (then the warp barrier)
@@ -828,11 +836,16 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
       for (int i = 0; i < 4; ++i) {
         const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
         if (col < it.n) {
-          const float2* pc = part_of(col);
+          const float* pc = part_of(col) + row * NV;
           for (int q = 0; q < it.KP; ++q) {
-            const float2 v = __ldcg(pc + q * 16 + row);
-            acc2[0][i] = q == 0 ? v.x : acc2[0][i] + v.x;
-            acc2[1][i] = q == 0 ? v.y : acc2[1][i] + v.y;
+            if (PHASE == 1) {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(pc + q * 16 * NV));
+              acc2[0][i] = q == 0 ? v.x : acc2[0][i] + v.x;
+              acc2[1][i] = q == 0 ? v.y : acc2[1][i] + v.y;
+            } else {
+              const float v = __ldcg(pc + q * 16 * NV);
+              acc2[0][i] = q == 0 ? v : acc2[0][i] + v;
+            }
           }
         }
       }
@@ -923,16 +936,17 @@ int pick_chunk(int nb, int bb, int cap_per_mat, int align_blocks, int* whole) {
   return cb;
 }
 
-// Phase-1 K parts per tile: routed tiles split into one item per chunk; shared (Q8_0) tiles
-// into at most 4 parts (a divisor of their chunk count).
-void phase1_kparts(int d, bool has_shared, int* kpr, int* kps) {
+// K parts per tile of a phase whose rows hold nb_r Q2_K / nb_s Q8_0 blocks: routed tiles split
+// into one item per chunk; shared (Q8_0) tiles into at most 4 parts (a divisor of their chunk
+// count).
+void phase_kparts(int nb_r, int nb_s, bool has_shared, int* kpr, int* kps) {
   int whole = 0;
-  const int cbr = pick_chunk(d / 256, Q2K_BB, STAGE, 4, &whole);
-  *kpr = cbr > 0 ? (d / 256) / cbr : 1;
+  const int cbr = pick_chunk(nb_r, Q2K_BB, STAGE, 4, &whole);
+  *kpr = cbr > 0 ? nb_r / cbr : 1;
   *kps = 1;
   if (has_shared) {
-    const int cbs = pick_chunk(d / 32, Q80_BB, STAGE, 8, &whole);
-    const int Cs = cbs > 0 ? (d / 32) / cbs : 1;
+    const int cbs = pick_chunk(nb_s, Q80_BB, STAGE, 8, &whole);
+    const int Cs = cbs > 0 ? nb_s / cbs : 1;
     for (int q = Cs < 4 ? Cs : 4; q >= 1; --q)
       if (Cs % q == 0) {
         *kps = q;
@@ -943,10 +957,12 @@ void phase1_kparts(int d, bool has_shared, int* kpr, int* kps) {
 
 }  // namespace
 
-// 1 KB of work counters, then one K-part counter per phase-1 tile of the largest decode batch
-// (shared tiles + DECODE_T_MAX * k routed pairs' tiles).
-size_t ffn_reserved_bytes(int k, int F, int Fs) {
-  const size_t slots = (size_t)Fs / 16 + (size_t)DECODE_T_MAX * k * (F / 16);
+// 1 KB of work counters, then one K-part counter per tile of the largest decode batch (shared
+// tiles + DECODE_T_MAX * k routed pairs' tiles, the larger of the two phases).
+size_t ffn_reserved_bytes(int k, int d, int F, int Fs) {
+  const size_t s1 = (size_t)Fs / 16 + (size_t)DECODE_T_MAX * k * (F / 16);
+  const size_t s2 = (Fs > 0 ? (size_t)d / 16 : 0) + (size_t)DECODE_T_MAX * k * (d / 16);
+  const size_t slots = s1 > s2 ? s1 : s2;
   return 1024 + ((slots * 4 + 255) & ~(size_t)255);
 }
 
@@ -959,19 +975,25 @@ struct DecWs {
 
 DecWs dec_ws_layout(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
-  int kpr = 1, kps = 1;
-  phase1_kparts(d, Fs > 0, &kpr, &kps);
+  int kpr1 = 1, kps1 = 1, kpr2 = 1, kps2 = 1;
+  phase_kparts(d / 256, d / 32, Fs > 0, &kpr1, &kps1);
+  (void)kpr2;
+  (void)kps2;   // phase 2 is not split
+  // partials: phase 1 (gate, up) pairs over d_ff rows, phase 2 single values over d rows; the
+  // phases run one after the other and share the buffers
+  const size_t pr = std::max(P * (F / 16) * kpr1 * 16 * 2, P * (d / 16) * kpr2 * 16) * 4;
+  const size_t ps = std::max((size_t)T * (Fs / 16) * kps1 * 16 * 2, (size_t)T * (d / 16) * kps2 * 16) * 4;
   auto up256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
   DecWs w;
   w.cnt = 1024;                                                  // after the work counters
-  w.pkg = ffn_reserved_bytes(k, F, Fs);
+  w.pkg = ffn_reserved_bytes(k, d, F, Fs);
   w.hB = up256(w.pkg + pkg_layout(T, d).total);
   w.HBm = up256(w.hB + P * (F / 256) * 512 * 2);
   w.hS = up256(w.HBm + P * (F / 256) * 4 * 12 * 2);
   w.HS16 = up256(w.hS + (size_t)T * 2 * Fs * 2);
   w.part_r = up256(w.HS16 + (size_t)T * (Fs / 16) * 4);
-  w.part_s = up256(w.part_r + P * (F / 16) * kpr * 16 * 8);
-  w.total = up256(w.part_s + (size_t)T * (Fs / 16) * kps * 16 * 8);
+  w.part_s = up256(w.part_r + pr);
+  w.total = up256(w.part_s + (Fs > 0 ? ps : 0));
   return w;
 }
 
@@ -1064,9 +1086,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   p.hS = reinterpret_cast<uint16_t*>(w + L.hS);
   p.HS16 = reinterpret_cast<float*>(w + L.HS16);
   p.tile_cnt = reinterpret_cast<int*>(w + L.cnt);
-  p.part_r = reinterpret_cast<float2*>(w + L.part_r);
-  p.part_s = reinterpret_cast<float2*>(w + L.part_s);
-  phase1_kparts(p.d, S != nullptr, &p.kp_r, &p.kp_s);
+  p.part_r = reinterpret_cast<float*>(w + L.part_r);
+  p.part_s = reinterpret_cast<float*>(w + L.part_s);
   p.xstride = p.d * 2 + 32;
   p.m43 = 0x43004300u;
 
@@ -1110,8 +1131,16 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     if (p.cb_r <= 0 || p.cb_s <= 0) return cudaErrorInvalidValue;
     p.C_r = p.nb_r / p.cb_r;
     p.C_s = S ? p.nb_s / p.cb_s : 1;
+    // phase 1 splits tiles along K (two whole-tile items per warp left SMs idle); phase 2 has
+    // enough items per warp for balance, and its fix-up would cost registers
+    if (phase == 1) {
+      phase_kparts(p.nb_r, p.nb_s, S != nullptr, &p.kp_r, &p.kp_s);
+    } else {
+      p.kp_r = 1;
+      p.kp_s = 1;
+    }
     {
-      const int kpr = phase == 1 ? p.kp_r : 1, kps = phase == 1 ? p.kp_s : 1;
+      const int kpr = p.kp_r, kps = p.kp_s;
       p.fd_kpr = make_fdiv(kpr);
       p.fd_kps = make_fdiv(kps);
       p.fd_trk = make_fdiv((unsigned)(p.rows_r / 16 * kpr));

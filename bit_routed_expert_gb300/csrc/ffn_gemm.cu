@@ -231,11 +231,6 @@ struct RawQ80 {
   uint32_t w[17];   // two 34-byte blocks (68 bytes, 4-byte aligned)
 };
 
-__device__ __forceinline__ void load_raw_q80(const uint8_t* row, int ks, RawQ80& r) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(row + ks * 2 * Q80_BB);
-#pragma unroll
-  for (int i = 0; i < 17; ++i) r.w[i] = __ldg(p + i);
-}
 
 __device__ __forceinline__ uint32_t byte_at(const RawQ80& r, int b) {  // byte b of the 68
   return (r.w[b >> 2] >> (8 * (b & 3))) & 0xFFu;
@@ -453,23 +448,48 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           rowA = p.s0 + (long long)(ti.nt * 256 + i) * rb;
           rowB = p.s0 + (long long)(ti.nt * 256 + 128 + i) * rb;
         }
-        RawQ80 ca, cb, na, nb;
-        load_raw_q80(rowA, 0, ca);
-        load_raw_q80(rowB, 0, cb);
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          if (ks + 1 < KS) {   // one K step ahead
-            load_raw_q80(rowA, ks + 1, na);
-            load_raw_q80(rowB, ks + 1, nb);
+        // The two Q8_0 blocks (68 bytes) of each row for a K step reach the warp's staging area
+        // by coalesced copies (lanes 0..16 copy one row's 17 words per instruction); the copy of
+        // the next K step runs while this one is dequantised.
+        const int pw = warp - 4;
+        unsigned char* stg = stage_raw + pw * 64 * Q2K_BB;
+        const uint8_t* pa0 = rowA - (long long)lane * rb + 4 * lane;
+        const uint8_t* pb0 = rowB - (long long)lane * rb + 4 * lane;
+        auto stage_copy = [&](int ks) {
+          if (lane < 17) {
+            const uint8_t* pa = pa0 + ks * 2 * Q80_BB;
+            const uint8_t* pb = pb0 + ks * 2 * Q80_BB;
+            unsigned char* dst = stg + 4 * lane;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) cp_async4(dst + r * 68, pa + (long long)r * rb, 4);
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) cp_async4(dst + (32 + r) * 68, pb + (long long)r * rb, 4);
           }
+          cp_async_commit();
+        };
+        auto stage_read = [&](RawQ80& a, RawQ80& b) {
+          cp_async_wait<0>();
+          __syncwarp();
+#pragma unroll
+          for (int w = 0; w < 17; ++w) {
+            a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * 68 + 4 * w);
+            b.w[w] = *reinterpret_cast<const uint32_t*>(stg + (32 + lane) * 68 + 4 * w);
+          }
+          __syncwarp();
+        };
+        RawQ80 ca, cb;
+        stage_copy(0);
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          stage_read(ca, cb);
+          if (ks + 1 < KS) stage_copy(ks + 1);
           const int s = it % G_STAGES;
           if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) { fail(); break; }
           store_q80_row(ca, b_st + s * G_B_BYTES, i);
           store_q80_row(cb, b_st + s * G_B_BYTES, i + 128);
           fence_proxy_async_smem();
           mbar_arrive(&full[s]);
-          ca = na;
-          cb = nb;
         }
+        cp_async_wait<0>();   // no copy stays in flight past the tile
       }
     }
   } else if (warp == 9) {
@@ -573,7 +593,7 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int K) {
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
   // the reserved prefix stays with the decode path's counters, which must keep their zeros
-  size_t s = ffn_reserved_bytes(k, F, Fs) + ((sizeof(Plan) + 1023) & ~(size_t)1023);
+  size_t s = ffn_reserved_bytes(k, d, F, Fs) + ((sizeof(Plan) + 1023) & ~(size_t)1023);
   s += ((P + T) * d * 2 + 1023) & ~(size_t)1023;     // gathered activations
   s += (P * F * 2 + 1023) & ~(size_t)1023;           // routed intermediate
   s += ((size_t)T * Fs * 2 + 1023) & ~(size_t)1023;  // shared intermediate
@@ -585,7 +605,7 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   const bre_ffn_weights* S = a.shared;
   const int T = a.T, k = a.k, d = R->d, F = R->d_ff, Fs = S ? S->d_ff : 0, E = R->n_experts;
   const size_t P = (size_t)T * k;
-  char* w = static_cast<char*>(a.ws) + ffn_reserved_bytes(k, F, Fs);
+  char* w = static_cast<char*>(a.ws) + ffn_reserved_bytes(k, d, F, Fs);
   Plan* plan = reinterpret_cast<Plan*>(w);
   w += (sizeof(Plan) + 1023) & ~(size_t)1023;
   uint16_t* xp = reinterpret_cast<uint16_t*>(w);

@@ -42,7 +42,7 @@ struct FfnArgs {
 constexpr int DECODE_T_MAX = 8;   // larger batches take the grouped-GEMM path
 // Leading bytes of the FFN workspace that hold the decode path's counters; they keep their
 // zeros between calls whatever T, so both paths place everything else after them.
-size_t ffn_reserved_bytes(int k, int F, int Fs);
+size_t ffn_reserved_bytes(int k, int d, int F, int Fs);
 size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs);
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs);
 bre_status ffn_check_shapes(const bre_ffn_weights* routed, const bre_ffn_weights* shared, int T);
