@@ -802,110 +802,18 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
     }
     q_pop();
 
-    // ---- K-part fix-up: the last part of a tile to finish adds the parts in order 0..KP-1
-    if (PHASE == 1 && it.KP > 1) {
-      constexpr int NV = (PHASE == 1) ? 2 : 1;   // values per (row, column): (gate, up) or y
-      // partials of column col: [col source][tile][K part][16 rows][NV]
-      auto part_of = [&](int col) -> float* {
-        return it.shared ? p.part_s + ((size_t)col * tiles_s + it.tile) * it.KP * 16 * NV
-                         : p.part_r + ((size_t)(it.off + col) * tiles_r + it.tile) * it.KP * 16 * NV;
-      };
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
-        if (col < it.n) {
-          float* pc = part_of(col) + (it.kp * 16 + row) * NV;
-          if (PHASE == 1)
-            *reinterpret_cast<float2*>(pc) = make_float2(acc2[0][i], acc2[1][i]);
-          else
-            *pc = acc2[0][i];
-        }
-      }
-      // the warp barrier orders every lane's partial stores before lane 0's release; the
-      // finisher's acquire orders its reads of the other parts after it (then the warp barrier)
-      __syncwarp();
-      int prev = 0;
-      if (lane == 0) {
-        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.tile_cnt + it.slot) : "memory");
-        if (prev == it.KP - 1) p.tile_cnt[it.slot] = 0;   // ready for the next call
-      }
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev != it.KP - 1) continue;
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
-        if (col < it.n) {
-          const float* pc = part_of(col) + row * NV;
-          for (int q = 0; q < it.KP; ++q) {
-            if (PHASE == 1) {
-              const float2 v = __ldcg(reinterpret_cast<const float2*>(pc + q * 16 * NV));
-              acc2[0][i] = q == 0 ? v.x : acc2[0][i] + v.x;
-              acc2[1][i] = q == 0 ? v.y : acc2[1][i] + v.y;
-            } else {
-              const float v = __ldcg(pc + q * 16 * NV);
-              acc2[0][i] = q == 0 ? v : acc2[0][i] + v;
-            }
-          }
-        }
-      }
-    }
-
-    // ---- epilogue
+    // ---- phase 1 ends an item by storing its FP32 (gate, up) partial sums for the expert's real
+    // columns; ffn_finish_kernel adds the K parts in order and forms h.  Phase 2 stores y.
     if (PHASE == 1) {
-      // h = silu(gate) * up, stored as two bf16 limbs; per-column sums over the 16 rows
-      float hs[2] = {0.0f, 0.0f};
+      float* base = it.shared ? p.part_s + (size_t)it.tile * it.KP * 32 : p.part_r + (size_t)it.tile * it.KP * 32;
+      const size_t col_stride = (size_t)(it.shared ? tiles_s : tiles_r) * it.KP * 32;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int col_src_i = (i & 1) ? sc1 : sc0;
-        const int row = r0 + g + 8 * (i >> 1);
-        float h = silu_mul(acc2[0][i], acc2[1][i]);
-        uint32_t hi, lo;
-        split_bf16x2(h, hi, lo);
-        const float hq = bf16_bits_to_f32(hi) + bf16_bits_to_f32(lo);
-        if (col_src_i >= 0) {
-          hs[i & 1] += hq;
-          if (it.shared) {
-            p.hS[((size_t)col_src_i * 2 + 0) * p.Fs + row] = (uint16_t)hi;
-            p.hS[((size_t)col_src_i * 2 + 1) * p.Fs + row] = (uint16_t)lo;
-          } else {
-            const int pos = it.off + 2 * t + (i & 1);
-            const int b2 = row >> 8, j = (row >> 4) & 15, ip = row & 15;
-            const int byte = ip >> 2, s = ip & 3, v4 = (byte & 1) * 2 + (byte >> 1);
-            // limbs of h * 4^-min(s,2) (the down projection's A fragments keep codes in place)
-            uint32_t shi, slo;
-            split_bf16x2(__fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f)), shi, slo);
-            const size_t base = ((((size_t)pos * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 8 + (size_t)(j >> 2) * 8;
-            p.hB[base + v4] = (uint16_t)shi;
-            p.hB[base + 4 + v4] = (uint16_t)slo;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 4; o <= 16; o <<= 1) {
-        hs[0] += __shfl_xor_sync(0xffffffffu, hs[0], o);
-        hs[1] += __shfl_xor_sync(0xffffffffu, hs[1], o);
-      }
-      if (g == 0) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int col = 2 * t + q;
-          if (col < it.n) {
-            if (it.shared) {
-              p.HS16[(size_t)col * (p.Fs / 16) + (r0 >> 4)] = hs[q];
-            } else {
-              const int pos = it.off + col;
-              const int b2 = r0 >> 8, j = (r0 >> 4) & 15;
-              uint32_t hi = f32_to_bf16_rne(hs[q]);
-              const float r1 = hs[q] - bf16_bits_to_f32(hi);
-              uint32_t mid = f32_to_bf16_rne(r1);
-              uint32_t lo = f32_to_bf16_rne(r1 - bf16_bits_to_f32(mid));
-              uint16_t* dst = p.HBm + (((size_t)pos * Fnb + b2) * 4 + (j >> 2)) * 12 + (j & 3);
-              dst[0] = (uint16_t)hi;
-              dst[4] = (uint16_t)mid;
-              dst[8] = (uint16_t)lo;
-            }
-          }
+        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
+        if (col < it.n) {
+          const size_t src = it.shared ? (size_t)col : (size_t)(it.off + col);   // token / pair position
+          *reinterpret_cast<float2*>(base + src * col_stride + (it.kp * 16 + row) * 2) =
+              make_float2(acc2[0][i], acc2[1][i]);
         }
       }
     } else {
@@ -920,6 +828,90 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
             p.y_pairs[(size_t)cs * p.d + row] = acc2[0][i];
         }
       }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// finish: for every (pair or token, row) add the K-part partial sums of gate and up in order
+// 0..KP-1, form h = silu(gate) * up and store it in the layouts phase 2 reads (routed: two BF16
+// limbs of h * 4^-min(s,2) in the fragment order plus three limbs of each 16-row sum; shared:
+// two limbs in natural order plus FP32 16-row sums).  One warp per 32 rows of one pair/token.
+// ----------------------------------------------------------------------------
+struct FinishParams {
+  const float* part_r;
+  const float* part_s;
+  int kp_r, kp_s;
+  int F, Fs, P, T, E;
+  const int32_t* offsets;
+  uint16_t* hB;
+  uint16_t* HBm;
+  uint16_t* hS;
+  float* HS16;
+};
+
+__global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int gr = f.F / 32, gs = f.Fs / 32;
+  const long long nr = (long long)f.P * gr;
+  const bool shared = w >= nr;
+  int src, rg;
+  if (!shared) {
+    src = (int)(w / gr);
+    rg = (int)(w % gr);
+    if (src >= __ldg(f.offsets + f.E)) return;   // no pair there (fewer valid pairs than T * k)
+  } else {
+    const long long w2 = w - nr;
+    if (w2 >= (long long)f.T * gs) return;
+    src = (int)(w2 / gs);
+    rg = (int)(w2 % gs);
+  }
+  const int rows = shared ? f.Fs : f.F;
+  const int KP = shared ? f.kp_s : f.kp_r;
+  const int row = rg * 32 + lane, tile = row >> 4, r = row & 15;
+  const float* pc = (shared ? f.part_s : f.part_r) + ((size_t)src * (rows / 16) + tile) * KP * 32 + r * 2;
+  float gv = 0.0f, uv = 0.0f;
+  for (int q = 0; q < KP; ++q) {
+    const float2 v = *reinterpret_cast<const float2*>(pc + q * 32);
+    gv = q == 0 ? v.x : gv + v.x;
+    uv = q == 0 ? v.y : uv + v.y;
+  }
+  const float h = silu_mul(gv, uv);
+  uint32_t hi, lo;
+  split_bf16x2(h, hi, lo);
+  float hq = bf16_bits_to_f32(hi) + bf16_bits_to_f32(lo);
+  const int Fnb = f.F / 256;
+  if (shared) {
+    f.hS[((size_t)src * 2 + 0) * f.Fs + row] = (uint16_t)hi;
+    f.hS[((size_t)src * 2 + 1) * f.Fs + row] = (uint16_t)lo;
+  } else {
+    const int b2 = row >> 8, j = (row >> 4) & 15, ip = row & 15;
+    const int byte = ip >> 2, s = ip & 3, v4 = (byte & 1) * 2 + (byte >> 1);
+    // limbs of h * 4^-min(s,2) (the down projection's A fragments keep codes in place)
+    uint32_t shi, slo;
+    split_bf16x2(__fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f)), shi, slo);
+    const size_t base = ((((size_t)src * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 8 + (size_t)(j >> 2) * 8;
+    f.hB[base + v4] = (uint16_t)shi;
+    f.hB[base + 4 + v4] = (uint16_t)slo;
+  }
+  // 16-row sums of the limb values (half warps)
+#pragma unroll
+  for (int o = 1; o <= 8; o <<= 1) hq += __shfl_xor_sync(0xffffffffu, hq, o);
+  if ((lane & 15) == 0) {
+    if (shared) {
+      f.HS16[(size_t)src * (f.Fs / 16) + tile] = hq;
+    } else {
+      const int b2 = tile >> 4, j = tile & 15;
+      const uint32_t h1 = f32_to_bf16_rne(hq);
+      const float r1 = hq - bf16_bits_to_f32(h1);
+      const uint32_t h2 = f32_to_bf16_rne(r1);
+      const uint32_t h3 = f32_to_bf16_rne(r1 - bf16_bits_to_f32(h2));
+      uint16_t* dst = f.HBm + (((size_t)src * Fnb + b2) * 4 + (j >> 2)) * 12 + (j & 3);
+      dst[0] = (uint16_t)h1;
+      dst[4] = (uint16_t)h2;
+      dst[8] = (uint16_t)h3;
     }
   }
 }
@@ -1176,6 +1168,24 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
                                         ms1);
         if (le != cudaSuccess) return le;
       }
+      FinishParams fp;
+      fp.part_r = p.part_r;
+      fp.part_s = p.part_s;
+      fp.kp_r = p.kp_r;
+      fp.kp_s = p.kp_s;
+      fp.F = p.F;
+      fp.Fs = p.Fs;
+      fp.P = (int)((size_t)a.T * a.k);
+      fp.T = a.T;
+      fp.E = p.E;
+      fp.offsets = a.offsets;
+      fp.hB = p.hB;
+      fp.HBm = p.HBm;
+      fp.hS = p.hS;
+      fp.HS16 = p.HS16;
+      const long long warps = (long long)fp.P * (p.F / 32) + (S ? (long long)a.T * (p.Fs / 32) : 0);
+      const cudaError_t le = launch_k(ffn_finish_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, fp);
+      if (le != cudaSuccess) return le;
     } else {
       e = cudaFuncSetAttribute(ffn_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;

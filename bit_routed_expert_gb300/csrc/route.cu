@@ -170,39 +170,27 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
   return v;
 }
 
-// Warp arg-best of one candidate per lane: the (key, id) that ranks first among lanes with has.
-// Returns the winner's id (0x7FFFFFFF when no lane has a candidate) and its key.
-__device__ __forceinline__ int warp_best(float key, int id, bool has, float& wkey) {
-  float wk = key;
-  int wid = has ? id : 0x7FFFFFFF;
-  bool wh = has;
-  for (int o = 16; o >= 1; o >>= 1) {
-    const float ok = __shfl_xor_sync(0xffffffffu, wk, o);
-    const int oid = __shfl_xor_sync(0xffffffffu, wid, o);
-    const bool oh = __shfl_xor_sync(0xffffffffu, (int)wh, o) != 0;
-    bool take;
-    if (wh != oh)
-      take = oh;
-    else if (!wh)
-      take = oid < wid;
-    else
-      take = ranks_before(ok, oid, wk, wid);
-    if (take) {
-      wk = ok;
-      wid = oid;
-      wh = oh;
-    }
-  }
-  wkey = wk;
-  return wid;
+// Selection order as an unsigned code: (code, id) ascending = key descending, then id ascending,
+// NaN keys last (an exact restatement of ranks_before for keys that are never -0; -0 is mapped
+// to +0).
+__device__ __forceinline__ uint32_t key_code(float k) {
+  if (isnan(k)) return 0xFFFFFFFFu;
+  uint32_t u = __float_as_uint(k);
+  if ((u << 1) == 0u) u = 0u;                                   // -0 -> +0
+  const uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // float order as unsigned order
+  return ~asc;
+}
+__device__ __forceinline__ bool code_before(uint32_t ca, int ia, uint32_t cb, int ib) {
+  return ca < cb || (ca == cb && ia < ib);
 }
 
-// Candidates of one token: kc slots per expert block, (s, id) with id = -1 for an empty slot.
+// Candidates of one token: kc slots per expert block, (code, s, id), sorted by rank within the
+// block; id = -1 for an empty slot (a block with fewer than kc experts).
 __host__ __device__ __forceinline__ int rc_slots(int E, int k) { return ((E + 31) / 32) * (k < 32 ? k : 32); }
 
 __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     route_cluster_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w_r,
-                         const float* __restrict__ bias, int T, int d, int E, int k, float* __restrict__ cand_k,
+                         const float* __restrict__ bias, int T, int d, int E, int k, uint32_t* __restrict__ cand_c,
                          float* __restrict__ cand_s, int* __restrict__ cand_id, int* tickets,
                          int32_t* __restrict__ ids, float* __restrict__ wts) {
   extern __shared__ __align__(16) float rc_smem[];
@@ -219,15 +207,16 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   const int kc = min(k, 32);
   const int slots = rc_slots(E, k);
   if ((E & 3) == 0) {
-    // 16-byte pieces: row (i, jj) of the slice is 8 pieces of the W_r row 32 i + RC_J jb + jj
-    for (int q = tid; q < n * RC_J * 8; q += RC_THREADS) {
-      const int pc = q & 7, row = q >> 3;           // row = i * RC_J + jj
-      const int i = row / RC_J, jj = row % RC_J;
-      const int ee = blockIdx.x * 32 + pc * 4;
-      const bool ok = ee < E;
-      const float* src = ok ? w_r + (size_t)(32 * i + jb * RC_J + jj) * E + ee : w_r;
-      cp_async16(Ws + (size_t)row * 32 + pc * 4, src, ok ? 16 : 0);
-    }
+    // 16-byte pieces: slice row (i, jj) is 8 pieces of W_r row 32 i + RC_J jb + jj; thread tid
+    // copies piece tid % 8 of jj = (tid / 8) % 4 for i = tid / 32, +4, +8, ...
+    const int pc = tid & 7, jj = (tid >> 3) & 3, i0 = tid >> 5;
+    const int ee = blockIdx.x * 32 + pc * 4;
+    const bool ok = ee < E;
+    const float* src = w_r + (size_t)(32 * i0 + jb * RC_J + jj) * E + (ok ? ee : 0);
+    float* dst = Ws + (size_t)(i0 * RC_J + jj) * 32 + pc * 4;
+    const size_t sstep = (size_t)128 * E;
+#pragma unroll 4
+    for (int i = i0; i < n; i += 4, src += sstep, dst += 4 * RC_J * 32) cp_async16(dst, src, ok ? 16 : 0);
   } else {
     const float* src = w_r + (size_t)j * E + (e < E ? e : 0);
     const size_t rstride = (size_t)32 * E;
@@ -247,16 +236,15 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   }
   cp_async_wait_all();
   __syncthreads();
-  // partial j of expert e: rows c = j + 32 i in ascending i, fmaf from +0
+  // partial j of expert e: rows c = j + 32 i in ascending i, fmaf from +0; the operands of eight
+  // rows are loaded before their FMAs (one warp per scheduler: the loads' latency is not hidden
+  // by other warps)
   float acc[SMALL_TT];
 #pragma unroll
   for (int tt = 0; tt < SMALL_TT; ++tt) acc[tt] = 0.0f;
   const float4* xw = reinterpret_cast<const float4*>(xs + (size_t)warp * n * SMALL_TT);
   const float* wp = Ws + warp * 32 + lane;
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    const float wgt = wp[(size_t)i * RC_J * 32];
-    const float4 a = xw[2 * i], b = xw[2 * i + 1];
+  auto fma_row = [&](float wgt, float4 a, float4 b) {
     acc[0] = fmaf(a.x, wgt, acc[0]);
     acc[1] = fmaf(a.y, wgt, acc[1]);
     acc[2] = fmaf(a.z, wgt, acc[2]);
@@ -265,13 +253,28 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     acc[5] = fmaf(b.y, wgt, acc[5]);
     acc[6] = fmaf(b.z, wgt, acc[6]);
     acc[7] = fmaf(b.w, wgt, acc[7]);
+  };
+  int i = 0;
+  for (; i + 8 <= n; i += 8) {
+    float wv[8];
+    float4 xa[8], xb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      wv[u] = wp[(size_t)(i + u) * RC_J * 32];
+      xa[u] = xw[2 * (i + u)];
+      xb[u] = xw[2 * (i + u) + 1];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) fma_row(wv[u], xa[u], xb[u]);
   }
+  for (; i < n; ++i) fma_row(wp[(size_t)i * RC_J * 32], xw[2 * i], xw[2 * i + 1]);
 #pragma unroll
   for (int tt = 0; tt < SMALL_TT; ++tt) part[tt][warp][lane] = acc[tt];
   cluster_sync_all();
   // CTA of rank r adds the 32 partials of token t0 + r for the 32 experts of the block, then
-  // selects the block's top kc of that token; the last block to deliver a token's candidates
-  // (per-token ticket, reset by it) merges them, so the tokens' merges run in parallel
+  // writes the block's top kc of that token in rank order (rank = number of the block's experts
+  // that come first); the last block to deliver a token's candidates (per-token ticket, reset by
+  // it) merges them, so the tokens' merges run in parallel
   const uint32_t r = cluster_ctarank();
   bool merge = false;
   if (warp == 0 && (int)r < nt) {
@@ -287,79 +290,78 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     const bool valid = e < E;
     const float sv = valid ? sigmoid_ref(v[0]) : 0.0f;
     const float key = __fadd_rn(sv, (bias && valid) ? __ldg(bias + e) : 0.0f);
-    bool has = valid;
-    const size_t cbase = (size_t)(t0 + r) * slots + (size_t)blockIdx.x * kc;
-    for (int q = 0; q < kc; ++q) {
-      float wk;
-      const int wid = warp_best(key, e, has, wk);
-      if (has && wid == e) {
-        has = false;
-        cand_k[cbase + q] = key;
-        cand_s[cbase + q] = sv;
-        cand_id[cbase + q] = e;
-      }
-      if (wid == 0x7FFFFFFF && lane == 0) cand_id[cbase + q] = -1;   // block has fewer than kc experts
+    const uint32_t code = valid ? key_code(key) : 0xFFFFFFFFu;   // absent experts: last (id >= E)
+    int rank = 0;
+#pragma unroll 8
+    for (int src = 0; src < 32; ++src) {
+      const uint32_t c2 = __shfl_sync(0xffffffffu, code, src);
+      rank += (src != lane && code_before(c2, blockIdx.x * 32 + src, code, e)) ? 1 : 0;
     }
-    __threadfence();
+    const size_t cbase = (size_t)(t0 + r) * slots + (size_t)blockIdx.x * kc;
+    if (rank < kc) {
+      cand_c[cbase + rank] = code;
+      cand_s[cbase + rank] = sv;
+      cand_id[cbase + rank] = valid ? e : -1;
+    }
+    // the warp barrier orders the lanes' candidate stores before lane 0's release
     __syncwarp();
     int last = 0;
-    if (lane == 0) last = atomicAdd(tickets + t0 + r, 1) == (int)gridDim.x - 1;
+    if (lane == 0) {
+      int prev;
+      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + t0 + r) : "memory");
+      last = prev == (int)gridDim.x - 1;
+    }
     merge = __shfl_sync(0xffffffffu, last, 0) != 0;
   }
   cluster_sync_all();  // no CTA leaves, or reuses its shared memory, while another reads its partials
   if (!merge) return;
-  // merge (warp 0): the token's candidates, read once into shared memory (reusing the W slice)
-  // as (key, s, id); a selected candidate's id becomes -1
-  __threadfence();
+  // merge (warp 0): the token's nblk sorted lists of kc candidates go to shared memory (reusing the
+  // W slice); a candidate's rank among all of them is its rank in its own list plus, for every
+  // other list, the number of entries that come first (a binary search).  Ranks below k are the
+  // selection, in order.
   const int t = t0 + (int)r;
-  float* mk = Ws;
-  float* ms = mk + slots;
-  int* mid = reinterpret_cast<int*>(ms + slots);
+  const int nblk = gridDim.x;
+  uint32_t* mc = reinterpret_cast<uint32_t*>(Ws);
+  int* mid = reinterpret_cast<int*>(mc + slots);
+  float* ms = reinterpret_cast<float*>(mid + slots);
+  float* sel = ms + slots;   // [k] s of the selected, by rank
   const size_t cb = (size_t)t * slots;
-#pragma unroll 4
+  __syncwarp();   // lane 0's acquire comes first for every lane
   for (int c = lane; c < slots; c += 32) {
-    mk[c] = __ldcg(cand_k + cb + c);
-    ms[c] = __ldcg(cand_s + cb + c);
+    mc[c] = __ldcg(cand_c + cb + c);
     mid[c] = __ldcg(cand_id + cb + c);
+    ms[c] = __ldcg(cand_s + cb + c);
   }
   if (lane == 0) tickets[t] = 0;   // ready for the next call
   __syncwarp();
-  float my_s = 0.0f;
-  int my_id = 0;
-  for (int q = 0; q < k; ++q) {
-    float bk = 0.0f, bs = 0.0f;
-    int bid = -1, bc = -1;
-    for (int c = lane; c < slots; c += 32) {
-      const int id = mid[c];
-      if (id < 0) continue;
-      const float kv = mk[c];
-      if (bid < 0 || ranks_before(kv, id, bk, bid)) {
-        bk = kv;
-        bid = id;
-        bs = ms[c];
-        bc = c;
+  for (int c = lane; c < slots; c += 32) {
+    const int id = mid[c];
+    if (id < 0) continue;
+    const uint32_t code = mc[c];
+    const int b = c / kc;
+    int rank = c - b * kc;   // rank inside its own list
+    for (int b2 = 0; b2 < nblk; ++b2) {
+      if (b2 == b) continue;
+      // entries of list b2 before (code, id): the first position whose entry does not come first
+      int lo = 0, hi = kc;
+      while (lo < hi) {
+        const int mpos = (lo + hi) >> 1;
+        const int id2 = mid[b2 * kc + mpos];
+        const bool before = id2 >= 0 && code_before(mc[b2 * kc + mpos], id2, code, id);
+        if (before) lo = mpos + 1; else hi = mpos;
       }
+      rank += lo;
     }
-    float wk;
-    const int wid = warp_best(bk, bid, bid >= 0, wk);
-    const bool mine = bid >= 0 && bid == wid;
-    if (mine) mid[bc] = -1;
-    const int owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-    const float ws = __shfl_sync(0xffffffffu, bs, owner < 0 ? 0 : owner);
-    if (lane == q) {
-      my_s = ws;
-      my_id = wid;
+    if (rank < k) {
+      ids[(size_t)t * k + rank] = id;
+      sel[rank] = ms[c];
     }
-    __syncwarp();
   }
-  float S = 0.0f;
-  for (int q = 0; q < k; ++q) {
-    const float sq = __shfl_sync(0xffffffffu, my_s, q);
-    S = (q == 0) ? sq : __fadd_rn(S, sq);
-  }
+  __syncwarp();
   if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    wts[(size_t)t * k + lane] = __fdiv_rn(my_s, S);
+    float S = sel[0];
+    for (int q = 1; q < k; ++q) S = __fadd_rn(S, sel[q]);
+    wts[(size_t)t * k + lane] = __fdiv_rn(sel[lane], S);
   }
 }
 
@@ -623,7 +625,7 @@ cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias,
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
   const size_t small_smem = (size_t)(d / 32) * (RC_J * 32 + RC_J * SMALL_TT) * sizeof(float);
   if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() &&
-      small_smem >= (size_t)rc_slots(E, k) * 12) {
+      small_smem >= (size_t)rc_slots(E, k) * 12 + 32 * 4) {
     const size_t smem = small_smem;
     static int configured_dev = -1;
     static size_t configured_smem = 0;
@@ -636,13 +638,13 @@ cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias,
       configured_smem = smem;
     }
     const int slots = rc_slots(E, k);
-    float* cand_k = S;
+    uint32_t* cand_c = reinterpret_cast<uint32_t*>(S);
     float* cand_s = S + (size_t)T * slots;
     int* cand_id = reinterpret_cast<int*>(S + (size_t)2 * T * slots);
     dim3 grid((E + 31) / 32, RC_CLUSTER, (T + SMALL_TT - 1) / SMALL_TT);
     {
       const cudaError_t le = launch_k(route_cluster_kernel, dim3(grid), dim3(RC_THREADS), smem, s, x, w_r, bias, T,
-                                      d, E, k, cand_k, cand_s, cand_id, ticket, ids, w);
+                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w);
       if (le != cudaSuccess) return le;
     }
     return cudaGetLastError();
