@@ -872,11 +872,20 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
   const int KP = shared ? f.kp_s : f.kp_r;
   const int row = rg * 32 + lane, tile = row >> 4, r = row & 15;
   const float* pc = (shared ? f.part_s : f.part_r) + ((size_t)src * (rows / 16) + tile) * KP * 32 + r * 2;
+  // every part's load is issued before the sum (up to four at once)
   float gv = 0.0f, uv = 0.0f;
-  for (int q = 0; q < KP; ++q) {
-    const float2 v = *reinterpret_cast<const float2*>(pc + q * 32);
-    gv = q == 0 ? v.x : gv + v.x;
-    uv = q == 0 ? v.y : uv + v.y;
+  for (int q0 = 0; q0 < KP; q0 += 4) {
+    float2 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      v[q] = (q0 + q < KP) ? *reinterpret_cast<const float2*>(pc + (q0 + q) * 32) : make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q0 + q < KP) {
+        gv = (q0 + q == 0) ? v[q].x : gv + v[q].x;
+        uv = (q0 + q == 0) ? v[q].y : uv + v[q].y;
+      }
+    }
   }
   const float h = silu_mul(gv, uv);
   uint32_t hi, lo;

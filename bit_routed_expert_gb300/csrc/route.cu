@@ -315,12 +315,10 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   }
   cluster_sync_all();  // no CTA leaves, or reuses its shared memory, while another reads its partials
   if (!merge) return;
-  // merge (warp 0): the token's nblk sorted lists of kc candidates go to shared memory (reusing the
-  // W slice); a candidate's rank among all of them is its rank in its own list plus, for every
-  // other list, the number of entries that come first (a binary search).  Ranks below k are the
-  // selection, in order.
+  // merge (warp 0): the token's candidates (nblk lists of kc) go to shared memory (reusing the W
+  // slice); a candidate's rank among all of them is the number of candidates that come first.
+  // Ranks below k are the selection, in order.
   const int t = t0 + (int)r;
-  const int nblk = gridDim.x;
   uint32_t* mc = reinterpret_cast<uint32_t*>(Ws);
   int* mid = reinterpret_cast<int*>(mc + slots);
   float* ms = reinterpret_cast<float*>(mid + slots);
@@ -334,25 +332,19 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   }
   if (lane == 0) tickets[t] = 0;   // ready for the next call
   __syncwarp();
-  for (int c = lane; c < slots; c += 32) {
-    const int id = mid[c];
-    if (id < 0) continue;
-    const uint32_t code = mc[c];
-    const int b = c / kc;
-    int rank = c - b * kc;   // rank inside its own list
-    for (int b2 = 0; b2 < nblk; ++b2) {
-      if (b2 == b) continue;
-      // entries of list b2 before (code, id): the first position whose entry does not come first
-      int lo = 0, hi = kc;
-      while (lo < hi) {
-        const int mpos = (lo + hi) >> 1;
-        const int id2 = mid[b2 * kc + mpos];
-        const bool before = id2 >= 0 && code_before(mc[b2 * kc + mpos], id2, code, id);
-        if (before) lo = mpos + 1; else hi = mpos;
-      }
-      rank += lo;
+  // ranks by a linear scan: every lane compares its candidates with all slots (broadcast reads,
+  // no dependent chain; a binary search per list chained shared-memory latencies)
+  for (int c0 = 0; c0 < slots; c0 += 32) {
+    const int c = c0 + lane;
+    const int id = c < slots ? mid[c] : -1;
+    const uint32_t code = c < slots ? mc[c] : 0u;
+    int rank = 0;
+#pragma unroll 8
+    for (int c2 = 0; c2 < slots; ++c2) {
+      const int id2 = mid[c2];
+      rank += (id2 >= 0 && code_before(mc[c2], id2, code, id)) ? 1 : 0;
     }
-    if (rank < k) {
+    if (id >= 0 && rank < k) {
       ids[(size_t)t * k + rank] = id;
       sel[rank] = ms[c];
     }
