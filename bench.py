@@ -43,6 +43,25 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # environment
 # --------------------------------------------------------------------------- #
 
+def measured_traffic(name: str, source: str):
+    """DRAM bytes (read + write) per launch of a kernel, as captured by ncu and recorded in
+    profiles/<name>.md on a line 'traffic_bytes_per_call: N source_sha256: H'.  None when the
+    file is absent or the kernel source has changed since the capture (H differs)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    src = os.path.join(ROOT, "bit_routed_expert_gb300", "csrc", source)
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    for line in text.splitlines():
+        parts = line.replace("`", "").split()
+        if len(parts) >= 4 and parts[0] == "traffic_bytes_per_call:" and parts[2] == "source_sha256:":
+            return int(parts[1]) if parts[3] == digest else None
+    return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -194,8 +213,8 @@ class DecodeWorkload:
 
     @property
     def launches_per_step(self):
-        # route, permute, FFN prep, FFN gate/up, FFN down, combine (+ Engram)
-        return 7 if self.engram else 6
+        # route, permute, FFN prep, FFN gate/up, FFN finish, FFN down, combine (+ Engram)
+        return 8 if self.engram else 7
 
     def _engram_fork(self, ids):
         """The Engram gather does not depend on the MoE layer: it runs on a side stream (a
@@ -355,9 +374,11 @@ def run_prefill(args, ws, rank, local):
             "config": {"workload": "prefill MoE layer T=8192, Zipf(1.1) popularity via bias (V4.1 shape)",
                        "T": T, "pairs": P, "active_experts": int(info["n_active"].item()),
                        "algorithmic_tflop": round(flops / 1e12, 4), "l2": "flushed before every timed step"},
-            "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (grouped GEMM, two launches)",
+            "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (plan, gather, grouped GEMM x2)",
                          "achieved": round(tfl, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": round(tfl / pk["bf16_tflops"], 4), "traffic": None, "peak_source": pk["source"]},
+                         "frac": round(tfl / pk["bf16_tflops"], 4),
+                         "traffic": measured_traffic("prefill_T8192_ffn_traffic", "ffn_gemm.cu"),
+                         "peak_source": pk["source"]},
             "ffn_ms_median": round(statistics.median(ffn_ms), 4), "step_ms_median": round(statistics.median(ms), 4),
             "breakdown_us_median": bd, "clocks": clk}
 
@@ -533,9 +554,10 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": round(job_throughput(ws, T, K, total_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": K * wl.launches_per_step,
-        "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (prep + gate/up + down launches)",
+        "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (prep, gate/up, finish, down launches)",
                      "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": measured_traffic("decode_T8_ffn_traffic", "ffn_decode.cu"),
                      "peak_source": pk["source"], "bytes_per_launch_avg": int(np.mean(ffn_bytes))},
         "step_hbm_gbs": round(sum(step_bytes) / (sum(step_ms) * 1e-3) / 1e9, 1),
         "ffn_us_median": round(statistics.median(ffn_ms) * 1e3, 2),

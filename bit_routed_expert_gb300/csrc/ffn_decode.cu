@@ -37,7 +37,7 @@ namespace {
 constexpr int NS = 2;                 // ring stages per warp
 constexpr int STAGE = 5376;           // bytes per stage: 16 rows x 336 B of one matrix
 constexpr int MAX_WARPS = 12;         // phase 1 (at most 170 registers a thread)
-constexpr int MAX_WARPS_P2 = 8;       // phase 2 (at most 255 registers a thread)
+constexpr int MAX_WARPS_P2 = 12;      // phase 2 (at most 170 registers a thread)
 constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
@@ -469,18 +469,16 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
 __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb, int c, int nb, int g, int t,
                                              int pos_g, const uint16_t* __restrict__ hB,
                                              const uint16_t* __restrict__ HBm, uint32_t m43, float (&acc)[4]) {
+  // B of each block loads at the block's start; twelve warps an SM hide its latency (a second
+  // register set for the next block's B would leave room for eight)
   const int chunk_bytes = cb * Q2K_BB;
-  P2B B0, B1;
-  p2_load_b(B0, hB, HBm, pos_g, nb, c * cb, t);
-  for (int bl = 0; bl < cb; bl += 2) {
+#pragma unroll 1
+  for (int bl = 0; bl < cb; ++bl) {
     const int b = c * cb + bl;
-    if (bl + 1 < cb) p2_load_b(B1, hB, HBm, pos_g, nb, b + 1, t);
+    P2B B0;
+    p2_load_b(B0, hB, HBm, pos_g, nb, b, t);
     const uint16_t* hm = HBm + (((long long)pos_g * nb + b) * 4 + t) * 12;   // limbs of block b
     p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B0, hm, m43, acc);
-    if (bl + 1 < cb) {
-      if (bl + 2 < cb) p2_load_b(B0, hB, HBm, pos_g, nb, b + 2, t);
-      p2_q2k_block(stage + (bl + 1) * Q2K_BB, chunk_bytes, g, t, B1, hm + 48, m43, acc);
-    }
   }
 }
 
