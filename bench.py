@@ -213,8 +213,8 @@ class DecodeWorkload:
 
     @property
     def launches_per_step(self):
-        # route, permute, FFN prep, FFN gate/up, FFN finish, FFN down, combine (+ Engram)
-        return 8 if self.engram else 7
+        # route + permute (one launch at T <= 32), FFN prep, gate/up, finish, down, combine (+ Engram)
+        return 7 if self.engram else 6
 
     def _engram_fork(self, ids):
         """The Engram gather does not depend on the MoE layer: it runs on a side stream (a
@@ -261,9 +261,8 @@ class DecodeWorkload:
         L = self.layer
         x = self.xs[s]
         ev[0].record()
-        ids, w = api.moe_route(x, L.w_r, L.bias, L.k, ws=L.route_ws)
+        ids, w, perm = api.moe_route_permute(x, L.w_r, L.bias, L.k, ws=L.route_ws, dev_err=L.dev_err)
         ev[1].record()
-        perm = api.moe_permute(ids, L.E, dev_err=L.dev_err)
         ev[2].record()
         yp, ys = api.moe_expert_ffn(L.routed, L.shared, x, L.k, perm, ws=L.ffn_ws, dev_err=L.dev_err,
                                     y_pairs=L.y_pairs[:self.T * L.k], y_shared=L.y_shared[:self.T])
@@ -517,9 +516,9 @@ def run_ours(args, ws, rank, local):
         flush_l2(flush)
         wl.step_breakdown(i, evs)
     torch.cuda.synchronize()
-    names = ["route", "permute", "expert_ffn", "combine", "engram"]
+    names = ["route_permute", "", "expert_ffn", "combine", "engram"]
     breakdown = {n: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in bev) * 1e3, 2)
-                 for q, n in enumerate(names)}
+                 for q, n in enumerate(names) if n}
 
     total_ms = max_over_ranks(ws, sum(step_ms))
     total_e2e = max_over_ranks(ws, sum(e2e_ms))

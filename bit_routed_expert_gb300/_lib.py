@@ -23,6 +23,7 @@ SIGNATURES = {
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_route_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_permute": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _P]),

@@ -80,6 +80,31 @@ def moe_permute(ids, E: int, dev_err=None, stream=None, out=None):
     return out
 
 
+def moe_route_permute(x, w_r, bias, k: int, ws=None, dev_err=None, stream=None, ids=None, w=None, out=None):
+    """moe_route then moe_permute as one call; returns (ids, w, perm dict)."""
+    L = _lib.load()
+    T, d = x.shape
+    E = w_r.shape[1]
+    _dev(x, "x"), _dev(w_r, "w_r")
+    dv = x.device
+    if ws is None:
+        ws = torch.zeros(L.moe_route_workspace(T, E), dtype=torch.uint8, device=dv)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=dv)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=dv)
+    if out is None:
+        out = dict(offsets=torch.empty(E + 1, dtype=torch.int32, device=dv),
+                   perm=torch.empty(T * k, dtype=torch.int32, device=dv),
+                   inv=torch.empty(T * k, dtype=torch.int32, device=dv),
+                   active=torch.empty(E, dtype=torch.int32, device=dv),
+                   n_active=torch.empty(1, dtype=torch.int32, device=dv))
+    check(L.moe_route_permute(ptr(x), ptr(w_r), ptr(bias), T, d, E, k, ptr(ids), ptr(w), ptr(out["offsets"]),
+                              ptr(out["perm"]), ptr(out["inv"]), ptr(out["active"]), ptr(out["n_active"]),
+                              ptr(dev_err), ptr(ws), ws.numel(), stream_handle(stream)), "moe_route_permute")
+    return ids, w, out
+
+
 def moe_expert_ffn_workspace(T: int, k: int, E: int, d: int, d_ff: int, d_ff_shared: int) -> int:
     return _lib.load().moe_expert_ffn_workspace(T, k, E, d, d_ff, d_ff_shared)
 
@@ -152,7 +177,7 @@ def bre_dequant(fmt: int, blocks, stream=None):
 
 class MoeLayer:
     """One MoE layer resident on the device, with its workspaces; forward() runs
-    route -> permute -> expert FFN (routed + shared) -> combine."""
+    route + permute (one call) -> expert FFN (routed + shared) -> combine."""
 
     def __init__(self, w_r, bias, routed: FfnWeights, shared: FfnWeights | None, k: int, T_max: int):
         self.w_r, self.bias, self.routed, self.shared, self.k = w_r, bias, routed, shared, k
@@ -180,12 +205,12 @@ class MoeLayer:
         """ffn_events: optional (start, end) CUDA events recorded around the expert FFN call;
         out_f32: optional [T, d] FP32 tensor for the layer output before BF16 rounding."""
         T = x.shape[0]
-        ids, w = moe_route(x, self.w_r, self.bias, self.k, ws=self.route_ws, stream=stream,
-                           ids=self.ids[:T], w=self.w[:T])
         pb = self.perm_buf
-        perm = moe_permute(ids, self.E, dev_err=self.dev_err, stream=stream,
-                           out=dict(offsets=pb["offsets"], perm=pb["perm"][:T * self.k], inv=pb["inv"][:T * self.k],
-                                    active=pb["active"], n_active=pb["n_active"]))
+        ids, w, perm = moe_route_permute(x, self.w_r, self.bias, self.k, ws=self.route_ws, dev_err=self.dev_err,
+                                         stream=stream, ids=self.ids[:T], w=self.w[:T],
+                                         out=dict(offsets=pb["offsets"], perm=pb["perm"][:T * self.k],
+                                                  inv=pb["inv"][:T * self.k], active=pb["active"],
+                                                  n_active=pb["n_active"]))
         s = stream if stream is not None else torch.cuda.current_stream()
         if ffn_events is not None:
             ffn_events[0].record(s)

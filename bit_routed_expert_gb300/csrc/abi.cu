@@ -69,6 +69,21 @@ bre_status moe_route(const void* x_bf16, const float* w_r, const float* bias, in
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+bre_status moe_route_permute(const void* x_bf16, const float* w_r, const float* bias, int T, int d, int E, int k,
+                             int32_t* topk_ids, float* topk_w, int32_t* offsets, int32_t* perm, int32_t* inv,
+                             int32_t* active, int32_t* n_active, int32_t* dev_err, void* ws, size_t ws_bytes,
+                             bre_stream_t stream) {
+  if (!x_bf16 || !w_r || !topk_ids || !topk_w || !offsets || !perm || !inv || !active || !n_active || T <= 0 ||
+      d <= 0 || E <= 0 || k <= 0)
+    return BRE_ERR_ARG;
+  if (k > E || k > 32 || E > 1024 || d % 32 != 0) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(w_r, 16)) return BRE_ERR_ARG;
+  if (!ws || ws_bytes < route_ws_bytes(T, E) || !aligned(ws, 256)) return BRE_ERR_WORKSPACE;
+  return cuda_status(launch_route_permute(static_cast<const uint16_t*>(x_bf16), w_r, bias, T, d, E, k, topk_ids,
+                                          topk_w, offsets, perm, inv, active, n_active, dev_err, ws,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bre_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
                        int32_t* active, int32_t* n_active, int32_t* dev_err, bre_stream_t stream) {
   if (!topk_ids || !offsets || !perm || !inv || !active || !n_active || T <= 0 || k <= 0 || E <= 0)

@@ -188,11 +188,21 @@ __device__ __forceinline__ bool code_before(uint32_t ca, int ia, uint32_t cb, in
 // block; id = -1 for an empty slot (a block with fewer than kc experts).
 __host__ __device__ __forceinline__ int rc_slots(int E, int k) { return ((E + 31) / 32) * (k < 32 ? k : 32); }
 
+// Outputs of the permutation when the router kernel also permutes (offsets == nullptr: it does not).
+struct PermOut {
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* active;
+  int32_t* n_active;
+};
+constexpr int RC_TOKENS_DONE = 32;   // ticket index counting merged tokens (token tickets use 0..31)
+
 __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     route_cluster_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w_r,
                          const float* __restrict__ bias, int T, int d, int E, int k, uint32_t* __restrict__ cand_c,
                          float* __restrict__ cand_s, int* __restrict__ cand_id, int* tickets,
-                         int32_t* __restrict__ ids, float* __restrict__ wts) {
+                         int32_t* __restrict__ ids, float* __restrict__ wts, const PermOut po) {
   extern __shared__ __align__(16) float rc_smem[];
   __shared__ float part[SMALL_TT][RC_J][33];     // partial sums of this CTA's j, padded
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -354,6 +364,76 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     float S = sel[0];
     for (int q = 1; q < k; ++q) S = __fadd_rn(S, sel[q]);
     wts[(size_t)t * k + lane] = __fdiv_rn(sel[lane], S);
+  }
+  if (po.offsets == nullptr) return;
+  // the last token merged (second-level ticket) permutes all T * k pairs: stable counting sort by
+  // expert id in one warp (ids are in [0, E) by construction)
+  __syncwarp();
+  int lastp = 0;
+  if (lane == 0) {
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + RC_TOKENS_DONE) : "memory");
+    lastp = prev == T - 1;
+    if (lastp) tickets[RC_TOKENS_DONE] = 0;   // ready for the next call
+  }
+  if (!__shfl_sync(0xffffffffu, lastp, 0)) return;
+  __syncwarp();
+  int* cnt = reinterpret_cast<int*>(sel + 32);   // [E + 1], then the running counts [E + 1]
+  int* run = cnt + (E + 1);
+  for (int i = lane; i <= E; i += 32) {
+    cnt[i] = 0;
+    run[i] = 0;
+  }
+  __syncwarp();
+  const int P = T * k;
+  for (int q = lane; q < P; q += 32) atomicAdd(&cnt[__ldcg(ids + q)], 1);
+  __syncwarp();
+  // exclusive scan of the counts; lane l takes experts [l * per, (l + 1) * per)
+  const int per = (E + 31) / 32, a0 = min(E, lane * per), a1 = min(E, a0 + per);
+  int sum = 0, nact = 0;
+  for (int i = a0; i < a1; ++i) {
+    sum += cnt[i];
+    nact += cnt[i] > 0 ? 1 : 0;
+  }
+  int ps = sum, pa = nact;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ys = __shfl_up_sync(0xffffffffu, ps, o), ya = __shfl_up_sync(0xffffffffu, pa, o);
+    if (lane >= o) {
+      ps += ys;
+      pa += ya;
+    }
+  }
+  int base = ps - sum, abase = pa - nact;
+  for (int i = a0; i < a1; ++i) {
+    const int c = cnt[i];
+    po.offsets[i] = base;
+    cnt[i] = base;
+    if (c > 0) po.active[abase++] = i;
+    base += c;
+  }
+  const int total_act = __shfl_sync(0xffffffffu, pa, 31);
+  if (lane == 31) {
+    po.offsets[E] = ps;
+    *po.n_active = pa;
+  }
+  for (int i = total_act + lane; i < E; i += 32) po.active[i] = -1;
+  __syncwarp();
+  // pairs in chunks of 32, in order; rank among equal ids from a warp match
+  const unsigned lt = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < P; c0 += 32) {
+    const int q = c0 + lane;
+    const int key = q < P ? __ldcg(ids + q) : E;
+    const unsigned m = __match_any_sync(0xffffffffu, key);
+    const int lr = __popc(m & lt);
+    if (q < P) {
+      const int pos = cnt[key] + run[key] + lr;
+      po.perm[pos] = q;
+      po.inv[q] = pos;
+    }
+    __syncwarp();
+    if (q < P && lr == 0) run[key] += __popc(m);
+    __syncwarp();
   }
 }
 
@@ -609,15 +689,39 @@ size_t route_ws_bytes(int T, int E) {
   return s + 256;
 }
 
+namespace {
+cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                       int32_t* ids, float* w, void* ws, const PermOut& po, bool* permuted, cudaStream_t s);
+}
+
 cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                          int32_t* ids, float* w, void* ws, cudaStream_t s) {
+  bool permuted = false;
+  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, &permuted, s);
+}
+
+cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                 int32_t* active, int32_t* n_active, int32_t* err, void* ws, cudaStream_t s) {
+  bool permuted = false;
+  const cudaError_t e =
+      route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, &permuted, s);
+  if (e != cudaSuccess || permuted) return e;
+  return launch_permute(ids, T, k, E, offsets, perm, inv, active, n_active, err, s);
+}
+
+namespace {
+cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                       int32_t* ids, float* w, void* ws, const PermOut& po, bool* permuted, cudaStream_t s) {
   // one ticket per token of the small-batch kernel, at fixed offsets so that calls with
   // different T share them
   int* ticket = reinterpret_cast<int*>(ws);
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
   const size_t small_smem = (size_t)(d / 32) * (RC_J * 32 + RC_J * SMALL_TT) * sizeof(float);
-  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() &&
-      small_smem >= (size_t)rc_slots(E, k) * 12 + 32 * 4) {
+  // merge area: candidates (12 bytes a slot) + 32 selected s; then, when permuting, two count arrays
+  const size_t merge_bytes = (size_t)rc_slots(E, k) * 12 + 32 * 4;
+  const bool can_permute = po.offsets != nullptr && small_smem >= merge_bytes + (size_t)8 * (E + 1);
+  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() && small_smem >= merge_bytes) {
     const size_t smem = small_smem;
     static int configured_dev = -1;
     static size_t configured_smem = 0;
@@ -636,9 +740,11 @@ cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias,
     dim3 grid((E + 31) / 32, RC_CLUSTER, (T + SMALL_TT - 1) / SMALL_TT);
     {
       const cudaError_t le = launch_k(route_cluster_kernel, dim3(grid), dim3(RC_THREADS), smem, s, x, w_r, bias, T,
-                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w);
+                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w,
+                                      can_permute ? po : PermOut{});
       if (le != cudaSuccess) return le;
     }
+    *permuted = can_permute;
     return cudaGetLastError();
   }
   static int tiled_dev = -1;
@@ -664,6 +770,7 @@ cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias,
   }
   return cudaGetLastError();
 }
+}  // namespace
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
                            int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s) {

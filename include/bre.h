@@ -138,6 +138,16 @@ bre_status moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *of
                        int32_t *inv, int32_t *active, int32_t *n_active, int32_t *dev_err,
                        bre_stream_t stream);
 
+/* moe_route followed by moe_permute, with the same arguments and outputs as the two calls
+ * (ws: moe_route_workspace(T, E) bytes, zero-filled once after allocation).  For batches of
+ * at most 32 tokens the router kernel's last merging warp also builds the permutation, so the
+ * pair is one launch; otherwise the two kernels run back to back on `stream`.  Router ids are
+ * always in [0, E), so dev_err is only touched by the second form. */
+bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
+                             int32_t *topk_ids, float *topk_w, int32_t *offsets, int32_t *perm, int32_t *inv,
+                             int32_t *active, int32_t *n_active, int32_t *dev_err, void *ws, size_t ws_bytes,
+                             bre_stream_t stream);
+
 /* Routed expert FFN plus the always-on shared expert ([S] V4-Flash "How it
  * works", finish step; "Verifying it"): for every active expert e and each of
  * its pairs p (token t = p / k):

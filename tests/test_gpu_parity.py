@@ -176,6 +176,32 @@ def test_route_odd_shapes(cuda_dev, T, d, E, k):
     assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("shape,T", [(synth.TINY, 4), (synth.V41, 1), (synth.V41, 8), (synth.V41, 5),
+                                     (synth.V41, 17), (synth.V41, 32), (synth.V41, 33), (synth.TINY, 300)])
+def test_route_permute_fused(cuda_dev, shape, T):
+    """moe_route_permute equals the oracle's route followed by its permutation (one launch up to
+    32 tokens, two above)."""
+    x = synth.x_bf16(SEED, 0, 9, T, shape.d)
+    w_r = synth.router_weight(SEED, 0, shape.d, shape.E)
+    b = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width)
+    ids_ref, w_ref = oracle.route(x, w_r, b, shape.k)
+    ref = oracle.permute(ids_ref, shape.E)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    ws = torch.zeros(api.moe_route_workspace(T, shape.E), dtype=torch.uint8, device=cuda_dev)
+    for _ in range(2):   # the second call reuses the workspace (its counters must be back at zero)
+        ids, w, got = api.moe_route_permute(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), shape.k, ws=ws,
+                                            dev_err=err)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+        for key in ("offsets", "perm", "inv"):
+            assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+        na = int(got["n_active"])
+        assert na == ref["n_active"]
+        assert np.array_equal(got["active"].cpu().numpy()[:na], ref["active"])
+        assert np.all(got["active"].cpu().numpy()[na:] == -1)
+    assert int(err) == 0
+
+
 def test_route_ties_and_zero_bias(cuda_dev):
     d, E, k = 64, 16, 6
     x = synth.x_bf16(2, 0, 0, 3, d)
