@@ -36,13 +36,15 @@ namespace {
 
 constexpr int NS = 2;                 // ring stages per warp
 constexpr int STAGE = 5376;           // bytes per stage: 16 rows x 336 B of one matrix
-constexpr int MAX_WARPS = 12;         // phase 1 (at most 170 registers a thread)
-constexpr int MAX_WARPS_P2 = 12;      // phase 2 (at most 170 registers a thread)
+constexpr int MAX_WARPS = 16;         // phase 1 (at most 128 registers a thread; fewer when the
+                                      // activation package leaves less shared memory)
+constexpr int MAX_WARPS_P2 = 16;      // phase 2 (at most 128 registers a thread)
 constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
-constexpr int BAR_BYTES = 256;                  // mbarrier region: MAX_WARPS * NS ring barriers + package
+constexpr int BAR_BYTES = 512;                  // mbarrier region: MAX_WARPS * NS ring barriers + package
+static_assert((MAX_WARPS * NS + 1) * 8 <= BAR_BYTES, "mbarrier region too small");
 
 // n / d as a multiply and shift, for 0 <= n < 2^31 (round-up multiplier m = ceil(2^(31+l) / d),
 // 2^l >= d; the error n (m - 2^(31+l)/d) / 2^(31+l) stays below 1/d, so the floor is exact).
@@ -77,7 +79,7 @@ struct DecParams {
   const int32_t* active;
   const int32_t* n_active;
   int E;
-  uint16_t* hB;   // routed h, permuted, 2 limbs: [P][F/256][4][4][4][2][4]
+  uint16_t* hB;   // routed h (BF16), permuted: [P][F/256][4][4][4][4]
   uint16_t* HBm;  // routed sub-block sums of h, 3 limbs: [P][F/256][4][3][4]
   uint16_t* hS;   // shared h, natural, 2 limbs: [T][2][Fs]
   float* HS16;    // shared 16-row sums of h: [T][Fs/16]
@@ -117,7 +119,7 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
   Item it;
   it.id = id;
   if (id < 0) return it;
-  const int kps = (PHASE == 1) ? p.kp_s : 1, kpr = (PHASE == 1) ? p.kp_r : 1;   // phase 2 is not split
+  const int kps = p.kp_s, kpr = p.kp_r;
   if (id < tiles_s * kps) {
     it.shared = true;
     it.tile = fdiv(id, p.fd_kps);
@@ -230,6 +232,17 @@ __device__ __forceinline__ void q2k_scale_pairs(uint32_t sclo, int jj, uint32_t&
   nsc2 = bf16x2_fma(u, 0xC300C300u, 0x46804680u);                                         // 16384 - 128 u
 }
 
+// A fragments of the min-term MMA: the 4-bit mins of the lane's four sub-blocks for rows g
+// (scales word sw0) and g + 8 (sw1) as exact BF16 pairs, m = (128 + m) - 128.
+__device__ __forceinline__ void min_frags(uint32_t sw0, uint32_t sw1, uint32_t& A0, uint32_t& A1, uint32_t& A2,
+                                          uint32_t& A3) {
+  const uint32_t mg = (sw0 >> 4) & 0x0F0F0F0Fu, mg8 = (sw1 >> 4) & 0x0F0F0F0Fu;
+  A0 = bf16x2_fma(prmt(mg, C43, SEL_LO), 0x3F803F80u, 0xC300C300u);
+  A1 = bf16x2_fma(prmt(mg8, C43, SEL_LO), 0x3F803F80u, 0xC300C300u);
+  A2 = bf16x2_fma(prmt(mg, C43, SEL_HI), 0x3F803F80u, 0xC300C300u);
+  A3 = bf16x2_fma(prmt(mg8, C43, SEL_HI), 0x3F803F80u, 0xC300C300u);
+}
+
 // Q8_0 nibble planes of one row word (4 consecutive int8): (128+lo) and (128+hi') pairs.
 __device__ __forceinline__ void q80_frag(uint32_t w, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
                                          uint32_t& hi23) {
@@ -250,7 +263,6 @@ template <int CB>
 __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt, int c, int g, int t,
                                            const unsigned char* xb_g,    // permuted x of column g
                                            const unsigned char* xbm_g,   // XBm of column g
-                                           const float* xbM0, const float* xbM1,  // XbM rows of columns 2t, 2t+1
                                            uint32_t m43, float (&acc)[4]) {
   const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q2K_BB;
@@ -266,8 +278,9 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
     }
-    // one accumulator per jj: four independent MMA chains, each started by a C = 0 MMA
-    float P[4][4], M[4];
+    // one accumulator chain, started by a C = 0 MMA (the MMAs are far apart in the instruction
+    // stream, so the chain costs no waiting)
+    float P[4], M[4];
     const unsigned char* xblk = xb_g + b * 512;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
@@ -284,17 +297,16 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
         a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
         a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
         a3 = bf16x2_fma(a3, sc2[1], nsc2[1]);
-        if (s == 0)
-          mma_bf16_16816_z(P[jj], a0, a1, a2, a3, bv.x, bv.y);
+        if (jj == 0 && s == 0)
+          mma_bf16_16816_z(P, a0, a1, a2, a3, bv.x, bv.y);
         else
-          mma_bf16_16816(P[jj], a0, a1, a2, a3, bv.x, bv.y);
+          mma_bf16_16816(P, a0, a1, a2, a3, bv.x, bv.y);
       }
     }
-    // min term: M' = sum_j (128 + m_j) X_j over the 16 sub-blocks, X_j in three limbs
+    // min term: M = sum_j m_j X_j over the 16 sub-blocks, X_j in three limbs
     {
-      const uint32_t mg = (sw[0] >> 4) & 0x0F0F0F0Fu, mg8 = (sw[1] >> 4) & 0x0F0F0F0Fu;
-      const uint32_t A0 = prmt(mg, C43, SEL_LO), A1 = prmt(mg8, C43, SEL_LO);
-      const uint32_t A2 = prmt(mg, C43, SEL_HI), A3 = prmt(mg8, C43, SEL_HI);
+      uint32_t A0, A1, A2, A3;
+      min_frags(sw[0], sw[1], A0, A1, A2, A3);
 #pragma unroll
       for (int limb = 0; limb < 3; ++limb) {
         const uint2 bm = *reinterpret_cast<const uint2*>(xbm_g + ((b * 4 + t) * 3 + limb) * 8);
@@ -304,15 +316,11 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
           mma_bf16_16816(M, A0, A1, A2, A3, bm.x, bm.y);
       }
     }
-    const float x0 = xbM0[b], x1 = xbM1[b];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t ddv = dd[i >> 1];
       const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
-      const float xs = (i & 1) ? x1 : x0;
-      const float psum = (P[0][i] + P[1][i]) + (P[2][i] + P[3][i]);
-      const float mv = fmaf(-128.0f, xs, M[i]);
-      acc[i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[i]));
+      acc[i] = fmaf(dv, P[i], fmaf(-dmv, M[i], acc[i]));
     }
   }
 }
@@ -368,21 +376,24 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
   }
 }
 
-// B operand of one block for column g: 16 uint4 (both limbs of h, fragment order).
+// B operand of one block for column g: 16 uint2 (h in BF16, fragment order).
 struct P2B {
-  uint4 v[16];
+  uint2 v[16];
 };
 
-__device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, const uint16_t* __restrict__,
-                                          int pos_g, int nb, int b, int t) {
-  const uint16_t* hblk = hB + ((long long)pos_g * nb + b) * 512;
+__device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, int pos_g, int nb, int b, int t) {
+  const uint16_t* hblk = hB + ((long long)pos_g * nb + b) * 256;
 #pragma unroll
-  for (int q = 0; q < 16; ++q) B.v[q] = __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8));
+  for (int q = 0; q < 16; ++q) B.v[q] = __ldg(reinterpret_cast<const uint2*>(hblk + (q * 4 + t) * 4));
 }
 
 // One 256-column block of 16 rows of the down projection.
-__device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_bytes, int g, int t, const P2B& B,
-                                             const uint16_t* __restrict__ hm, uint32_t m43, float (&acc)[4]) {
+// B holds this block's h on entry; each sub-block step, once its MMAs are issued, refills its
+// registers with the same step of hnext (the next block's h), so that those loads have a
+// whole block of work to arrive.
+__device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_bytes, int g, int t, P2B& B,
+                                             const uint16_t* __restrict__ hnext, const uint16_t* __restrict__ hm,
+                                             uint32_t m43, float (&acc)[4]) {
   // the three limbs of the sub-block sums are first needed at the block's end: loaded here
   uint2 bm[3];
 #pragma unroll
@@ -396,45 +407,37 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
   }
-  float P[4][4], M[4];
-  // s outer, jj inner: consecutive MMAs go to different accumulators
-  uint32_t sc2[4][2], nsc2[4][2];
+  // jj outer, s inner (one sub-block's scales live at a time); consecutive MMAs alternate
+  // between two accumulators
+  float P[2][4], M[4];
+  const uint32_t sl0 = sw[0] & 0x0F0F0F0Fu, sl1 = sw[1] & 0x0F0F0F0Fu;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    q2k_scale_pairs(sw[0] & 0x0F0F0F0Fu, jj, sc2[jj][0], nsc2[jj][0]);
-    q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, jj, sc2[jj][1], nsc2[jj][1]);
-  }
+    uint32_t sc2[2], nsc2[2];
+    q2k_scale_pairs(sl0, jj, sc2[0], nsc2[0]);
+    q2k_scale_pairs(sl1, jj, sc2[1], nsc2[1]);
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    uint32_t A[4][4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      q2k_pairs(qw[0][jj], s, m43, A[jj][0], A[jj][2]);
-      q2k_pairs(qw[1][jj], s, m43, A[jj][1], A[jj][3]);
-      A[jj][0] = bf16x2_fma(A[jj][0], sc2[jj][0], nsc2[jj][0]);
-      A[jj][2] = bf16x2_fma(A[jj][2], sc2[jj][0], nsc2[jj][0]);
-      A[jj][1] = bf16x2_fma(A[jj][1], sc2[jj][1], nsc2[jj][1]);
-      A[jj][3] = bf16x2_fma(A[jj][3], sc2[jj][1], nsc2[jj][1]);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint4 bv = B.v[jj * 4 + s];
-      if (s == 0)
-        mma_bf16_16816_z(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.x, bv.y);
+    for (int s = 0; s < 4; ++s) {
+      uint32_t a0, a1, a2, a3;
+      q2k_pairs(qw[0][jj], s, m43, a0, a2);
+      q2k_pairs(qw[1][jj], s, m43, a1, a3);
+      a0 = bf16x2_fma(a0, sc2[0], nsc2[0]);
+      a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
+      a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
+      a3 = bf16x2_fma(a3, sc2[1], nsc2[1]);
+      const uint2 bv = B.v[jj * 4 + s];
+      if (jj == 0 && s < 2)
+        mma_bf16_16816_z(P[s & 1], a0, a1, a2, a3, bv.x, bv.y);
       else
-        mma_bf16_16816(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.x, bv.y);
+        mma_bf16_16816(P[s & 1], a0, a1, a2, a3, bv.x, bv.y);
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint4 bv = B.v[jj * 4 + s];
-      mma_bf16_16816(P[jj], A[jj][0], A[jj][1], A[jj][2], A[jj][3], bv.z, bv.w);
-    }
+    for (int s = 0; s < 4; ++s)
+      B.v[jj * 4 + s] = __ldg(reinterpret_cast<const uint2*>(hnext + ((jj * 4 + s) * 4 + t) * 4));
   }
-  float hsum = 0.0f;
   {
-    const uint32_t mg = (sw[0] >> 4) & 0x0F0F0F0Fu, mg8 = (sw[1] >> 4) & 0x0F0F0F0Fu;
-    const uint32_t A0 = prmt(mg, C43, SEL_LO), A1 = prmt(mg8, C43, SEL_LO);
-    const uint32_t A2 = prmt(mg, C43, SEL_HI), A3 = prmt(mg8, C43, SEL_HI);
+    uint32_t A0, A1, A2, A3;
+    min_frags(sw[0], sw[1], A0, A1, A2, A3);
 #pragma unroll
     for (int limb = 0; limb < 3; ++limb) {
       const uint2 b2 = bm[limb];
@@ -442,43 +445,34 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
         mma_bf16_16816_z(M, A0, A1, A2, A3, b2.x, b2.y);
       else
         mma_bf16_16816(M, A0, A1, A2, A3, b2.x, b2.y);
-      hsum += bf16_bits_to_f32(b2.x & 0xFFFFu) + bf16_bits_to_f32(b2.x >> 16) + bf16_bits_to_f32(b2.y & 0xFFFFu) +
-              bf16_bits_to_f32(b2.y >> 16);
     }
   }
-  // block sum of h for column g, then for the C-fragment columns 2t and 2t+1
-  hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
-  hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
-  const float x0 = __shfl_sync(0xffffffffu, hsum, (2 * t) * 4);
-  const float x1 = __shfl_sync(0xffffffffu, hsum, (2 * t + 1) * 4);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t ddv = dd[i >> 1];
     const float dv = f16_bits_to_f32(ddv & 0xFFFFu), dmv = f16_bits_to_f32(ddv >> 16);
-    const float xs = (i & 1) ? x1 : x0;
-    const float psum = (P[0][i] + P[1][i]) + (P[2][i] + P[3][i]);
-    const float mv = fmaf(-128.0f, xs, M[i]);
-    acc[i] = fmaf(dv, psum, fmaf(-dmv, mv, acc[i]));
+    acc[i] = fmaf(dv, P[0][i] + P[1][i], fmaf(-dmv, M[i], acc[i]));
   }
 }
 
 // ----------------------------------------------------------------------------
-// phase 2, routed Q2_K down: 16 rows over one chunk; B = h limbs from global memory, loaded
-// one block ahead (two register sets) so that their latency hides behind a block of MMAs
+// phase 2, routed Q2_K down: 16 rows over one chunk; B = h from global memory, one register
+// set refilled a block ahead (the last block of the chunk refills from itself, an L1 hit)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb, int c, int nb, int g, int t,
                                              int pos_g, const uint16_t* __restrict__ hB,
                                              const uint16_t* __restrict__ HBm, uint32_t m43, float (&acc)[4]) {
-  // B of each block loads at the block's start; twelve warps an SM hide its latency (a second
-  // register set for the next block's B would leave room for eight)
   const int chunk_bytes = cb * Q2K_BB;
+  const int b0 = c * cb;
+  const uint16_t* hcol = hB + (long long)pos_g * nb * 256;              // h of column g, block 0
+  const uint16_t* hmcol = HBm + ((long long)pos_g * nb * 4 + t) * 12;   // its sub-block sum limbs
+  P2B B;
+  p2_load_b(B, hB, pos_g, nb, b0, t);
 #pragma unroll 1
   for (int bl = 0; bl < cb; ++bl) {
-    const int b = c * cb + bl;
-    P2B B0;
-    p2_load_b(B0, hB, HBm, pos_g, nb, b, t);
-    const uint16_t* hm = HBm + (((long long)pos_g * nb + b) * 4 + t) * 12;   // limbs of block b
-    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B0, hm, m43, acc);
+    const int b = b0 + bl;
+    const int bn = bl + 1 < cb ? b + 1 : b;
+    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B, hcol + bn * 256, hmcol + b * 48, m43, acc);
   }
 }
 
@@ -550,7 +544,7 @@ __device__ __forceinline__ float silu_mul(float gv, float uv) { return gv / (1.0
 // once per call by ffn_prep_kernel and copied whole into shared memory by phase 1.
 // ----------------------------------------------------------------------------
 struct PkgLayout {
-  int xB, XBm, XbM, X32, total;
+  int xB, XBm, X32, total;
 };
 
 __host__ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
@@ -560,18 +554,16 @@ __host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
   PkgLayout L;
   L.xB = 0;
   L.XBm = T * xstride;
-  L.XbM = L.XBm + T * nbx * 96;
-  L.X32 = L.XbM + round16(T * nbx * 4);
+  L.X32 = L.XBm + T * nbx * 96;
   L.total = L.X32 + round16(T * (d / 32) * 4);
   return L;
 }
 
 // grid (d/256, T), 256 threads: thread i owns value k = 256*b + i of token t.
 //   xB: x (BF16) permuted into the Q2_K fragment order; XBm: 16-value sub-block sums as
-//   three BF16 limbs; XbM: their block total; X32: 32-value sums (Q8_0 shared expert).
+//   three BF16 limbs; X32: 32-value sums (Q8_0 shared expert).
 __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restrict__ x, int T, int d,
                                                        unsigned char* __restrict__ pkg) {
-  __shared__ float sub_limbs[16];
   pdl_wait();
   const int b = blockIdx.x, t = blockIdx.y, i = threadIdx.x, lane = i & 31;
   const int nbx = d / 256;
@@ -605,13 +597,6 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
     dst[0] = (uint16_t)hi;
     dst[4] = (uint16_t)mid;
     dst[8] = (uint16_t)lo;
-    sub_limbs[j] = (bf16_bits_to_f32(hi) + bf16_bits_to_f32(mid)) + bf16_bits_to_f32(lo);
-  }
-  __syncthreads();
-  if (i == 0) {
-    float sacc = 0.0f;
-    for (int j = 0; j < 16; ++j) sacc += sub_limbs[j];
-    reinterpret_cast<float*>(pkg + L.XbM)[(size_t)t * nbx + b] = sacc;
   }
 }
 
@@ -647,7 +632,7 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
   const int n_act = *p.n_active;
   const int tiles_s = p.has_shared ? p.rows_s / 16 : 0;
   const int tiles_r = p.rows_r / 16;
-  const int n_items = (PHASE == 1) ? tiles_s * p.kp_s + n_act * tiles_r * p.kp_r : tiles_s + n_act * tiles_r;
+  const int n_items = tiles_s * p.kp_s + n_act * tiles_r * p.kp_r;
 
   unsigned char* my_stage = stages + warp * NS * STAGE;
   uint64_t* my_bar = bars + warp * NS;
@@ -712,7 +697,6 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
   const int nbx = d / 256;
   unsigned char* xB = xprep + PL.xB;                                   // [T][xstride]
   unsigned char* XBm = xprep + PL.XBm;                                 // [T][nbx][4][3][4] bf16
-  float* XbM = reinterpret_cast<float*>(xprep + PL.XbM);              // [T][nbx]
   float* X32 = reinterpret_cast<float*>(xprep + PL.X32);              // [T][d/32]
   if (PHASE == 1) {
     if (!mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT)) {
@@ -772,12 +756,10 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
         } else {
           const unsigned char* xb = xB + (size_t)dg * p.xstride;
           const unsigned char* xm = XBm + (size_t)dg * nbx * 96;
-          const float* x0 = XbM + d0 * nbx;
-          const float* x1 = XbM + d1 * nbx;
           if (it.cb == 4)
-            p1_q2k_mat<4>(stage, 4, c, g, t, xb, xm, x0, x1, p.m43, accm);
+            p1_q2k_mat<4>(stage, 4, c, g, t, xb, xm, p.m43, accm);
           else
-            p1_q2k_mat<0>(stage, it.cb, c, g, t, xb, xm, x0, x1, p.m43, accm);
+            p1_q2k_mat<0>(stage, it.cb, c, g, t, xb, xm, p.m43, accm);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -896,12 +878,12 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
   } else {
     const int b2 = row >> 8, j = (row >> 4) & 15, ip = row & 15;
     const int byte = ip >> 2, s = ip & 3, v4 = (byte & 1) * 2 + (byte >> 1);
-    // limbs of h * 4^-min(s,2) (the down projection's A fragments keep codes in place)
-    uint32_t shi, slo;
-    split_bf16x2(__fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f)), shi, slo);
-    const size_t base = ((((size_t)src * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 8 + (size_t)(j >> 2) * 8;
-    f.hB[base + v4] = (uint16_t)shi;
-    f.hB[base + 4 + v4] = (uint16_t)slo;
+    // BF16 of h * 4^-min(s,2) (the down projection's A fragments keep codes in place); a power
+    // of two commutes with the rounding, so the 16-row sums below use h rounded to BF16
+    const float hs = __fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f));
+    const size_t base = ((((size_t)src * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 4 + (size_t)(j >> 2) * 4;
+    f.hB[base + v4] = (uint16_t)f32_to_bf16_rne(hs);
+    hq = bf16_bits_to_f32(f32_to_bf16_rne(h));
   }
   // 16-row sums of the limb values (half warps)
 #pragma unroll
@@ -974,20 +956,18 @@ struct DecWs {
 
 DecWs dec_ws_layout(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
-  int kpr1 = 1, kps1 = 1, kpr2 = 1, kps2 = 1;
+  int kpr1 = 1, kps1 = 1;
   phase_kparts(d / 256, d / 32, Fs > 0, &kpr1, &kps1);
-  (void)kpr2;
-  (void)kps2;   // phase 2 is not split
-  // partials: phase 1 (gate, up) pairs over d_ff rows, phase 2 single values over d rows; the
-  // phases run one after the other and share the buffers
-  const size_t pr = std::max(P * (F / 16) * kpr1 * 16 * 2, P * (d / 16) * kpr2 * 16) * 4;
-  const size_t ps = std::max((size_t)T * (Fs / 16) * kps1 * 16 * 2, (size_t)T * (d / 16) * kps2 * 16) * 4;
+  // partials: phase 1's (gate, up) pairs over d_ff rows (phase 2 adds its K halves into the
+  // outputs themselves)
+  const size_t pr = P * (F / 16) * kpr1 * 16 * 2 * 4;
+  const size_t ps = (size_t)T * (Fs / 16) * kps1 * 16 * 2 * 4;
   auto up256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
   DecWs w;
   w.cnt = 1024;                                                  // after the work counters
   w.pkg = ffn_reserved_bytes(k, d, F, Fs);
   w.hB = up256(w.pkg + pkg_layout(T, d).total);
-  w.HBm = up256(w.hB + P * (F / 256) * 512 * 2);
+  w.HBm = up256(w.hB + P * (F / 256) * 256 * 2);
   w.hS = up256(w.HBm + P * (F / 256) * 4 * 12 * 2);
   w.HS16 = up256(w.hS + (size_t)T * 2 * Fs * 2);
   w.part_r = up256(w.HS16 + (size_t)T * (Fs / 16) * 4);
@@ -1130,8 +1110,9 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     if (p.cb_r <= 0 || p.cb_s <= 0) return cudaErrorInvalidValue;
     p.C_r = p.nb_r / p.cb_r;
     p.C_s = S ? p.nb_s / p.cb_s : 1;
-    // phase 1 splits tiles along K (two whole-tile items per warp left SMs idle); phase 2 has
-    // enough items per warp for balance, and its fix-up would cost registers
+    // phase 1 splits tiles along K into parts the finish kernel sums (whole-tile items, two
+    // per warp, left SMs idle); phase 2 is not split (its halves would add into the outputs,
+    // and the per-item work that costs was measured to outweigh the shorter last wave)
     if (phase == 1) {
       phase_kparts(p.nb_r, p.nb_s, S != nullptr, &p.kp_r, &p.kp_s);
     } else {
