@@ -8,7 +8,10 @@ namespace bre {
 
 namespace {
 
-// out[t][c] = bf16(y_shared[t][c] + sum_j w[t,j] * y_pairs[inv[t*k+j]][c]); 8 values per thread.
+// out[t][c] = bf16(y_shared[t][c] + sum_j w[t,j] * y_pairs[inv[t*k+j]][c]), j ascending; four
+// values per thread.  The routing entries of up to eight pairs, then their rows, are loaded
+// before the FMAs, so that a token's loads are in flight together rather than one pair after
+// another.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_pairs,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ inv,
@@ -17,42 +20,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       uint16_t* __restrict__ out, float* __restrict__ out_f32) {
   pdl_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int per_row = d / 8;
+  const int per_row = d / 4;
   if (i >= (long long)T * per_row) return;
-  const int t = (int)(i / per_row), c = (int)(i % per_row) * 8;
-  float acc[8];
-  if (y_shared) {
-    const float4* ys = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
-    float4 a = __ldg(ys), b = __ldg(ys + 1);
-    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-  }
+  const int t = (int)(i / per_row), c = (int)(i % per_row) * 4;
+  float4 acc = y_shared ? __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   const int nvalid = __ldg(offsets + E);
-  for (int j = 0; j < k; ++j) {
-    const int pos = __ldg(inv + (size_t)t * k + j);
-    if (pos < 0 || pos >= nvalid) continue;
-    const float w = __ldg(topk_w + (size_t)t * k + j);
-    const float4* yp = reinterpret_cast<const float4*>(y_pairs + (size_t)pos * d + c);
-    float4 a = __ldg(yp), b = __ldg(yp + 1);
-    acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
-    acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
-    acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
-    acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int pos[8];
+    float w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const bool in = j0 + q < k;
+      pos[q] = in ? __ldg(inv + (size_t)t * k + j0 + q) : -1;
+      w[q] = in ? __ldg(topk_w + (size_t)t * k + j0 + q) : 0.0f;
+    }
+    float4 y[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (pos[q] < 0 || pos[q] >= nvalid) pos[q] = -1;
+      y[q] = pos[q] >= 0 ? __ldg(reinterpret_cast<const float4*>(y_pairs + (size_t)pos[q] * d + c))
+                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (pos[q] >= 0) {
+        acc.x = fmaf(w[q], y[q].x, acc.x);
+        acc.y = fmaf(w[q], y[q].y, acc.y);
+        acc.z = fmaf(w[q], y[q].z, acc.z);
+        acc.w = fmaf(w[q], y[q].w, acc.w);
+      }
+    }
   }
-  uint4 o;
-  o.x = f32_to_bf16_rne(acc[0]) | (f32_to_bf16_rne(acc[1]) << 16);
-  o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
-  o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
-  o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
-  *reinterpret_cast<uint4*>(out + (size_t)t * d + c) = o;
-  if (out_f32) {
-    float4* of = reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c);
-    of[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    of[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  }
+  uint2 o;
+  o.x = f32_to_bf16_rne(acc.x) | (f32_to_bf16_rne(acc.y) << 16);
+  o.y = f32_to_bf16_rne(acc.z) | (f32_to_bf16_rne(acc.w) << 16);
+  *reinterpret_cast<uint2*>(out + (size_t)t * d + c) = o;
+  if (out_f32) *reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c) = acc;
 }
 
 // One CTA per token: x_out = bf16(x + bf16(moe) * scale); the sum of squares of x_out in the
@@ -119,7 +123,7 @@ __global__ void dequant_q80_kernel(const uint8_t* __restrict__ blk, long long nb
 cudaError_t launch_combine(const float* y_pairs, const float* topk_w, const int32_t* inv, const int32_t* offsets,
                            int E, const float* y_shared, int T, int k, int d, uint16_t* out, float* out_f32,
                            cudaStream_t s) {
-  const long long n = (long long)T * (d / 8);
+  const long long n = (long long)T * (d / 4);
   {
     const cudaError_t le = launch_k(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y_pairs,
                                     topk_w, inv, offsets, E, y_shared, T, k, d, out, out_f32);

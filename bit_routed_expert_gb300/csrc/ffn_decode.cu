@@ -363,7 +363,7 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
         mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bv.x, bv.y);
       }
     }
-    const float x0 = x32_0[bq], x1 = x32_1[bq];
+    const float x0 = __ldg(x32_0 + bq), x1 = __ldg(x32_1 + bq);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float dv = f16_bits_to_f32(dd[i >> 1]);
@@ -540,8 +540,8 @@ __device__ __forceinline__ float silu_mul(float gv, float uv) { return gv / (1.0
 
 // ----------------------------------------------------------------------------
 // activation package: x permuted into the Q2_K fragment order, the 16-value sub-block
-// sums of x as three BF16 limbs, their block totals, and 32-value sums for Q8_0.  Built
-// once per call by ffn_prep_kernel and copied whole into shared memory by phase 1.
+// sums of x as three BF16 limbs, and 32-value sums for Q8_0.  Built once per call by
+// ffn_prep_kernel; phase 1 copies the first two parts into shared memory.
 // ----------------------------------------------------------------------------
 struct PkgLayout {
   int xB, XBm, X32, total;
@@ -624,8 +624,8 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
   __syncthreads();
   const PkgLayout PL = pkg_layout(p.T, p.d);
   if (PHASE == 1 && threadIdx.x == 0) {
-    mbar_arrive_expect_tx(pkg_bar, PL.total);
-    bulk_g2s(xprep, p.pkg, PL.total, pkg_bar);
+    mbar_arrive_expect_tx(pkg_bar, PL.X32);
+    bulk_g2s(xprep, p.pkg, PL.X32, pkg_bar);   // xB and XBm (a multiple of 16 bytes)
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
 
@@ -697,7 +697,9 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
   const int nbx = d / 256;
   unsigned char* xB = xprep + PL.xB;                                   // [T][xstride]
   unsigned char* XBm = xprep + PL.XBm;                                 // [T][nbx][4][3][4] bf16
-  float* X32 = reinterpret_cast<float*>(xprep + PL.X32);              // [T][d/32]
+  // the 32-value sums (read only by the shared expert's items) stay in global memory, so that
+  // the package in shared memory leaves room for one more ring at T = 8
+  const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.X32);  // [T][d/32]
   if (PHASE == 1) {
     if (!mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT)) {
       if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
@@ -1142,7 +1144,7 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
       if (phase == 1 && !weight_map(&ms1, p.sw1, 1, 0, p.rows_s, p.nb_s * Q80_BB, p.cb_s * Q80_BB))
         return cudaErrorInvalidValue;
     }
-    const size_t xbytes = (phase == 1) ? (size_t)pkg_layout(a.T, p.d).total : 0;
+    const size_t xbytes = (phase == 1) ? (size_t)pkg_layout(a.T, p.d).X32 : 0;   // shared-memory part
     int nw = (phase == 1) ? MAX_WARPS : MAX_WARPS_P2;
     while (nw > 1 && (size_t)nw * NS * STAGE + BAR_BYTES + xbytes > (size_t)smem_max) --nw;
     const size_t smem = (size_t)nw * NS * STAGE + BAR_BYTES + xbytes;
