@@ -39,7 +39,6 @@ constexpr int STAGE = 5376;           // bytes per stage: 16 rows x 336 B of one
 constexpr int MAX_WARPS = 16;         // phase 1 (at most 128 registers a thread; fewer when the
                                       // activation package leaves less shared memory)
 constexpr int MAX_WARPS_P2 = 16;      // phase 2 (at most 128 registers a thread)
-constexpr uint32_t C43 = 0x43434343u;
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
@@ -60,6 +59,14 @@ static FDiv make_fdiv(unsigned d) {
   while ((1ull << l) < d) ++l;
   return FDiv{(uint32_t)(((1ull << (31 + l)) + d - 1) / d), 31 + l};
 }
+
+// Bit patterns the dequant combines with every weight word, held in registers (kernel
+// parameters) rather than rebuilt as immediates inside the loops: m43 = 0x43004300 (BF16 128 in
+// both halves, the exponent OR-ed onto codes), k43 = 0x43434343 (PRMT source of that exponent
+// byte), m128 = 0xC300C300 (BF16 -128 in both halves).
+struct DecConst {
+  uint32_t m43, k43, m128;
+};
 
 struct DecParams {
   const uint8_t* rw0;  // routed: phase 1 gate, phase 2 down
@@ -89,7 +96,7 @@ struct DecParams {
   int32_t* err;
   int xstride;  // bytes per token row of the permuted activations in shared memory
   const unsigned char* pkg;  // activation package in global memory (phase 1)
-  uint32_t m43;              // 0x43004300: BF16 exponent pattern of 128 in both halves
+  DecConst kc;
   int kp_r, kp_s;            // K parts per 16-row tile: items are (tile, K part)
   int C_r, C_s;              // chunks per matrix row of a routed / the shared expert
   int cpi_r, cpi_s;          // chunks per matrix in one item (C / K parts)
@@ -224,34 +231,72 @@ __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t 
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
-// (sc, sc) and (-128 sc, -128 sc) as BF16 pairs for sub-block byte jj of a scales word (exact).
-__device__ __forceinline__ void q2k_scale_pairs(uint32_t sclo, int jj, uint32_t& sc2, uint32_t& nsc2) {
-  const uint32_t u = prmt(sclo, C43, (uint32_t)(jj | (4 << 4) | (jj << 8) | (4 << 12)));   // 128 + sc
-  sc2 = bf16x2_fma(u, 0x3F803F80u, 0xC300C300u);                                          // u - 128
-  nsc2 = bf16x2_fma(u, 0xC300C300u, 0x46804680u);                                         // 16384 - 128 u
+// (sc, sc) and (-128 sc, -128 sc) as BF16 pairs for one sub-block byte of a scales word
+// (exact); sel selects the byte (RotConst), k43 is 0x43434343 and m43 0x43004300 (128, 128),
+// m128 0xC300C300 (-128, -128): registers (kernel parameters), so that no constant is
+// rebuilt inside the loops.
+__device__ __forceinline__ void q2k_scale_pairs(uint32_t sclo, uint32_t sel, const DecConst& k, uint32_t& sc2,
+                                                uint32_t& nsc2) {
+  const uint32_t u = prmt(sclo, k.k43, sel);   // 128 + sc
+  sc2 = bf16x2_sub(u, k.m43);                  // sc
+  nsc2 = bf16x2_mul(sc2, k.m128);              // -128 sc
+}
+
+// Fragment step jj of thread quad t works on sub-block 4t + rot_sub(t, jj) of a block.  Rotating
+// the sub-block with t spreads one load instruction's code words over all 32 banks: the 16 rows
+// of a stage lie 84 * cb bytes apart, a multiple of four words, so a common sub-block would put
+// four of a warp's 32 words in each of 8 banks.
+__host__ __device__ __forceinline__ int rot_sub(int t, int jj) { return (t + jj) & 3; }
+
+// Per-thread constants of the rotation: byte offsets of the code words inside a block row and
+// PRMT selectors of the matching scale bytes, for steps jj = 0..3.
+struct RotConst {
+  int qoff[4];
+  uint32_t ssel[4];
+};
+
+__device__ __forceinline__ RotConst rot_const(int t) {
+  RotConst r;
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = rot_sub(t, jj);
+    r.qoff[jj] = 16 + 16 * t + 4 * j;
+    r.ssel[jj] = (uint32_t)(j * 0x0101 + 0x4040);
+  }
+  return r;
 }
 
 // A fragments of the min-term MMA: the 4-bit mins of the lane's four sub-blocks for rows g
 // (scales word sw0) and g + 8 (sw1) as exact BF16 pairs, m = (128 + m) - 128.
-__device__ __forceinline__ void min_frags(uint32_t sw0, uint32_t sw1, uint32_t& A0, uint32_t& A1, uint32_t& A2,
-                                          uint32_t& A3) {
+__device__ __forceinline__ void min_frags(uint32_t sw0, uint32_t sw1, const DecConst& k, uint32_t& A0, uint32_t& A1,
+                                          uint32_t& A2, uint32_t& A3) {
   const uint32_t mg = (sw0 >> 4) & 0x0F0F0F0Fu, mg8 = (sw1 >> 4) & 0x0F0F0F0Fu;
-  A0 = bf16x2_fma(prmt(mg, C43, SEL_LO), 0x3F803F80u, 0xC300C300u);
-  A1 = bf16x2_fma(prmt(mg8, C43, SEL_LO), 0x3F803F80u, 0xC300C300u);
-  A2 = bf16x2_fma(prmt(mg, C43, SEL_HI), 0x3F803F80u, 0xC300C300u);
-  A3 = bf16x2_fma(prmt(mg8, C43, SEL_HI), 0x3F803F80u, 0xC300C300u);
+  A0 = bf16x2_sub(prmt(mg, k.k43, SEL_LO), k.m43);
+  A1 = bf16x2_sub(prmt(mg8, k.k43, SEL_LO), k.m43);
+  A2 = bf16x2_sub(prmt(mg, k.k43, SEL_HI), k.m43);
+  A3 = bf16x2_sub(prmt(mg8, k.k43, SEL_HI), k.m43);
 }
 
 // Q8_0 nibble planes of one row word (4 consecutive int8): (128+lo) and (128+hi') pairs.
-__device__ __forceinline__ void q80_frag(uint32_t w, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
+__device__ __forceinline__ void q80_frag(uint32_t w, uint32_t k43, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
                                          uint32_t& hi23) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
   const uint32_t hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;
-  lo01 = prmt(lo, C43, SEL_LO);
-  lo23 = prmt(lo, C43, SEL_HI);
-  hi01 = prmt(hi, C43, SEL_LO);
-  hi23 = prmt(hi, C43, SEL_HI);
+  lo01 = prmt(lo, k43, SEL_LO);
+  lo23 = prmt(lo, k43, SEL_HI);
+  hi01 = prmt(hi, k43, SEL_LO);
+  hi23 = prmt(hi, k43, SEL_HI);
 }
 
 // ----------------------------------------------------------------------------
@@ -263,7 +308,7 @@ template <int CB>
 __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt, int c, int g, int t,
                                            const unsigned char* xb_g,    // permuted x of column g
                                            const unsigned char* xbm_g,   // XBm of column g
-                                           uint32_t m43, float (&acc)[4]) {
+                                           const RotConst& rc, const DecConst& k, float (&acc)[4]) {
   const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q2K_BB;
 #pragma unroll 1
@@ -276,7 +321,7 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
       sw[rr] = lds_u32(base + 4 * t);
       dd[rr] = lds_u32(base + 80);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
+      for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + rc.qoff[jj]);
     }
     // one accumulator chain, started by a C = 0 MMA (the MMAs are far apart in the instruction
     // stream, so the chain costs no waiting)
@@ -285,14 +330,17 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       uint32_t sc2[2], nsc2[2];
-      q2k_scale_pairs(sw[0] & 0x0F0F0F0Fu, jj, sc2[0], nsc2[0]);
-      q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, jj, sc2[1], nsc2[1]);
+      q2k_scale_pairs(sw[0] & 0x0F0F0F0Fu, rc.ssel[jj], k, sc2[0], nsc2[0]);
+      q2k_scale_pairs(sw[1] & 0x0F0F0F0Fu, rc.ssel[jj], k, sc2[1], nsc2[1]);
+      uint4 bq[2];   // steps s = 0, 1 and 2, 3: one 16-byte load each
+#pragma unroll
+      for (int sp = 0; sp < 2; ++sp) bq[sp] = *reinterpret_cast<const uint4*>(xblk + ((jj * 2 + sp) * 4 + t) * 16);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const uint2 bv = *reinterpret_cast<const uint2*>(xblk + ((jj * 4 + s) * 4 + t) * 8);
+        const uint2 bv = (s & 1) ? make_uint2(bq[s >> 1].z, bq[s >> 1].w) : make_uint2(bq[s >> 1].x, bq[s >> 1].y);
         uint32_t a0, a1, a2, a3;
-        q2k_pairs(qw[0][jj], s, m43, a0, a2);
-        q2k_pairs(qw[1][jj], s, m43, a1, a3);
+        q2k_pairs(qw[0][jj], s, k.m43, a0, a2);
+        q2k_pairs(qw[1][jj], s, k.m43, a1, a3);
         a0 = bf16x2_fma(a0, sc2[0], nsc2[0]);
         a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
         a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
@@ -306,7 +354,7 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
     // min term: M = sum_j m_j X_j over the 16 sub-blocks, X_j in three limbs
     {
       uint32_t A0, A1, A2, A3;
-      min_frags(sw[0], sw[1], A0, A1, A2, A3);
+      min_frags(sw[0], sw[1], k, A0, A1, A2, A3);
 #pragma unroll
       for (int limb = 0; limb < 3; ++limb) {
         const uint2 bm = *reinterpret_cast<const uint2*>(xbm_g + ((b * 4 + t) * 3 + limb) * 8);
@@ -330,7 +378,7 @@ __device__ __forceinline__ void p1_q2k_mat(const unsigned char* stage, int cb_rt
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, int c, int g, int t,
                                            const uint16_t* xrow_g,  // global x row of column g
-                                           const float* x32_0, const float* x32_1, float (&acc)[4]) {
+                                           const float* x32_0, const float* x32_1, uint32_t k43, float (&acc)[4]) {
   const int chunk_bytes = cb * Q80_BB;
   // B (x from global memory) of block bl + 1 loads while block bl is processed
   auto load_b = [&](int bq, uint2 (&b)[2]) {
@@ -353,7 +401,7 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
       for (int rr = 0; rr < 2; ++rr) {
         const unsigned char* base = stage + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
         if (hf == 0) dd[rr] = lds_u16(base);
-        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), l01[rr], l23[rr], h01[rr], h23[rr]);
+        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k43, l01[rr], l23[rr], h01[rr], h23[rr]);
       }
       if (hf == 0) {
         mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bv.x, bv.y);
@@ -376,15 +424,16 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
   }
 }
 
-// B operand of one block for column g: 16 uint2 (h in BF16, fragment order).
+// B operand of one block for column g: 8 uint4 (h in BF16, fragment order; entry jj * 2 + sp
+// holds steps s = 2 sp and 2 sp + 1 of step jj).
 struct P2B {
-  uint2 v[16];
+  uint4 v[8];
 };
 
 __device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ hB, int pos_g, int nb, int b, int t) {
   const uint16_t* hblk = hB + ((long long)pos_g * nb + b) * 256;
 #pragma unroll
-  for (int q = 0; q < 16; ++q) B.v[q] = __ldg(reinterpret_cast<const uint2*>(hblk + (q * 4 + t) * 4));
+  for (int q = 0; q < 8; ++q) B.v[q] = __ldg(reinterpret_cast<const uint4*>(hblk + (q * 4 + t) * 8));
 }
 
 // One 256-column block of 16 rows of the down projection.
@@ -393,7 +442,7 @@ __device__ __forceinline__ void p2_load_b(P2B& B, const uint16_t* __restrict__ h
 // whole block of work to arrive.
 __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_bytes, int g, int t, P2B& B,
                                              const uint16_t* __restrict__ hnext, const uint16_t* __restrict__ hm,
-                                             uint32_t m43, float (&acc)[4]) {
+                                             const RotConst& rc, const DecConst& k, float (&acc)[4]) {
   // the three limbs of the sub-block sums are first needed at the block's end: loaded here
   uint2 bm[3];
 #pragma unroll
@@ -405,7 +454,7 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
     sw[rr] = lds_u32(base + 4 * t);
     dd[rr] = lds_u32(base + 80);
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + 16 + 16 * t + 4 * jj);
+    for (int jj = 0; jj < 4; ++jj) qw[rr][jj] = lds_u32(base + rc.qoff[jj]);
   }
   // jj outer, s inner (one sub-block's scales live at a time); consecutive MMAs alternate
   // between two accumulators
@@ -414,30 +463,31 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     uint32_t sc2[2], nsc2[2];
-    q2k_scale_pairs(sl0, jj, sc2[0], nsc2[0]);
-    q2k_scale_pairs(sl1, jj, sc2[1], nsc2[1]);
+    q2k_scale_pairs(sl0, rc.ssel[jj], k, sc2[0], nsc2[0]);
+    q2k_scale_pairs(sl1, rc.ssel[jj], k, sc2[1], nsc2[1]);
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       uint32_t a0, a1, a2, a3;
-      q2k_pairs(qw[0][jj], s, m43, a0, a2);
-      q2k_pairs(qw[1][jj], s, m43, a1, a3);
+      q2k_pairs(qw[0][jj], s, k.m43, a0, a2);
+      q2k_pairs(qw[1][jj], s, k.m43, a1, a3);
       a0 = bf16x2_fma(a0, sc2[0], nsc2[0]);
       a2 = bf16x2_fma(a2, sc2[0], nsc2[0]);
       a1 = bf16x2_fma(a1, sc2[1], nsc2[1]);
       a3 = bf16x2_fma(a3, sc2[1], nsc2[1]);
-      const uint2 bv = B.v[jj * 4 + s];
+      const uint4 bq = B.v[jj * 2 + (s >> 1)];
+      const uint32_t b0 = (s & 1) ? bq.z : bq.x, b1 = (s & 1) ? bq.w : bq.y;
       if (jj == 0 && s < 2)
-        mma_bf16_16816_z(P[s & 1], a0, a1, a2, a3, bv.x, bv.y);
+        mma_bf16_16816_z(P[s & 1], a0, a1, a2, a3, b0, b1);
       else
-        mma_bf16_16816(P[s & 1], a0, a1, a2, a3, bv.x, bv.y);
+        mma_bf16_16816(P[s & 1], a0, a1, a2, a3, b0, b1);
     }
 #pragma unroll
-    for (int s = 0; s < 4; ++s)
-      B.v[jj * 4 + s] = __ldg(reinterpret_cast<const uint2*>(hnext + ((jj * 4 + s) * 4 + t) * 4));
+    for (int sp = 0; sp < 2; ++sp)
+      B.v[jj * 2 + sp] = __ldg(reinterpret_cast<const uint4*>(hnext + ((jj * 2 + sp) * 4 + t) * 8));
   }
   {
     uint32_t A0, A1, A2, A3;
-    min_frags(sw[0], sw[1], A0, A1, A2, A3);
+    min_frags(sw[0], sw[1], k, A0, A1, A2, A3);
 #pragma unroll
     for (int limb = 0; limb < 3; ++limb) {
       const uint2 b2 = bm[limb];
@@ -461,7 +511,8 @@ __device__ __forceinline__ void p2_q2k_block(const unsigned char* blk, int row_b
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb, int c, int nb, int g, int t,
                                              int pos_g, const uint16_t* __restrict__ hB,
-                                             const uint16_t* __restrict__ HBm, uint32_t m43, float (&acc)[4]) {
+                                             const uint16_t* __restrict__ HBm, const RotConst& rc,
+                                             const DecConst& k, float (&acc)[4]) {
   const int chunk_bytes = cb * Q2K_BB;
   const int b0 = c * cb;
   const uint16_t* hcol = hB + (long long)pos_g * nb * 256;              // h of column g, block 0
@@ -472,7 +523,7 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
   for (int bl = 0; bl < cb; ++bl) {
     const int b = b0 + bl;
     const int bn = bl + 1 < cb ? b + 1 : b;
-    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B, hcol + bn * 256, hmcol + b * 48, m43, acc);
+    p2_q2k_block(stage + bl * Q2K_BB, chunk_bytes, g, t, B, hcol + bn * 256, hmcol + b * 48, rc, k, acc);
   }
 }
 
@@ -481,7 +532,7 @@ __device__ __forceinline__ void p2_q2k_chunk(const unsigned char* stage, int cb,
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb, int c, int g, int t, int Fs,
                                              const uint16_t* hrow_g,  // hS[tok_g][0][:]
-                                             const float* hs16_0, const float* hs16_1, float (&acc)[4]) {
+                                             const float* hs16_0, const float* hs16_1, uint32_t k43, float (&acc)[4]) {
   const int chunk_bytes = cb * Q80_BB;
   // B (both limbs of h) and the 16-row sums of block bl + 1 load while block bl is processed
   auto load_b = [&](int bq, uint2 (&b)[4], float (&xs2)[2]) {
@@ -509,7 +560,7 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb,
       for (int rr = 0; rr < 2; ++rr) {
         const unsigned char* base = stage + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
         if (hf == 0) dd[rr] = lds_u16(base);
-        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), l01[rr], l23[rr], h01[rr], h23[rr]);
+        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k43, l01[rr], l23[rr], h01[rr], h23[rr]);
       }
       if (hf == 0) {
         mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
@@ -549,8 +600,12 @@ struct PkgLayout {
 
 __host__ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
 
+// bytes per token row of the permuted activations: 16 bytes a lane per load, and a pitch of
+// 16 (mod 32) words puts the rows of a quarter warp's loads in different bank halves
+__host__ __device__ __forceinline__ int x_stride(int d) { return d * 2 + 64; }
+
 __host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
-  const int nbx = d / 256, xstride = d * 2 + 32;
+  const int nbx = d / 256, xstride = x_stride(d);
   PkgLayout L;
   L.xB = 0;
   L.XBm = T * xstride;
@@ -570,14 +625,16 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
   const PkgLayout L = pkg_layout(T, d);
   const uint32_t v = x[(size_t)t * d + 256 * b + i];
   {
-    // fragment order: step (jj, s) of thread tq holds codes s, 8+s | 4+s, 12+s of sub-block 4tq+jj,
-    // each activation scaled by 4^-min(s,2) to match the code left in place in the A fragment
-    const int j = i >> 4, tq = j >> 2, jj = j & 3, ip = i & 15;
+    // fragment order: step (jj, s) of thread tq holds codes s, 8+s | 4+s, 12+s of sub-block
+    // 4tq + rot_sub(tq, jj), each activation scaled by 4^-min(s,2) to match the code left in
+    // place in the A fragment; steps s = 2sp, 2sp+1 are adjacent (one 16-byte load)
+    const int j = i >> 4, tq = j >> 2, jr = j & 3, ip = i & 15;
+    const int jj = (jr - tq) & 3;   // the step at which thread quad tq works on sub-block j
     const int byte = ip >> 2, s = ip & 3;
     const int v4 = (byte & 1) * 2 + (byte >> 1);
-    const int rem = ((((b * 4 + jj) * 4 + s) * 4 + tq) * 4 + v4);
+    const int rem = (((((b * 4 + jj) * 2 + (s >> 1)) * 4 + tq) * 2 + (s & 1)) * 4 + v4);
     const float scaled = __fmul_rn(bf16_bits_to_f32(v), s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f));
-    reinterpret_cast<uint16_t*>(pkg + L.xB + (size_t)t * (d * 2 + 32))[rem] = (uint16_t)f32_to_bf16_rne(scaled);
+    reinterpret_cast<uint16_t*>(pkg + L.xB + (size_t)t * x_stride(d))[rem] = (uint16_t)f32_to_bf16_rne(scaled);
   }
   const float f = bf16_bits_to_f32(v);
   // 16-value sub-block sum (lanes of a half warp), fixed tree order
@@ -612,6 +669,7 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const RotConst rc = rot_const(t);
   unsigned char* stages = sm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + nw * NS * STAGE);
   uint64_t* pkg_bar = bars + MAX_WARPS * NS;
@@ -754,14 +812,14 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
           const uint16_t* xr = p.x + (size_t)dg * d;
           const float* x0 = X32 + d0 * (d / 32);
           const float* x1 = X32 + d1 * (d / 32);
-          p1_q80_mat(stage, it.cb, c, g, t, xr, x0, x1, accm);
+          p1_q80_mat(stage, it.cb, c, g, t, xr, x0, x1, p.kc.k43, accm);
         } else {
           const unsigned char* xb = xB + (size_t)dg * p.xstride;
           const unsigned char* xm = XBm + (size_t)dg * nbx * 96;
           if (it.cb == 4)
-            p1_q2k_mat<4>(stage, 4, c, g, t, xb, xm, p.m43, accm);
+            p1_q2k_mat<4>(stage, 4, c, g, t, xb, xm, rc, p.kc, accm);
           else
-            p1_q2k_mat<0>(stage, it.cb, c, g, t, xb, xm, p.m43, accm);
+            p1_q2k_mat<0>(stage, it.cb, c, g, t, xb, xm, rc, p.kc, accm);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -772,9 +830,9 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
         const int c = it.kp * it.cpi + cc;
         if (it.shared) {
           p2_q80_chunk(stage, it.cb, c, g, t, p.Fs, p.hS + (size_t)dg * 2 * p.Fs, p.HS16 + (size_t)d0 * (p.Fs / 16),
-                       p.HS16 + (size_t)d1 * (p.Fs / 16), acc2[0]);
+                       p.HS16 + (size_t)d1 * (p.Fs / 16), p.kc.k43, acc2[0]);
         } else {
-          p2_q2k_chunk(stage, it.cb, c, Fnb, g, t, dg, p.hB, p.HBm, p.m43, acc2[0]);
+          p2_q2k_chunk(stage, it.cb, c, Fnb, g, t, dg, p.hB, p.HBm, rc, p.kc, acc2[0]);
         }
       }
       fence_proxy_async_smem();
@@ -880,11 +938,12 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
   } else {
     const int b2 = row >> 8, j = (row >> 4) & 15, ip = row & 15;
     const int byte = ip >> 2, s = ip & 3, v4 = (byte & 1) * 2 + (byte >> 1);
+    const int tq = j >> 2, jj = ((j & 3) - tq) & 3;   // fragment step of sub-block j (rot_sub)
     // BF16 of h * 4^-min(s,2) (the down projection's A fragments keep codes in place); a power
     // of two commutes with the rounding, so the 16-row sums below use h rounded to BF16
     const float hs = __fmul_rn(h, s == 0 ? 1.0f : (s == 1 ? 0.25f : 0.0625f));
-    const size_t base = ((((size_t)src * Fnb + b2) * 4 + (j & 3)) * 4 + s) * 4 * 4 + (size_t)(j >> 2) * 4;
-    f.hB[base + v4] = (uint16_t)f32_to_bf16_rne(hs);
+    const size_t idx = (((((size_t)src * Fnb + b2) * 4 + jj) * 2 + (s >> 1)) * 4 + tq) * 8 + (s & 1) * 4 + v4;
+    f.hB[idx] = (uint16_t)f32_to_bf16_rne(hs);
     hq = bf16_bits_to_f32(f32_to_bf16_rne(h));
   }
   // 16-row sums of the limb values (half warps)
@@ -1069,8 +1128,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   p.tile_cnt = reinterpret_cast<int*>(w + L.cnt);
   p.part_r = reinterpret_cast<float*>(w + L.part_r);
   p.part_s = reinterpret_cast<float*>(w + L.part_s);
-  p.xstride = p.d * 2 + 32;
-  p.m43 = 0x43004300u;
+  p.xstride = x_stride(p.d);
+  p.kc = DecConst{0x43004300u, 0x43434343u, 0xC300C300u};
 
   const int sms = device_sm_count();
   const int smem_max = device_max_smem_optin();
