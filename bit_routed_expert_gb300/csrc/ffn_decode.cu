@@ -174,13 +174,6 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_ac
   return it;
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Lane 0 issues the copy of chunk cc of `it` into `stage`: one bulk copy of a whole 16-row tile,
 // or one tensor copy of a 16-row x cb-block box (maps: [experts][rows][row words]).

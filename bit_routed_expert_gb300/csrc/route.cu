@@ -12,6 +12,7 @@
 // ascending order starting from +0, then a butterfly p_j + p_(j^o) for
 // o = 16, 8, 4, 2, 1.  Any thread mapping computes exactly this.
 #include <algorithm>
+#include <mutex>
 
 #include "bre_common.cuh"
 #include "kernels.h"
@@ -148,8 +149,9 @@ __device__ void topk_warp(const float* __restrict__ s_row, const float* __restri
 // the producing kernel: W_r is a weight); x is staged once as FP32 in [j][i][token] order.
 // Every loop stays rolled: each SM runs this code once, so its size, not its arithmetic,
 // would set the time.  Each cluster then selects a local top k of its 32 experts per token;
-// the last block to deliver a token's candidates merges them (the global top k of a token is
-// contained in the union of the per-block top k).
+// the CTA that makes the last delivery (one ticket for all tokens) merges every token's block
+// lists (the global top k of a token is contained in the union of the per-block top k) and,
+// for moe_route_permute, builds the permutation from the ids it holds.
 constexpr int RC_J = 4;                   // partials (warps) per CTA
 constexpr int RC_CLUSTER = 32 / RC_J;     // CTAs per cluster
 constexpr int RC_THREADS = RC_J * 32;
@@ -196,15 +198,94 @@ struct PermOut {
   int32_t* active;
   int32_t* n_active;
 };
-constexpr int RC_TOKENS_DONE = 32;   // ticket index counting merged tokens (token tickets use 0..31)
+constexpr long long RC_WAIT_LIMIT = 2000000000LL;   // cycles (~1 s) before the W wait gives up
+
+// A group of W lanes (W = 32, or 16: two tokens per warp) merges the candidate lists of one
+// token: list b (lane b of the group, b < nblk <= W) holds the block's top kc in rank order, so
+// the token's top k are k rounds of "take the best list head".  Writes ids / weights (weights
+// from the unbiased s, S summed in slot order) and keeps the ids in ids_s for the permutation.
+// lane is the lane inside the group; every lane of the warp calls it (W = 16: each half-warp
+// with its own token, or with active = false for a half that has none).
+template <int W>
+__device__ __forceinline__ void merge_token(const uint32_t* mc, const int* mid, const float* ms, int nblk, int kc,
+                                            int k, int lane, bool active, int32_t* __restrict__ ids_t,
+                                            float* __restrict__ w_t, int* ids_s) {
+  int h = 0;
+  uint32_t hc = 0xFFFFFFFFu;
+  int hid = 0x7FFFFFFF;
+  float hs = 0.0f;
+  auto load_head = [&]() {
+    hc = 0xFFFFFFFFu;
+    hid = 0x7FFFFFFF;
+    if (active && lane < nblk && h < kc) {
+      const int id = mid[lane * kc + h];
+      if (id >= 0) {
+        hc = mc[lane * kc + h];
+        hid = id;
+        hs = ms[lane * kc + h];
+      }
+    }
+  };
+  load_head();
+  float my_s = 0.0f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bc = hc;
+    int bid = hid;
+#pragma unroll
+    for (int o = W / 2; o >= 1; o >>= 1) {
+      const uint32_t oc = __shfl_xor_sync(0xffffffffu, bc, o, W);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, o, W);
+      if (code_before(oc, oid, bc, bid)) {
+        bc = oc;
+        bid = oid;
+      }
+    }
+    // ids are distinct across lists, so exactly one lane of the group holds the winner
+    const bool mine = hid == bid && hid != 0x7FFFFFFF;
+    const unsigned gm = __ballot_sync(0xffffffffu, mine) >> ((threadIdx.x & 31) & ~(W - 1) & 31);
+    const unsigned wmask = W == 32 ? gm : (gm & 0xFFFFu);
+    const float ws = __shfl_sync(0xffffffffu, hs, wmask ? __ffs(wmask) - 1 : 0, W);
+    if (lane == j) {
+      my_s = ws;
+      my_id = bid;
+    }
+    if (mine) {
+      ++h;
+      load_head();
+    }
+  }
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const float sj = __shfl_sync(0xffffffffu, my_s, j, W);
+    S = (j == 0) ? sj : __fadd_rn(S, sj);
+  }
+  if (active && lane < k) {
+    ids_t[lane] = my_id;
+    w_t[lane] = __fdiv_rn(my_s, S);
+    ids_s[lane] = my_id;
+  }
+}
+
+// The W_r slice of a CTA arrives by one tensor copy when W_r allows (E % 4 == 0, d / 32 <= 256,
+// 16-byte aligned): a map over W_r viewed as [d/32][32][E] (innermost E) with box
+// {32 experts, RC_J rows j, d/32 groups} lands as [i][jj][e], the layout the FMA loop reads.
+struct RouteMap {
+  CUtensorMap map;
+  int use;
+};
 
 __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     route_cluster_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w_r,
                          const float* __restrict__ bias, int T, int d, int E, int k, uint32_t* __restrict__ cand_c,
                          float* __restrict__ cand_s, int* __restrict__ cand_id, int* tickets,
-                         int32_t* __restrict__ ids, float* __restrict__ wts, const PermOut po) {
-  extern __shared__ __align__(16) float rc_smem[];
+                         int32_t* __restrict__ ids, float* __restrict__ wts, const PermOut po, int merge_group,
+                         int32_t* err, const __grid_constant__ RouteMap wm) {
+  extern __shared__ __align__(128) float rc_smem[];
   __shared__ float part[SMALL_TT][RC_J][33];     // partial sums of this CTA's j, padded
+  __shared__ __align__(8) uint64_t wbar;
+  __shared__ int s_last;
+  __shared__ int s_scan[2][RC_J];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = d / 32;
   float* Ws = rc_smem;                           // [n][RC_J][32]
@@ -216,7 +297,14 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   const int nt = min(SMALL_TT, T - t0);
   const int kc = min(k, 32);
   const int slots = rc_slots(E, k);
-  if ((E & 3) == 0) {
+  if (wm.use) {
+    if (tid == 0) {
+      mbar_init(&wbar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&wbar, (uint32_t)(n * RC_J * 32 * 4));
+      tma_load_3d(Ws, &wm.map, blockIdx.x * 32, jb * RC_J, 0, &wbar);
+    }
+  } else if ((E & 3) == 0) {
     // 16-byte pieces: slice row (i, jj) is 8 pieces of W_r row 32 i + RC_J jb + jj; thread tid
     // copies piece tid % 8 of jj = (tid / 8) % 4 for i = tid / 32, +4, +8, ...
     const int pc = tid & 7, jj = (tid >> 3) & 3, i0 = tid >> 5;
@@ -234,17 +322,38 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     for (int i = 0; i < n; ++i) cp_async4(dst + (size_t)i * RC_J * 32, src + i * rstride, e < E ? 4 : 0);
   }
   pdl_wait();
-  // stage x: item q = (i, tt) reads the RC_J values x[t0+tt][32 i + RC_J jb ...] (8 bytes)
-  for (int q = tid; q < n * SMALL_TT; q += RC_THREADS) {
-    const int tt = q & (SMALL_TT - 1), i = q / SMALL_TT;
-    uint2 v = make_uint2(0u, 0u);
-    if (tt < nt) v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * d + 32 * i + RC_J * jb));
-    xs[(0 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.x & 0xFFFFu);
-    xs[(1 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.x >> 16);
-    xs[(2 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.y & 0xFFFFu);
-    xs[(3 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v.y >> 16);
+  // stage x: item q = (i, tt) reads the RC_J values x[t0+tt][32 i + RC_J jb ...] (8 bytes); a
+  // thread's loads (eight at a time) are all issued before their stores, so their latencies
+  // overlap instead of adding up
+  for (int q0 = 0; q0 < n * SMALL_TT; q0 += 8 * RC_THREADS) {
+    uint2 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + u * RC_THREADS + tid;
+      const int tt = q & (SMALL_TT - 1), i = q / SMALL_TT;
+      v[u] = make_uint2(0u, 0u);
+      if (q < n * SMALL_TT && tt < nt)
+        v[u] = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * d + 32 * i + RC_J * jb));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + u * RC_THREADS + tid;
+      if (q < n * SMALL_TT) {
+        const int tt = q & (SMALL_TT - 1), i = q / SMALL_TT;
+        xs[(0 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v[u].x & 0xFFFFu);
+        xs[(1 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v[u].x >> 16);
+        xs[(2 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v[u].y & 0xFFFFu);
+        xs[(3 * n + i) * SMALL_TT + tt] = bf16_bits_to_f32(v[u].y >> 16);
+      }
+    }
   }
-  cp_async_wait_all();
+  if (wm.use) {
+    // bounded: on a timeout the error word is set and the CTA carries on (it must still reach
+    // the cluster barriers its peers wait on)
+    if (!mbar_wait_bounded(&wbar, 0, RC_WAIT_LIMIT) && err && tid == 0) atomicOr(err, BRE_DEVERR_TIMEOUT);
+  } else {
+    cp_async_wait_all();
+  }
   __syncthreads();
   // partial j of expert e: rows c = j + 32 i in ascending i, fmaf from +0; the operands of eight
   // rows are loaded before their FMAs (one warp per scheduler: the loads' latency is not hidden
@@ -283,10 +392,9 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
   cluster_sync_all();
   // CTA of rank r adds the 32 partials of token t0 + r for the 32 experts of the block, then
   // writes the block's top kc of that token in rank order (rank = number of the block's experts
-  // that come first); the last block to deliver a token's candidates (per-token ticket, reset by
-  // it) merges them, so the tokens' merges run in parallel
+  // that come first).  One ticket counts the deliveries of all tokens; the CTA that makes the
+  // last one merges every token and, when asked, permutes.
   const uint32_t r = cluster_ctarank();
-  bool merge = false;
   if (warp == 0 && (int)r < nt) {
     float v[32];
 #pragma unroll
@@ -315,85 +423,92 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     }
     // the warp barrier orders the lanes' candidate stores before lane 0's release
     __syncwarp();
-    int last = 0;
     if (lane == 0) {
       int prev;
-      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + t0 + r) : "memory");
-      last = prev == (int)gridDim.x - 1;
+      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets) : "memory");
+      const int last = prev == (int)gridDim.x * T - 1;
+      if (last) tickets[0] = 0;   // every delivery is counted: ready for the next call
+      s_last = last;
     }
-    merge = __shfl_sync(0xffffffffu, last, 0) != 0;
+  } else if (tid == 0) {
+    s_last = 0;
   }
-  cluster_sync_all();  // no CTA leaves, or reuses its shared memory, while another reads its partials
-  if (!merge) return;
-  // merge (warp 0): the token's candidates (nblk lists of kc) go to shared memory (reusing the W
-  // slice); a candidate's rank among all of them is the number of candidates that come first.
-  // Ranks below k are the selection, in order.
-  const int t = t0 + (int)r;
-  uint32_t* mc = reinterpret_cast<uint32_t*>(Ws);
-  int* mid = reinterpret_cast<int*>(mc + slots);
-  float* ms = reinterpret_cast<float*>(mid + slots);
-  float* sel = ms + slots;   // [k] s of the selected, by rank
-  const size_t cb = (size_t)t * slots;
-  __syncwarp();   // lane 0's acquire comes first for every lane
-  for (int c = lane; c < slots; c += 32) {
-    mc[c] = __ldcg(cand_c + cb + c);
-    mid[c] = __ldcg(cand_id + cb + c);
-    ms[c] = __ldcg(cand_s + cb + c);
-  }
-  if (lane == 0) tickets[t] = 0;   // ready for the next call
-  __syncwarp();
-  // ranks by a linear scan: every lane compares its candidates with all slots (broadcast reads,
-  // no dependent chain; a binary search per list chained shared-memory latencies)
-  for (int c0 = 0; c0 < slots; c0 += 32) {
-    const int c = c0 + lane;
-    const int id = c < slots ? mid[c] : -1;
-    const uint32_t code = c < slots ? mc[c] : 0u;
-    int rank = 0;
-#pragma unroll 8
-    for (int c2 = 0; c2 < slots; ++c2) {
-      const int id2 = mid[c2];
-      rank += (id2 >= 0 && code_before(mc[c2], id2, code, id)) ? 1 : 0;
+  cluster_sync_all();  // no CTA leaves while another reads its partials; s_last is visible
+  if (!s_last) return;
+  // ---- the last CTA: merge every token (one warp per token, token groups that fit the shared
+  // memory), then the permutation from the ids kept in shared memory
+  const int nblk = (E + 31) / 32;
+  const int P = T * k;
+  int* ids_s = reinterpret_cast<int*>(rc_smem);   // [T * k]
+  int* cnt = ids_s + P;                            // [E + 1], then run [E + 1] (permutation)
+  int* run = cnt + (E + 1);
+  uint32_t* mc = reinterpret_cast<uint32_t*>(run + (E + 1));   // [merge_group * slots] x 3
+  int* mid = reinterpret_cast<int*>(mc + (size_t)merge_group * slots);
+  float* ms = reinterpret_cast<float*>(mid + (size_t)merge_group * slots);
+  for (int g0 = 0; g0 < T; g0 += merge_group) {
+    const int ng = min(merge_group, T - g0);
+    // the acquire of the last ticket precedes this barrier-ordered read of every delivery; a
+    // thread's loads (eight slots at a time) are issued before their stores
+    for (int c0 = 0; c0 < ng * slots; c0 += 8 * RC_THREADS) {
+      uint32_t vc[8];
+      int vi[8];
+      float vs[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * RC_THREADS + tid;
+        if (c < ng * slots) {
+          const size_t gi = (size_t)g0 * slots + c;
+          vc[u] = __ldcg(cand_c + gi);
+          vi[u] = __ldcg(cand_id + gi);
+          vs[u] = __ldcg(cand_s + gi);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * RC_THREADS + tid;
+        if (c < ng * slots) {
+          mc[c] = vc[u];
+          mid[c] = vi[u];
+          ms[c] = vs[u];
+        }
+      }
     }
-    if (id >= 0 && rank < k) {
-      ids[(size_t)t * k + rank] = id;
-      sel[rank] = ms[c];
+    __syncthreads();
+    if (nblk <= 16 && k <= 16) {
+      // two tokens per warp, one per half-warp
+      for (int p0 = 2 * warp; p0 < ng; p0 += 2 * RC_J) {
+        const int tt = p0 + (lane >> 4);
+        const bool act = tt < ng;
+        const int ts = act ? tt : p0;
+        const int t = g0 + ts;
+        merge_token<16>(mc + (size_t)ts * slots, mid + (size_t)ts * slots, ms + (size_t)ts * slots, nblk, kc, k,
+                        lane & 15, act, ids + (size_t)t * k, wts + (size_t)t * k, ids_s + (size_t)t * k);
+      }
+    } else {
+      for (int tt = warp; tt < ng; tt += RC_J) {
+        const int t = g0 + tt;
+        merge_token<32>(mc + (size_t)tt * slots, mid + (size_t)tt * slots, ms + (size_t)tt * slots, nblk, kc, k,
+                        lane, true, ids + (size_t)t * k, wts + (size_t)t * k, ids_s + (size_t)t * k);
+      }
     }
-  }
-  __syncwarp();
-  if (lane < k) {
-    float S = sel[0];
-    for (int q = 1; q < k; ++q) S = __fadd_rn(S, sel[q]);
-    wts[(size_t)t * k + lane] = __fdiv_rn(sel[lane], S);
+    __syncthreads();
   }
   if (po.offsets == nullptr) return;
-  // the last token merged (second-level ticket) permutes all T * k pairs: stable counting sort by
-  // expert id in one warp (ids are in [0, E) by construction)
-  __syncwarp();
-  int lastp = 0;
-  if (lane == 0) {
-    int prev;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + RC_TOKENS_DONE) : "memory");
-    lastp = prev == T - 1;
-    if (lastp) tickets[RC_TOKENS_DONE] = 0;   // ready for the next call
+  // stable counting sort of the T * k pairs by expert id (ids are in [0, E) by construction)
+  for (int q = tid; q <= E; q += RC_THREADS) {
+    cnt[q] = 0;
+    run[q] = 0;
   }
-  if (!__shfl_sync(0xffffffffu, lastp, 0)) return;
-  __syncwarp();
-  int* cnt = reinterpret_cast<int*>(sel + 32);   // [E + 1], then the running counts [E + 1]
-  int* run = cnt + (E + 1);
-  for (int i = lane; i <= E; i += 32) {
-    cnt[i] = 0;
-    run[i] = 0;
-  }
-  __syncwarp();
-  const int P = T * k;
-  for (int q = lane; q < P; q += 32) atomicAdd(&cnt[__ldcg(ids + q)], 1);
-  __syncwarp();
-  // exclusive scan of the counts; lane l takes experts [l * per, (l + 1) * per)
-  const int per = (E + 31) / 32, a0 = min(E, lane * per), a1 = min(E, a0 + per);
+  __syncthreads();
+  for (int q = tid; q < P; q += RC_THREADS) atomicAdd(&cnt[ids_s[q]], 1);
+  __syncthreads();
+  // exclusive scan of the counts (and of the active flags): thread i takes experts
+  // [i * per, (i + 1) * per)
+  const int per = (E + RC_THREADS - 1) / RC_THREADS, a0 = min(E, tid * per), a1 = min(E, a0 + per);
   int sum = 0, nact = 0;
-  for (int i = a0; i < a1; ++i) {
-    sum += cnt[i];
-    nact += cnt[i] > 0 ? 1 : 0;
+  for (int q = a0; q < a1; ++q) {
+    sum += cnt[q];
+    nact += cnt[q] > 0 ? 1 : 0;
   }
   int ps = sum, pa = nact;
 #pragma unroll
@@ -404,26 +519,41 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
       pa += ya;
     }
   }
-  int base = ps - sum, abase = pa - nact;
-  for (int i = a0; i < a1; ++i) {
-    const int c = cnt[i];
-    po.offsets[i] = base;
-    cnt[i] = base;
-    if (c > 0) po.active[abase++] = i;
+  if (lane == 31) {
+    s_scan[0][warp] = ps;
+    s_scan[1][warp] = pa;
+  }
+  __syncthreads();
+  int ws0 = 0, wa0 = 0, tot_s = 0, tot_a = 0;
+#pragma unroll
+  for (int w = 0; w < RC_J; ++w) {
+    if (w < warp) {
+      ws0 += s_scan[0][w];
+      wa0 += s_scan[1][w];
+    }
+    tot_s += s_scan[0][w];
+    tot_a += s_scan[1][w];
+  }
+  int base = ws0 + ps - sum, abase = wa0 + pa - nact;
+  for (int q = a0; q < a1; ++q) {
+    const int c = cnt[q];
+    po.offsets[q] = base;
+    cnt[q] = base;
+    if (c > 0) po.active[abase++] = q;
     base += c;
   }
-  const int total_act = __shfl_sync(0xffffffffu, pa, 31);
-  if (lane == 31) {
-    po.offsets[E] = ps;
-    *po.n_active = pa;
+  if (tid == 0) {
+    po.offsets[E] = tot_s;
+    *po.n_active = tot_a;
   }
-  for (int i = total_act + lane; i < E; i += 32) po.active[i] = -1;
-  __syncwarp();
+  for (int q = tot_a + tid; q < E; q += RC_THREADS) po.active[q] = -1;
+  __syncthreads();
+  if (warp != 0) return;
   // pairs in chunks of 32, in order; rank among equal ids from a warp match
   const unsigned lt = (1u << lane) - 1u;
   for (int c0 = 0; c0 < P; c0 += 32) {
     const int q = c0 + lane;
-    const int key = q < P ? __ldcg(ids + q) : E;
+    const int key = q < P ? ids_s[q] : E;
     const unsigned m = __match_any_sync(0xffffffffu, key);
     const int lr = __popc(m & lt);
     if (q < P) {
@@ -691,13 +821,14 @@ size_t route_ws_bytes(int T, int E) {
 
 namespace {
 cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
-                       int32_t* ids, float* w, void* ws, const PermOut& po, bool* permuted, cudaStream_t s);
+                       int32_t* ids, float* w, void* ws, const PermOut& po, int32_t* err, bool* permuted,
+                       cudaStream_t s);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                          int32_t* ids, float* w, void* ws, cudaStream_t s) {
   bool permuted = false;
-  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, &permuted, s);
+  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, nullptr, &permuted, s);
 }
 
 cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
@@ -705,23 +836,65 @@ cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const floa
                                  int32_t* active, int32_t* n_active, int32_t* err, void* ws, cudaStream_t s) {
   bool permuted = false;
   const cudaError_t e =
-      route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, &permuted, s);
+      route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, err, &permuted,
+                 s);
   if (e != cudaSuccess || permuted) return e;
   return launch_permute(ids, T, k, E, offsets, perm, inv, active, n_active, err, s);
 }
 
 namespace {
+// Tensor map of W_r for the small-batch router's slice copies (RouteMap), cached per (W_r, d, E):
+// decode calls repeat the same few, and an encode costs host time on every call.  use = 0 when
+// W_r does not meet the copy's rules (then the kernel copies with cp.async).
+bool route_map(RouteMap* rm, const float* w_r, int d, int E) {
+  rm->use = 0;
+  const int n = d / 32;
+  if ((E & 3) != 0 || n < 1 || n > 256 || (reinterpret_cast<uintptr_t>(w_r) & 15) != 0) return true;
+  struct Entry {
+    const float* w;
+    int d, E;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int n_cached = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cached; ++i) {
+    if (cache[i].w == w_r && cache[i].d == d && cache[i].E == E) {
+      rm->map = cache[i].map;
+      rm->use = 1;
+      return true;
+    }
+  }
+  const uint64_t dims[3] = {(uint64_t)E, 32u, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)E * 4u, (uint64_t)E * 128u};
+  const uint32_t box[3] = {32u, (uint32_t)RC_J, (uint32_t)n};
+  if (!encode_tiled(&rm->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, w_r, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return false;
+  cache[next] = Entry{w_r, d, E, rm->map};
+  next = (next + 1) % 32;
+  if (n_cached < 32) ++n_cached;
+  rm->use = 1;
+  return true;
+}
+
 cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
-                       int32_t* ids, float* w, void* ws, const PermOut& po, bool* permuted, cudaStream_t s) {
-  // one ticket per token of the small-batch kernel, at fixed offsets so that calls with
-  // different T share them
+                       int32_t* ids, float* w, void* ws, const PermOut& po, int32_t* err, bool* permuted,
+                       cudaStream_t s) {
+  // the small-batch kernel's ticket sits at a fixed offset, so that calls with different T share it
   int* ticket = reinterpret_cast<int*>(ws);
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
   const size_t small_smem = (size_t)(d / 32) * (RC_J * 32 + RC_J * SMALL_TT) * sizeof(float);
-  // merge area: candidates (12 bytes a slot) + 32 selected s; then, when permuting, two count arrays
-  const size_t merge_bytes = (size_t)rc_slots(E, k) * 12 + 32 * 4;
-  const bool can_permute = po.offsets != nullptr && small_smem >= merge_bytes + (size_t)8 * (E + 1);
-  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() && small_smem >= merge_bytes) {
+  // the merging CTA's shared memory (words): ids [T k], two count arrays [E + 1], and the
+  // candidates of at least one token (3 words a slot)
+  const int slots = rc_slots(E, k);
+  const size_t fixed_words = (size_t)T * k + 2 * (size_t)(E + 1);
+  const size_t avail_words = small_smem / 4;
+  if (T <= SMALL_T_MAX && small_smem <= (size_t)device_max_smem_optin() &&
+      avail_words >= fixed_words + 3 * (size_t)slots) {
+    const int merge_group = (int)std::min<size_t>((size_t)T, (avail_words - fixed_words) / (3 * (size_t)slots));
+    RouteMap rm;
+    if (!route_map(&rm, w_r, d, E)) return cudaErrorInvalidValue;
     const size_t smem = small_smem;
     static int configured_dev = -1;
     static size_t configured_smem = 0;
@@ -733,18 +906,16 @@ cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, i
       configured_dev = dev;
       configured_smem = smem;
     }
-    const int slots = rc_slots(E, k);
     uint32_t* cand_c = reinterpret_cast<uint32_t*>(S);
     float* cand_s = S + (size_t)T * slots;
     int* cand_id = reinterpret_cast<int*>(S + (size_t)2 * T * slots);
     dim3 grid((E + 31) / 32, RC_CLUSTER, (T + SMALL_TT - 1) / SMALL_TT);
     {
       const cudaError_t le = launch_k(route_cluster_kernel, dim3(grid), dim3(RC_THREADS), smem, s, x, w_r, bias, T,
-                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w,
-                                      can_permute ? po : PermOut{});
+                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w, po, merge_group, err, rm);
       if (le != cudaSuccess) return le;
     }
-    *permuted = can_permute;
+    *permuted = po.offsets != nullptr;
     return cudaGetLastError();
   }
   static int tiled_dev = -1;

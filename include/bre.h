@@ -140,8 +140,8 @@ bre_status moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *of
 
 /* moe_route followed by moe_permute, with the same arguments and outputs as the two calls
  * (ws: moe_route_workspace(T, E) bytes, zero-filled once after allocation).  For batches of
- * at most 32 tokens the router kernel's last merging warp also builds the permutation, so the
- * pair is one launch; otherwise the two kernels run back to back on `stream`.  Router ids are
+ * at most 32 tokens the router kernel's last CTA (the one that merges every token's
+ * candidates) also builds the permutation, so the pair is one launch; otherwise the two kernels run back to back on `stream`.  Router ids are
  * always in [0, E), so dev_err is only touched by the second form. */
 bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
                              int32_t *topk_ids, float *topk_w, int32_t *offsets, int32_t *perm, int32_t *inv,
