@@ -61,6 +61,9 @@ def lib():
         L.or_dequant_q8_0.argtypes = [P, i64, P]
         L.or_engram_gather.argtypes = [P, P, i32, P, i32, i32, P, P]
         L.or_route.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
+        L.or_sqrt_softplus.restype = C.c_float
+        L.or_sqrt_softplus.argtypes = [C.c_float]
+        L.or_route_ex.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P, P]
         L.or_permute.argtypes = [P, i32, i32, i32, P, P, P, P, P, P]
         L.or_expert_ffn.argtypes = [i32, P, P, P, i32, i32, P, i32, P]
         L.or_moe_layer.restype = C.c_int
@@ -138,6 +141,29 @@ def route(x, w_r, bias, k: int, want_scores: bool = False):
     if want_scores:
         return ids, w, z, s
     return ids, w
+
+
+def route_ex(x, w_r, bias, k: int, score: int = 0, vision_bias=None, is_media=None, tid2eid=None,
+             token_ids=None):
+    """Router with the per-row rule of the device router notes: score 0 sigmoid, 1 sqrt(softplus);
+    media rows take vision_bias; on a hash layer (tid2eid given) text rows take tid2eid[token].
+    Returns ids, weights, error word."""
+    xb = bf16_bits(x)
+    T, d = xb.shape
+    wr = _np(w_r, np.float32)
+    E = wr.shape[1]
+    b = None if bias is None else _np(bias, np.float32)
+    vb = None if vision_bias is None else _np(vision_bias, np.float32)
+    md = None if is_media is None else np.ascontiguousarray(_np(is_media).astype(np.uint8))
+    tb = None if tid2eid is None else _np(tid2eid, np.int32)
+    tk = None if token_ids is None else _np(token_ids, np.int32)
+    vocab = 0 if tb is None else tb.shape[0]
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    err = np.zeros(1, dtype=np.int32)
+    lib().or_route_ex(_p(xb), _p(wr), _p(b), T, d, E, k, score, _p(vb), _p(md), _p(tb), _p(tk), vocab,
+                      _p(ids), _p(w), _p(err))
+    return ids, w, int(err[0])
 
 
 def permute(ids, E: int):

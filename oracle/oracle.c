@@ -28,6 +28,7 @@
  *   R5  stable counting sort of pair ids p = t*k + j by expert id.
  *   R6  FFN in FP64 on exactly dequantised weights, no SwiGLU clamp.
  *   R10 Engram head sum: acc = v_0, then acc = acc + v_h (float), h ascending.
+ *   R12 router variant score s = sqrt(softplus(z)) in float (see or_sqrt_softplus).
  *   Q2_K code packing: code i = (qs[i/4] >> 2*(i%4)) & 3; sub-block j holds
  *       weights 16j..16j+15 (the field order is given, the bit packing is not).
  *   Q8_0 field order: fp16 d first, then int8 q[32].
@@ -286,6 +287,128 @@ void or_route(const uint16_t *x, const float *wr, const float *bias, int T, int 
             S = (j == 0) ? s[ids[t * k]] : S + s[ids[t * k + j]];
         for (int j = 0; j < k; ++j)
             w[t * k + j] = s[ids[t * k + j]] / S;
+    }
+    free(s);
+    free(key);
+    free(used);
+}
+
+/* ------------------------------------------------------------------------- */
+/* router variants ([V] device router notes, the per-row rule of               */
+/* "SqrtSoftplusRouteTopk")                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* R12: exp(x) for -87 <= x <= 0 in float, every step one IEEE operation: Cody-Waite reduction
+ * n = rint(x log2 e), r = x - n ln2 (two float parts), the degree-7 Taylor polynomial of exp(r)
+ * in Horner form with fmaf, scaled by 2^n (n >= -126, so the scaling is exact). */
+static float or_exp_neg(float x)
+{
+    const float LOG2E = 1.44269504088896341f;
+    const float LN2_HI = 0.693359375f;
+    const float LN2_LO = -2.12194440054690583e-4f;
+    float n = rintf(x * LOG2E);
+    float r = fmaf(-n, LN2_HI, x);
+    r = fmaf(-n, LN2_LO, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return ldexpf(p, (int)n);
+}
+
+/* R12: s = sqrt(softplus(z)) in float.  softplus(z) = max(z, 0) + log1p(exp(-|z|)); e =
+ * exp(-|z|) as above (|z| > 87: e = 0); log1p(e) = 2 atanh(u) with u = e / (2 + e) <= 1/3, as
+ * 2u (1 + v/3 + v^2/5 + ... + v^7/15), v = u^2, Horner with fmaf; then sqrtf.  Every step is one
+ * IEEE float operation. */
+float or_sqrt_softplus(float z)
+{
+    if (isnan(z))
+        return z;
+    const float a = fabsf(z);
+    const float e = (a > 87.0f) ? 0.0f : or_exp_neg(-a);
+    const float u = e / (2.0f + e);
+    const float v = u * u;
+    float q = 1.0f / 15.0f;
+    q = fmaf(q, v, 1.0f / 13.0f);
+    q = fmaf(q, v, 1.0f / 11.0f);
+    q = fmaf(q, v, 1.0f / 9.0f);
+    q = fmaf(q, v, 1.0f / 7.0f);
+    q = fmaf(q, v, 1.0f / 5.0f);
+    q = fmaf(q, v, 1.0f / 3.0f);
+    q = fmaf(q, v, 1.0f);
+    const float l = 2.0f * (u * q);
+    const float sp = (z > 0.0f ? z : 0.0f) + l;
+    return sqrtf(sp);
+}
+
+/* Router with the per-row rule of the device router notes ([V]):
+ *   score_fn 0: s = or_sigmoid(z) (R2); 1: s = or_sqrt_softplus(z) (R12).
+ *   Row t is media when vbias and media are both given and media[t] != 0; a media row's key is
+ *   s + vbias, a text row's s + bias (bias NULL: 0).  Selection as R3.
+ *   tid2eid [vocab][k] (or NULL) with tok [T]: on such a hash layer a TEXT row's ids are
+ *   tid2eid[tok[t]][0..k) in table order (no key, no bias); media rows select as above.
+ *   Weights (R4) from the unbiased s of the row's ids, S in slot order.
+ *   Hash rows: tok[t] outside [0, vocab) sets err bit 2 and gives ids -1, weights 0; a table id
+ *   outside [0, E) sets err bit 1, is written as it is, and counts s = 0. */
+void or_route_ex(const uint16_t *x, const float *wr, const float *bias, int T, int d, int E, int k,
+                 int score_fn, const float *vbias, const uint8_t *media, const int32_t *tid2eid,
+                 const int32_t *tok, int vocab, int32_t *ids, float *w, int32_t *err)
+{
+    float *s = (float *)malloc(sizeof(float) * (size_t)E);
+    float *key = (float *)malloc(sizeof(float) * (size_t)E);
+    int *used = (int *)malloc(sizeof(int) * (size_t)E);
+    float sel[64];
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *xt = x + (int64_t)t * d;
+        const int is_media = vbias && media && media[t] != 0;
+        const float *rb = is_media ? vbias : bias;
+        for (int e = 0; e < E; ++e) {
+            float z = lane32_dot(xt, wr, d, E, e);
+            s[e] = score_fn == 1 ? or_sqrt_softplus(z) : or_sigmoid(z);
+            key[e] = s[e] + (rb ? rb[e] : 0.0f);
+            used[e] = 0;
+        }
+        int32_t *it = ids + (int64_t)t * k;
+        float *wt = w + (int64_t)t * k;
+        if (tid2eid && !is_media) {
+            if (tok[t] < 0 || tok[t] >= vocab) {
+                *err |= 2;
+                for (int j = 0; j < k; ++j) {
+                    it[j] = -1;
+                    wt[j] = 0.0f;
+                }
+                continue;
+            }
+            for (int j = 0; j < k; ++j) {
+                const int32_t id = tid2eid[(int64_t)tok[t] * k + j];
+                it[j] = id;
+                if (id < 0 || id >= E) {
+                    *err |= 1;
+                    sel[j] = 0.0f;
+                } else {
+                    sel[j] = s[id];
+                }
+            }
+        } else {
+            for (int j = 0; j < k; ++j) {
+                int best = -1;
+                for (int e = 0; e < E; ++e)
+                    if (!used[e] && (best < 0 || ranks_before(key[e], e, key[best], best)))
+                        best = e;
+                used[best] = 1;
+                it[j] = best;
+                sel[j] = s[best];
+            }
+        }
+        float S = 0.0f;
+        for (int j = 0; j < k; ++j)
+            S = (j == 0) ? sel[0] : S + sel[j];
+        for (int j = 0; j < k; ++j)
+            wt[j] = sel[j] / S;
     }
     free(s);
     free(key);

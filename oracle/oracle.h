@@ -23,6 +23,11 @@ void or_engram_gather(const uint8_t *const *tables, const int64_t *n_rows, int n
 void or_route(const uint16_t *x, const float *wr, const float *bias, int T, int d, int E, int k,
               int32_t *ids, float *w, float *z_out, float *s_out);
 
+float or_sqrt_softplus(float z);
+void or_route_ex(const uint16_t *x, const float *wr, const float *bias, int T, int d, int E, int k,
+                 int score_fn, const float *vbias, const uint8_t *media, const int32_t *tid2eid,
+                 const int32_t *tok, int vocab, int32_t *ids, float *w, int32_t *err);
+
 void or_permute(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *perm,
                 int32_t *inv, int32_t *active, int32_t *n_active, int32_t *err);
 

@@ -433,6 +433,120 @@ def test_router_ties_go_to_lower_id_and_bias_is_selection_only():
 
 
 # --------------------------------------------------------------------------- #
+# router variants (per-row rule of the device router notes)
+# --------------------------------------------------------------------------- #
+
+def test_sqrt_softplus_vs_high_precision():
+    """R12: the float sqrt(softplus(z)) is within 2 ulp of the exact value on |z| <= 87, and
+    its special values are those of the definition (or of the documented cut-off)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    zs = np.concatenate([np.linspace(-86.9, 86.9, 3001), np.random.default_rng(5).standard_normal(2000) * 6,
+                         [0.0, -1e-30, 1e-30, 1.0, -1.0, 15.0, -15.0, 40.0, -40.0]]).astype(np.float32)
+    for z in zs:
+        got = np.float32(L.or_sqrt_softplus(float(z)))
+        zz = mpmath.mpf(float(z))
+        exact = mpmath.sqrt(mpmath.log(1 + mpmath.exp(zz)))
+        ref = np.float32(float(exact))
+        ulp = float(np.spacing(ref))
+        assert abs(Fraction(float(got)) - Fraction(str(mpmath.nstr(exact, 40)))) <= 2 * Fraction(ulp), float(z)
+    assert L.or_sqrt_softplus(-100.0) == 0.0                      # |z| > 87: exp term dropped
+    assert L.or_sqrt_softplus(100.0) == np.float32(10.0)
+    assert math.isinf(L.or_sqrt_softplus(float("inf"))) and L.or_sqrt_softplus(float("-inf")) == 0.0
+    assert math.isnan(L.or_sqrt_softplus(float("nan")))
+    # monotone non-decreasing (so, without a bias, it selects what the logits select)
+    grid = np.linspace(-86.0, 86.0, 20001).astype(np.float32)
+    vals = np.array([L.or_sqrt_softplus(float(z)) for z in grid], dtype=np.float32)
+    assert np.all(np.diff(vals) >= 0)
+
+
+def _variant_inputs(seed=4, T=6, d=256, E=40, k=6):
+    x = synth.x_bf16(seed, 0, 0, T, d)
+    wr = synth.router_weight(seed, 0, d, E)
+    b = synth.route_bias(seed, 0, E, 0.3)
+    vb = synth.route_bias(seed, 1, E, 0.3)
+    return x, wr, b, vb
+
+
+def test_route_ex_defaults_equal_route():
+    x, wr, b, _ = _variant_inputs()
+    ids0, w0 = oracle.route(x, wr, b, 6)
+    ids1, w1, err = oracle.route_ex(x, wr, b, 6)
+    assert err == 0 and np.array_equal(ids0, ids1) and same_f32(w0, w1)
+
+
+def test_route_ex_media_rows_take_the_vision_bias():
+    x, wr, b, vb = _variant_inputs()
+    media = np.array([0, 1, 1, 0, 1, 0], dtype=np.uint8)
+    ids, w, err = oracle.route_ex(x, wr, b, 6, vision_bias=vb, is_media=media)
+    ids_t, w_t = oracle.route(x, wr, b, 6)
+    ids_m, w_m = oracle.route(x, wr, vb, 6)
+    assert err == 0
+    for t in range(len(media)):
+        ref_i, ref_w = (ids_m, w_m) if media[t] else (ids_t, w_t)
+        assert np.array_equal(ids[t], ref_i[t]) and same_f32(w[t], ref_w[t])
+    # without the vision bias nothing is media
+    ids2, w2, _ = oracle.route_ex(x, wr, b, 6, is_media=media)
+    assert np.array_equal(ids2, ids_t) and same_f32(w2, w_t)
+
+
+def test_route_ex_hash_rows_take_the_table():
+    x, wr, b, vb = _variant_inputs()
+    T, k, E = 6, 6, 40
+    rng = np.random.default_rng(11)
+    vocab = 50
+    table = np.stack([rng.permutation(E)[:k] for _ in range(vocab)]).astype(np.int32)
+    tok = rng.integers(0, vocab, size=T).astype(np.int32)
+    media = np.array([0, 0, 1, 0, 0, 1], dtype=np.uint8)
+    ids, w, err = oracle.route_ex(x, wr, b, k, vision_bias=vb, is_media=media, tid2eid=table, token_ids=tok)
+    _, _, _, s = oracle.route(x, wr, b, k, want_scores=True)     # unbiased sigmoid scores
+    ids_m, w_m = oracle.route(x, wr, vb, k)
+    assert err == 0
+    for t in range(T):
+        if media[t]:
+            assert np.array_equal(ids[t], ids_m[t]) and same_f32(w[t], w_m[t])
+            continue
+        assert np.array_equal(ids[t], table[tok[t]])
+        sel = s[t, table[tok[t]]]
+        S = np.float32(0)
+        for j, v in enumerate(sel):
+            S = v if j == 0 else np.float32(S + v)
+        assert same_f32(w[t], (sel / S).astype(np.float32))
+
+
+def test_route_ex_sqrt_softplus_selects_what_the_logits_select():
+    T, d, E, k = 8, 512, 32, 6
+    x = synth.x_bf16(9, 0, 0, T, d)
+    wr = synth.router_weight(9, 0, d, E)
+    ids, w, err = oracle.route_ex(x, wr, None, k, score=1)
+    _, _, z, _ = oracle.route(x, wr, None, k, want_scores=True)
+    z64 = x.double().numpy() @ wr.double().numpy()
+    assert err == 0
+    for t in range(T):
+        order = np.argsort(-z64[t], kind="stable")
+        if z64[t, order[k - 1]] - z64[t, order[k]] > 1e-6:
+            assert list(ids[t]) == list(order[:k])
+        sel = np.array([L.or_sqrt_softplus(float(z[t, e])) for e in ids[t]], dtype=np.float32)
+        S = np.float32(0)
+        for j, v in enumerate(sel):
+            S = v if j == 0 else np.float32(S + v)
+        assert same_f32(w[t], (sel / S).astype(np.float32))
+
+
+def test_route_ex_hash_errors():
+    x, wr, b, _ = _variant_inputs(T=3)
+    k, E = 6, 40
+    table = np.array([[0, 1, 2, 3, 4, 5], [7, 99, 8, 9, 10, -2]], dtype=np.int32)
+    tok = np.array([1, 5, 0], dtype=np.int32)          # row 1: token outside the table
+    ids, w, err = oracle.route_ex(x, wr, b, k, tid2eid=table, token_ids=tok)
+    assert err == 3
+    assert list(ids[0]) == [7, 99, 8, 9, 10, -2]
+    assert w[0, 1] == 0 and w[0, 5] == 0 and np.all(w[0, [0, 2, 3, 4]] > 0)
+    assert np.all(ids[1] == -1) and np.all(w[1] == 0)
+    assert list(ids[2]) == [0, 1, 2, 3, 4, 5]
+
+
+# --------------------------------------------------------------------------- #
 # permutation
 # --------------------------------------------------------------------------- #
 
