@@ -471,6 +471,65 @@ def run_engram(args, ws, rank, local):
             "us_median": round(med * 1e3, 2), "clocks": clk}
 
 
+def run_route(args, ws, rank, local):
+    """The decode router (T = 8, V4.1 shape) under the per-row rule of the device router notes:
+    the default (sigmoid, one bias), sqrt(softplus) scores, media rows with a vision bias, a hash
+    layer (text rows from tid2eid), and all three at once; one call per timed step."""
+    dev = torch.device("cuda", local)
+    T, sh = args.T, synth.V41
+    d, E, k = sh.d, sh.E, sh.k
+    w_r = synth.router_weight(SEED, 0, d, E).to(dev)
+    b = synth.route_bias(SEED, 0, E, sh.bias_half_width).to(dev)
+    vb = synth.route_bias(SEED, 1, E, sh.bias_half_width).to(dev)
+    xs = [synth.x_bf16(SEED, 0, s + 8 * rank, T, d).to(dev) for s in range(8)]
+    rng = np.random.default_rng(SEED + rank)
+    vocab = 129280
+    table = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(vocab)]).astype(np.int32)).to(dev)
+    tok = torch.from_numpy(rng.integers(0, vocab, T).astype(np.int32)).to(dev)
+    media = torch.from_numpy((np.arange(T) % 2).astype(np.uint8)).to(dev)   # every other row media
+    ws_r = torch.zeros(api.moe_route_workspace(T, E), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    modes = {
+        "sigmoid": dict(),
+        "sqrt_softplus": dict(score=api.SCORE_SQRT_SOFTPLUS),
+        "media_vision_bias": dict(vision_bias=vb, is_media=media),
+        "hash_tid2eid": dict(tid2eid=table, token_ids=tok),
+        "all": dict(score=api.SCORE_SQRT_SOFTPLUS, vision_bias=vb, is_media=media, tid2eid=table, token_ids=tok),
+    }
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    res_us = {}
+    barrier(ws)
+    clocks.start()
+    for name, kw in modes.items():
+        call = lambda i, kw=kw: api.moe_route_ex(xs[i % 8], w_r, b, k, ws=ws_r, dev_err=err, ids=ids, w=w, **kw)
+        for i in range(args.warmup):
+            call(i)
+        torch.cuda.synchronize()
+        ms = timed(call, args.steps, flush, stream)
+        res_us[name] = round(statistics.median(ms) * 1e3, 2)
+    clk = clocks.stop()
+    assert int(err) == 0
+    pk = peaks()
+    alg = d * E * 4 + T * d * 2 + E * 4 + T * k * 8          # W_r, x, bias, ids + weights
+    us = res_us["all"]
+    gbs = alg / (us * 1e-6) / 1e9
+    return {"metric": "router call latency, T=8 decode (V4.1 shape), per-row variant rule", "value": us, "unit": "us",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "moe_route_ex, T=8, d=4096, E=384, k=6: sqrt(softplus) scores, every other row "
+                                   "media (vision bias), hash layer for text rows (tid2eid over a 129,280-token vocab)",
+                       "l2": "flushed before every timed call"},
+            "variants_us_median": res_us,
+            "roofline": {"bound": "hbm", "kernel": "route_cluster_kernel", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": pk["source"], "bytes_per_call": alg},
+            "clocks": clk}
+
+
 def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     T = args.T
@@ -652,7 +711,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--T", type=int, default=8)
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "verify", "engram"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "verify", "engram", "route"],
                     help="decode (default, the headline line) or one of the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-engram", action="store_true",
@@ -668,7 +727,8 @@ def main():
         return
     ws, rank, local = dist_setup()
     if args.workload != "decode":
-        res = {"prefill": run_prefill, "verify": run_verify, "engram": run_engram}[args.workload](args, ws, rank, local)
+        res = {"prefill": run_prefill, "verify": run_verify, "engram": run_engram,
+               "route": run_route}[args.workload](args, ws, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -64,6 +64,31 @@ def moe_route(x, w_r, bias, k: int, ws=None, stream=None, ids=None, w=None):
     return ids, w
 
 
+SCORE_SIGMOID = 0
+SCORE_SQRT_SOFTPLUS = 1
+
+
+def moe_route_ex(x, w_r, bias, k: int, score: int = SCORE_SIGMOID, vision_bias=None, is_media=None,
+                 tid2eid=None, token_ids=None, ws=None, dev_err=None, stream=None, ids=None, w=None):
+    """moe_route with the per-row rule of the device router notes: score, media rows with a
+    vision bias, hash layers (tid2eid [vocab][k], token_ids [T]).  Returns (ids, w)."""
+    L = _lib.load()
+    T, d = x.shape
+    E = w_r.shape[1]
+    _dev(x, "x"), _dev(w_r, "w_r")
+    if ws is None:
+        ws = torch.zeros(L.moe_route_workspace(T, E), dtype=torch.uint8, device=x.device)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    vocab = 0 if tid2eid is None else tid2eid.shape[0]
+    check(L.moe_route_ex(ptr(x), ptr(w_r), ptr(bias), T, d, E, k, score, ptr(vision_bias), ptr(is_media),
+                         ptr(tid2eid), ptr(token_ids), vocab, ptr(ids), ptr(w), ptr(dev_err), ptr(ws), ws.numel(),
+                         stream_handle(stream)), "moe_route_ex")
+    return ids, w
+
+
 def moe_permute(ids, E: int, dev_err=None, stream=None, out=None):
     """out: optional dict of preallocated offsets [E+1], perm/inv [T*k], active [E], n_active [1]."""
     L = _lib.load()

@@ -69,6 +69,21 @@ bre_status moe_route(const void* x_bf16, const float* w_r, const float* bias, in
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+bre_status moe_route_ex(const void* x_bf16, const float* w_r, const float* bias, int T, int d, int E, int k,
+                        int score, const float* vision_bias, const uint8_t* is_media, const int32_t* tid2eid,
+                        const int32_t* token_ids, int vocab, int32_t* topk_ids, float* topk_w, int32_t* dev_err,
+                        void* ws, size_t ws_bytes, bre_stream_t stream) {
+  if (!x_bf16 || !w_r || !topk_ids || !topk_w || T <= 0 || d <= 0 || E <= 0 || k <= 0) return BRE_ERR_ARG;
+  if (score != BRE_SCORE_SIGMOID && score != BRE_SCORE_SQRT_SOFTPLUS) return BRE_ERR_ARG;
+  if (tid2eid && (!token_ids || vocab <= 0)) return BRE_ERR_ARG;
+  if (k > E || k > 32 || E > 1024 || d % 32 != 0) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(w_r, 16)) return BRE_ERR_ARG;
+  if (!ws || ws_bytes < route_ws_bytes(T, E) || !aligned(ws, 256)) return BRE_ERR_WORKSPACE;
+  return cuda_status(launch_route_ex(static_cast<const uint16_t*>(x_bf16), w_r, bias, T, d, E, k, score, vision_bias,
+                                     is_media, tid2eid, tid2eid ? token_ids : nullptr, tid2eid ? vocab : 0, topk_ids,
+                                     topk_w, dev_err, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bre_status moe_route_permute(const void* x_bf16, const float* w_r, const float* bias, int T, int d, int E, int k,
                              int32_t* topk_ids, float* topk_w, int32_t* offsets, int32_t* perm, int32_t* inv,
                              int32_t* active, int32_t* n_active, int32_t* dev_err, void* ws, size_t ws_bytes,

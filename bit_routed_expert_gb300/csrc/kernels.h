@@ -20,6 +20,10 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
 size_t route_ws_bytes(int T, int E);
 cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                          int32_t* ids, float* w, void* ws, cudaStream_t s);
+cudaError_t launch_route_ex(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                            int score, const float* vision_bias, const uint8_t* is_media, const int32_t* tid2eid,
+                            const int32_t* token_ids, int vocab, int32_t* ids, float* w, int32_t* err, void* ws,
+                            cudaStream_t s);
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
                            int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s);
 // route, then permute; for small batches the router kernel's last merging warp permutes too

@@ -57,12 +57,112 @@ __device__ __forceinline__ float sigmoid_ref(float z) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
+// exp(x) for -87 <= x <= 0 with the same steps as sigmoid_ref (n >= -126: 2^n is a normal
+// number and the scaling is exact).
+__device__ __forceinline__ float exp_neg_ref(float x) {
+  const float LOG2E = 1.44269504088896341f;
+  const float LN2_HI = 0.693359375f;
+  const float LN2_LO = -2.12194440054690583e-4f;
+  const float n = rintf(__fmul_rn(x, LOG2E));
+  float r = __fmaf_rn(-n, LN2_HI, x);
+  r = __fmaf_rn(-n, LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = __fmaf_rn(p, r, 1.0f / 720.0f);
+  p = __fmaf_rn(p, r, 1.0f / 120.0f);
+  p = __fmaf_rn(p, r, 1.0f / 24.0f);
+  p = __fmaf_rn(p, r, 1.0f / 6.0f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  return __fmul_rn(p, __int_as_float((127 + (int)n) << 23));
+}
+
+// s = sqrt(softplus(z)) in float (the vllm.cpp device router notes' SqrtSoftplusRouteTopk
+// score): softplus(z) = max(z, 0) + log1p(exp(-|z|)), exp(-|z|) as above (0 for |z| > 87),
+// log1p(e) = 2 atanh(u), u = e / (2 + e) <= 1/3, as 2u (1 + v/3 + ... + v^7/15), v = u^2, in
+// Horner form; every step one IEEE operation, so any conforming machine gets the same bits.
+__device__ __forceinline__ float sqrt_softplus_ref(float z) {
+  if (isnan(z)) return z;
+  const float a = fabsf(z);
+  const float e = a > 87.0f ? 0.0f : exp_neg_ref(-a);
+  const float u = __fdiv_rn(e, __fadd_rn(2.0f, e));
+  const float v = __fmul_rn(u, u);
+  float q = 1.0f / 15.0f;
+  q = __fmaf_rn(q, v, 1.0f / 13.0f);
+  q = __fmaf_rn(q, v, 1.0f / 11.0f);
+  q = __fmaf_rn(q, v, 1.0f / 9.0f);
+  q = __fmaf_rn(q, v, 1.0f / 7.0f);
+  q = __fmaf_rn(q, v, 1.0f / 5.0f);
+  q = __fmaf_rn(q, v, 1.0f / 3.0f);
+  q = __fmaf_rn(q, v, 1.0f);
+  const float l = __fmul_rn(2.0f, __fmul_rn(u, q));
+  return __fsqrt_rn(__fadd_rn(z > 0.0f ? z : 0.0f, l));
+}
+
+__device__ __forceinline__ float score_ref(float z, int fn) { return fn == 1 ? sqrt_softplus_ref(z) : sigmoid_ref(z); }
+
+// The per-row rule of the device router notes (SqrtSoftplusRouteTopk): row t is media when a
+// vision bias and a media mask are given and media[t] != 0; a media row's key is s + vbias and
+// it selects the top k; a text row's key is s + bias, and on a hash layer (tid2eid given) its
+// ids are tid2eid[tok[t]][0..k) instead.  Weights come from the unbiased s.  A token id outside
+// [0, vocab) sets BRE_DEVERR_ROW_ID (ids -1, weights 0); a table id outside [0, E) sets
+// BRE_DEVERR_EXPERT_ID, is passed on, and counts s = 0.
+struct RouteVar {
+  int score;               // 0 sigmoid, 1 sqrt(softplus)
+  const float* vbias;      // [E] or null
+  const uint8_t* media;    // [T] or null
+  const int32_t* tid2eid;  // [vocab][k] or null
+  const int32_t* tok;      // [T]
+  int vocab;
+  float* hash_s;           // [T][k] scratch (small-batch kernel): s of each hash row's table ids
+  int32_t* err;            // error word or null
+};
+
+__device__ __forceinline__ bool row_media(const RouteVar& rv, int t) {
+  return rv.vbias != nullptr && rv.media != nullptr && rv.media[t] != 0;
+}
+
 // Does (ka, ia) rank before (kb, ib)?  Larger key first, then lower id; NaN last.
 __device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib) {
   const bool na = isnan(ka), nb = isnan(kb);
   if (na != nb) return !na;
   if (!na && ka != kb) return ka > kb;
   return ia < ib;
+}
+
+// One warp writes a hash row's ids (tid2eid[tok[t]] in table order) and weights (its unbiased
+// scores, S in slot order).  s_src: the row's E scores (from_slots = false) or its k table
+// scores in slot order (from_slots = true, the small-batch kernel's hash_s).
+__device__ void hash_row(const float* __restrict__ s_src, int E, int k, const RouteVar& rv, int t,
+                         int32_t* __restrict__ ids_t, float* __restrict__ w_t, bool from_slots) {
+  const int lane = threadIdx.x & 31;
+  const int tk = __ldg(rv.tok + t);
+  if (tk < 0 || tk >= rv.vocab) {
+    if (lane < k) {
+      ids_t[lane] = -1;
+      w_t[lane] = 0.0f;
+    }
+    if (lane == 0 && rv.err) atomicOr(rv.err, BRE_DEVERR_ROW_ID);
+    return;
+  }
+  int id = 0;
+  float sj = 0.0f;
+  bool bad = false;
+  if (lane < k) {
+    id = __ldg(rv.tid2eid + (size_t)tk * k + lane);
+    bad = id < 0 || id >= E;
+    if (!bad) sj = from_slots ? __ldcg(s_src + lane) : __ldcg(s_src + id);
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && rv.err) atomicOr(rv.err, BRE_DEVERR_EXPERT_ID);
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const float v = __shfl_sync(0xffffffffu, sj, j);
+    S = (j == 0) ? v : __fadd_rn(S, v);
+  }
+  if (lane < k) {
+    ids_t[lane] = id;
+    w_t[lane] = __fdiv_rn(sj, S);
+  }
 }
 
 // One warp selects the top k of the E scores of one token and writes ids and weights; lane l
@@ -280,7 +380,7 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
                          const float* __restrict__ bias, int T, int d, int E, int k, uint32_t* __restrict__ cand_c,
                          float* __restrict__ cand_s, int* __restrict__ cand_id, int* tickets,
                          int32_t* __restrict__ ids, float* __restrict__ wts, const PermOut po, int merge_group,
-                         int32_t* err, const __grid_constant__ RouteMap wm) {
+                         int32_t* err, const __grid_constant__ RouteMap wm, const RouteVar rv) {
   extern __shared__ __align__(128) float rc_smem[];
   __shared__ float part[SMALL_TT][RC_J][33];     // partial sums of this CTA's j, padded
   __shared__ __align__(8) uint64_t wbar;
@@ -406,8 +506,18 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
 #pragma unroll
       for (int q = 0; q < o; ++q) v[q] = __fadd_rn(v[q], v[q + o]);
     const bool valid = e < E;
-    const float sv = valid ? sigmoid_ref(v[0]) : 0.0f;
-    const float key = __fadd_rn(sv, (bias && valid) ? __ldg(bias + e) : 0.0f);
+    const int t = t0 + (int)r;
+    const bool media = row_media(rv, t);
+    const float* rb = media ? rv.vbias : bias;
+    const float sv = valid ? score_ref(v[0], rv.score) : 0.0f;
+    const float key = __fadd_rn(sv, (rb && valid) ? __ldg(rb + e) : 0.0f);
+    if (rv.tid2eid != nullptr && !media) {
+      // a hash row: the expert's score goes to every slot of the row's table that names it
+      const int tk = __ldg(rv.tok + t);
+      if (valid && tk >= 0 && tk < rv.vocab)
+        for (int q = 0; q < k; ++q)
+          if (__ldg(rv.tid2eid + (size_t)tk * k + q) == e) rv.hash_s[(size_t)t * k + q] = sv;
+    }
     const uint32_t code = valid ? key_code(key) : 0xFFFFFFFFu;   // absent experts: last (id >= E)
     int rank = 0;
 #pragma unroll 8
@@ -474,6 +584,8 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
       }
     }
     __syncthreads();
+    // hash rows (text rows of a hash layer) take their table instead of a merge
+    auto hash_t = [&](int t) { return rv.tid2eid != nullptr && !row_media(rv, t); };
     if (nblk <= 16 && k <= 16) {
       // two tokens per warp, one per half-warp
       for (int p0 = 2 * warp; p0 < ng; p0 += 2 * RC_J) {
@@ -482,15 +594,21 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
         const int ts = act ? tt : p0;
         const int t = g0 + ts;
         merge_token<16>(mc + (size_t)ts * slots, mid + (size_t)ts * slots, ms + (size_t)ts * slots, nblk, kc, k,
-                        lane & 15, act, ids + (size_t)t * k, wts + (size_t)t * k, ids_s + (size_t)t * k);
+                        lane & 15, act && !hash_t(t), ids + (size_t)t * k, wts + (size_t)t * k,
+                        ids_s + (size_t)t * k);
       }
     } else {
       for (int tt = warp; tt < ng; tt += RC_J) {
         const int t = g0 + tt;
         merge_token<32>(mc + (size_t)tt * slots, mid + (size_t)tt * slots, ms + (size_t)tt * slots, nblk, kc, k,
-                        lane, true, ids + (size_t)t * k, wts + (size_t)t * k, ids_s + (size_t)t * k);
+                        lane, !hash_t(t), ids + (size_t)t * k, wts + (size_t)t * k, ids_s + (size_t)t * k);
       }
     }
+    if (rv.tid2eid != nullptr)
+      for (int tt = warp; tt < ng; tt += RC_J) {
+        const int t = g0 + tt;
+        if (hash_t(t)) hash_row(rv.hash_s + (size_t)t * k, E, k, rv, t, ids + (size_t)t * k, wts + (size_t)t * k, true);
+      }
     __syncthreads();
   }
   if (po.offsets == nullptr) return;
@@ -584,7 +702,7 @@ constexpr size_t TILED_SMEM = (size_t)TSTAGES * (TR * TW * 4 + TILE_T * TR * 2);
 
 __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t* __restrict__ x,
                                                                   const float* __restrict__ w_r, int T, int d,
-                                                                  int E, float* __restrict__ S) {
+                                                                  int E, float* __restrict__ S, int score_fn) {
   extern __shared__ __align__(16) unsigned char tsm[];
   float* Wst = reinterpret_cast<float*>(tsm);                                          // [TSTAGES][TR][TW]
   uint16_t* Xst = reinterpret_cast<uint16_t*>(tsm + (size_t)TSTAGES * TR * TW * 4);    // [TSTAGES][TILE_T][TR]
@@ -672,7 +790,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t
     for (int b = 0; b < 8; ++b) {
       if (lane == ((a * 8 + b) & 31)) {
         const int t = t0 + tsub + a, e = e0 + esub + b;
-        if (t < T && e < E) S[(size_t)t * E + e] = sigmoid_ref(acc[a][b]);
+        if (t < T && e < E) S[(size_t)t * E + e] = score_ref(acc[a][b], score_fn);
       }
     }
 }
@@ -680,11 +798,16 @@ __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t
 template <int NI>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ S, const float* __restrict__ bias,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ wts) {
+                                                   float* __restrict__ wts, const RouteVar rv) {
   pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_warp<NI>(S + (size_t)t * E, bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
+  const bool media = row_media(rv, t);
+  if (rv.tid2eid != nullptr && !media) {
+    hash_row(S + (size_t)t * E, E, k, rv, t, ids + (size_t)t * k, wts + (size_t)t * k, false);
+    return;
+  }
+  topk_warp<NI>(S + (size_t)t * E, media ? rv.vbias : bias, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
 }
 
 // Stable counting sort of pair ids by expert, one CTA of 1024 threads.  Pairs are taken
@@ -814,29 +937,48 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) permute_kernel(const int32_t*
 size_t route_ws_bytes(int T, int E) {
   // scores (T x E) for the large-batch path; candidates (s, id) for the small-batch path
   size_t s = (size_t)T * E * sizeof(float);
-  if (T <= SMALL_T_MAX) s = std::max(s, (size_t)T * rc_slots(E, 32) * 12);
+  // small batches: candidates (12 bytes a slot), then the hash rows' table scores [T][32]
+  if (T <= SMALL_T_MAX) s = std::max(s, (size_t)T * rc_slots(E, 32) * 12 + (size_t)T * 32 * 4);
   s = (s + 255) & ~(size_t)255;
   return s + 256;
 }
 
 namespace {
 cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
-                       int32_t* ids, float* w, void* ws, const PermOut& po, int32_t* err, bool* permuted,
+                       int32_t* ids, float* w, void* ws, const PermOut& po, const RouteVar& rv, bool* permuted,
                        cudaStream_t s);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                          int32_t* ids, float* w, void* ws, cudaStream_t s) {
   bool permuted = false;
-  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, nullptr, &permuted, s);
+  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, RouteVar{}, &permuted, s);
+}
+
+cudaError_t launch_route_ex(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
+                            int score, const float* vision_bias, const uint8_t* is_media, const int32_t* tid2eid,
+                            const int32_t* token_ids, int vocab, int32_t* ids, float* w, int32_t* err, void* ws,
+                            cudaStream_t s) {
+  bool permuted = false;
+  RouteVar rv{};
+  rv.score = score;
+  rv.vbias = vision_bias;
+  rv.media = is_media;
+  rv.tid2eid = tid2eid;
+  rv.tok = token_ids;
+  rv.vocab = vocab;
+  rv.err = err;
+  return route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{}, rv, &permuted, s);
 }
 
 cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                                  int32_t* ids, float* w, int32_t* offsets, int32_t* perm, int32_t* inv,
                                  int32_t* active, int32_t* n_active, int32_t* err, void* ws, cudaStream_t s) {
   bool permuted = false;
+  RouteVar rv{};
+  rv.err = err;
   const cudaError_t e =
-      route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, err, &permuted,
+      route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, rv, &permuted,
                  s);
   if (e != cudaSuccess || permuted) return e;
   return launch_permute(ids, T, k, E, offsets, perm, inv, active, n_active, err, s);
@@ -879,8 +1021,10 @@ bool route_map(RouteMap* rm, const float* w_r, int d, int E) {
 }
 
 cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
-                       int32_t* ids, float* w, void* ws, const PermOut& po, int32_t* err, bool* permuted,
+                       int32_t* ids, float* w, void* ws, const PermOut& po, const RouteVar& rv_in, bool* permuted,
                        cudaStream_t s) {
+  RouteVar rv = rv_in;
+  int32_t* err = rv.err;
   // the small-batch kernel's ticket sits at a fixed offset, so that calls with different T share it
   int* ticket = reinterpret_cast<int*>(ws);
   float* S = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
@@ -909,10 +1053,11 @@ cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, i
     uint32_t* cand_c = reinterpret_cast<uint32_t*>(S);
     float* cand_s = S + (size_t)T * slots;
     int* cand_id = reinterpret_cast<int*>(S + (size_t)2 * T * slots);
+    rv.hash_s = S + (size_t)3 * T * rc_slots(E, 32);   // after the largest candidate area
     dim3 grid((E + 31) / 32, RC_CLUSTER, (T + SMALL_TT - 1) / SMALL_TT);
     {
       const cudaError_t le = launch_k(route_cluster_kernel, dim3(grid), dim3(RC_THREADS), smem, s, x, w_r, bias, T,
-                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w, po, merge_group, err, rm);
+                                      d, E, k, cand_c, cand_s, cand_id, ticket, ids, w, po, merge_group, err, rm, rv);
       if (le != cudaSuccess) return le;
     }
     *permuted = po.offsets != nullptr;
@@ -929,14 +1074,15 @@ cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, i
   }
   dim3 grid((T + TILE_T - 1) / TILE_T, (E + TILE_E - 1) / TILE_E);
   {
-    const cudaError_t le = launch_k(route_tiled_kernel, dim3(grid), dim3(TTHREADS), TILED_SMEM, s, x, w_r, T, d, E, S);
+    const cudaError_t le =
+        launch_k(route_tiled_kernel, dim3(grid), dim3(TTHREADS), TILED_SMEM, s, x, w_r, T, d, E, S, rv.score);
     if (le != cudaSuccess) return le;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
     auto kern = E <= 32 ? topk_kernel<1> : E <= 128 ? topk_kernel<4> : E <= 384 ? topk_kernel<12> : topk_kernel<32>;
-    const cudaError_t le = launch_k(kern, dim3((T + 7) / 8), dim3(256), 0, s, S, bias, T, E, k, ids, w);
+    const cudaError_t le = launch_k(kern, dim3((T + 7) / 8), dim3(256), 0, s, S, bias, T, E, k, ids, w, rv);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();

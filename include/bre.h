@@ -138,6 +138,32 @@ bre_status moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *of
                        int32_t *inv, int32_t *active, int32_t *n_active, int32_t *dev_err,
                        bre_stream_t stream);
 
+/* moe_route with the per-row rule of the vllm.cpp PR "DeepSeek-V4-Flash-Vision tower", device
+ * router notes (SqrtSoftplusRouteTopk):
+ *   score: BRE_SCORE_SIGMOID (the float sigmoid above) or BRE_SCORE_SQRT_SOFTPLUS:
+ *     s = sqrt(softplus(z)), softplus(z) = max(z, 0) + log1p(exp(-|z|)), in float with every
+ *     step one IEEE operation (exp(-|z|) by the sigmoid's exp, 0 for |z| > 87; log1p(e) =
+ *     2 atanh(u), u = e / (2 + e), by the degree-7 series in u^2 with fmaf), so it is
+ *     reproducible bit for bit;
+ *   row t is a media row when vision_bias and is_media are both given and is_media[t] != 0:
+ *     its key is s + vision_bias[e] and it selects the top k; a text row's key is s + bias[e]
+ *     (bias NULL: s);
+ *   tid2eid [vocab][k] int32 (or NULL): a hash layer -- a TEXT row's ids are
+ *     tid2eid[token_ids[t]][0..k) in table order, with no key; media rows select as above;
+ *   weights always from the UNBIASED s of the row's ids, S summed in slot order.
+ *   Hash rows: token_ids[t] outside [0, vocab) sets BRE_DEVERR_ROW_ID and gives ids -1 and
+ *   weights 0; a table id outside [0, E) sets BRE_DEVERR_EXPERT_ID, is written as it is (so
+ *   moe_permute places it after every group) and counts s = 0.
+ *   vision_bias [E] FP32, is_media [T] uint8, token_ids [T] int32: device pointers.
+ *   dev_err may be NULL.  Other arguments, limits and ws as for moe_route; with no option set
+ *   (score 0, all pointers NULL) it computes exactly what moe_route computes. */
+#define BRE_SCORE_SIGMOID 0
+#define BRE_SCORE_SQRT_SOFTPLUS 1
+bre_status moe_route_ex(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
+                        int score, const float *vision_bias, const uint8_t *is_media, const int32_t *tid2eid,
+                        const int32_t *token_ids, int vocab, int32_t *topk_ids, float *topk_w, int32_t *dev_err,
+                        void *ws, size_t ws_bytes, bre_stream_t stream);
+
 /* moe_route followed by moe_permute, with the same arguments and outputs as the two calls
  * (ws: moe_route_workspace(T, E) bytes, zero-filled once after allocation).  For batches of
  * at most 32 tokens the router kernel's last CTA (the one that merges every token's

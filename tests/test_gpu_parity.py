@@ -202,6 +202,84 @@ def test_route_permute_fused(cuda_dev, shape, T):
     assert int(err) == 0
 
 
+def _variant_case(T, d, E, k, seed):
+    x = synth.x_bf16(seed, 0, 3, T, d)
+    w_r = synth.router_weight(seed, 0, d, E)
+    b = synth.route_bias(seed, 0, E, 0.3)
+    vb = synth.route_bias(seed, 1, E, 0.3)
+    rng = np.random.default_rng(seed)
+    media = (rng.random(T) < 0.4).astype(np.uint8)
+    vocab = 1000
+    table = np.stack([rng.permutation(E)[:k] for _ in range(vocab)]).astype(np.int32)
+    tok = rng.integers(0, vocab, T).astype(np.int32)
+    return x, w_r, b, vb, media, table, tok
+
+
+_VARIANT_MODES = {
+    "softplus": dict(score=1),
+    "media": dict(media=True),
+    "hash": dict(hash=True),
+    "hash_softplus_media": dict(score=1, media=True, hash=True),
+}
+
+
+@pytest.mark.parametrize("T,d,E,k", [(1, 4096, 384, 6), (8, 4096, 384, 6), (5, 256, 40, 6), (32, 512, 384, 6),
+                                     (33, 256, 70, 9), (300, 512, 384, 6)])
+@pytest.mark.parametrize("mode", list(_VARIANT_MODES))
+def test_route_ex_bit_exact(cuda_dev, T, d, E, k, mode):
+    """moe_route_ex equals the oracle bit for bit in every mode of the per-row rule, on both
+    router kernels (T <= 32 and T > 32) and with partial expert blocks."""
+    x, w_r, b, vb, media, table, tok = _variant_case(T, d, E, k, SEED + T + E)
+    o = _VARIANT_MODES[mode]
+    score = o.get("score", 0)
+    kw_ref = dict(score=score)
+    if o.get("media"):
+        kw_ref.update(vision_bias=vb, is_media=media)
+    if o.get("hash"):
+        kw_ref.update(tid2eid=table, token_ids=tok)
+    ids_ref, w_ref, err_ref = oracle.route_ex(x, w_r, b, k, **kw_ref)
+    dv = cuda_dev
+    kw = dict(score=score)
+    if o.get("media"):
+        kw.update(vision_bias=vb.to(dv), is_media=torch.from_numpy(media).to(dv))
+    if o.get("hash"):
+        kw.update(tid2eid=torch.from_numpy(table).to(dv), token_ids=torch.from_numpy(tok).to(dv))
+    err = torch.zeros(1, dtype=torch.int32, device=dv)
+    ws = torch.zeros(api.moe_route_workspace(T, E), dtype=torch.uint8, device=dv)
+    for _ in range(2):   # the second call reuses the workspace
+        ids, w = api.moe_route_ex(x.to(dv), w_r.to(dv), b.to(dv), k, ws=ws, dev_err=err, **kw)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+    assert int(err) == err_ref == 0
+
+
+@pytest.mark.parametrize("T", [4, 8, 40])
+def test_route_ex_defaults_equal_moe_route(cuda_dev, T):
+    x, w_r, b, _, _, _, _ = _variant_case(T, 512, 384, 6, 3)
+    ids0, w0 = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), 6)
+    ids1, w1 = api.moe_route_ex(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), 6)
+    assert torch.equal(ids0, ids1) and torch.equal(w0.view(torch.int32), w1.view(torch.int32))
+
+
+@pytest.mark.parametrize("T", [3, 40])
+def test_route_ex_hash_errors(cuda_dev, T):
+    """A token outside the table gives ids -1 and weights 0 (BRE_DEVERR_ROW_ID); a table id
+    outside [0, E) is passed on with weight 0 (BRE_DEVERR_EXPERT_ID) -- as the oracle."""
+    d, E, k = 256, 40, 6
+    x, w_r, b, _, _, _, _ = _variant_case(T, d, E, k, 8)
+    table = np.array([[0, 1, 2, 3, 4, 5], [7, 99, 8, 9, 10, -2]], dtype=np.int32)
+    tok = np.resize(np.array([1, 5, 0], dtype=np.int32), T)
+    ids_ref, w_ref, err_ref = oracle.route_ex(x, w_r, b, k, tid2eid=table, token_ids=tok)
+    assert err_ref == 3
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    ids, w = api.moe_route_ex(x.to(cuda_dev), w_r.to(cuda_dev), b.to(cuda_dev), k,
+                              tid2eid=torch.from_numpy(table).to(cuda_dev),
+                              token_ids=torch.from_numpy(tok).to(cuda_dev), dev_err=err)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+    assert int(err) == err_ref
+
+
 def test_route_ties_and_zero_bias(cuda_dev):
     d, E, k = 64, 16, 6
     x = synth.x_bf16(2, 0, 0, 3, d)
