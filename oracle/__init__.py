@@ -65,6 +65,8 @@ def lib():
         L.or_sqrt_softplus.argtypes = [C.c_float]
         L.or_route_ex.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P, P]
         L.or_permute.argtypes = [P, i32, i32, i32, P, P, P, P, P, P]
+        L.or_engram_kv.argtypes = [P, P, i32, i32, i32, P]
+        L.or_engram_gate.argtypes = [P, P, P, P, P, i32, i32, C.c_double, P]
         L.or_expert_ffn.argtypes = [i32, P, P, P, i32, i32, P, i32, P]
         L.or_moe_layer.restype = C.c_int
         L.or_moe_layer.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32, P, P, P, P]
@@ -164,6 +166,32 @@ def route_ex(x, w_r, bias, k: int, score: int = 0, vision_bias=None, is_media=No
     lib().or_route_ex(_p(xb), _p(wr), _p(b), T, d, E, k, score, _p(vb), _p(md), _p(tb), _p(tk), vocab,
                       _p(ids), _p(w), _p(err))
     return ids, w, int(err[0])
+
+
+def engram_kv(rows, w_kv) -> np.ndarray:
+    """FP64 product of the gathered rows [T][K] (BF16) and engram_kv.weight [N][K] (BF16)."""
+    rb = bf16_bits(rows)
+    wb = bf16_bits(w_kv)
+    T, K = rb.shape
+    N = wb.shape[0]
+    kv = np.empty((T, N), dtype=np.float64)
+    lib().or_engram_kv(_p(rb), _p(wb), T, K, N, _p(kv))
+    return kv
+
+
+def engram_gate(kv, resid, q_norm, k_norm, mask=None, eps: float = 1e-6):
+    """Gate and residual injection on four hyper-connection branches: returns (new residual
+    [T][4][W] as BF16 bits, gates [T][4] in FP64)."""
+    kv = np.ascontiguousarray(np.asarray(kv, dtype=np.float64))
+    r = bf16_bits(resid).copy()
+    T = r.shape[0]
+    W = r.shape[-1]
+    qn = _np(q_norm, np.float32)
+    kn = _np(k_norm, np.float32)
+    m = None if mask is None else np.ascontiguousarray(_np(mask).astype(np.uint8))
+    g = np.empty((T, 4), dtype=np.float64)
+    lib().or_engram_gate(_p(kv), _p(r), _p(qn), _p(kn), _p(m), T, W, eps, _p(g))
+    return r, g
 
 
 def permute(ids, E: int):

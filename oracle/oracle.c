@@ -622,3 +622,68 @@ void or_rmsnorm(const uint16_t *x, int T, int d, float eps, uint16_t *u)
             u[(int64_t)t * d + c] = or_bf16_rne(or_bf16_to_f32(xt[c]) * r);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Engram gate and residual injection ([I] "Placement"), in FP64               */
+/* ------------------------------------------------------------------------- */
+
+/* kv[t][n] = sum_c rows[t][c] * w[n][c] (FP64; rows and w BF16, w stored [N][K], rows of w are
+ * the outputs).  The product of the gathered rows and engram_kv.weight. */
+void or_engram_kv(const uint16_t *rows, const uint16_t *w, int T, int K, int N, double *kv)
+{
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *r = rows + (int64_t)t * K;
+        for (int n = 0; n < N; ++n) {
+            const uint16_t *wn = w + (int64_t)n * K;
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c)
+                acc += (double)or_bf16_to_f32(r[c]) * (double)or_bf16_to_f32(wn[c]);
+            kv[(int64_t)t * N + n] = acc;
+        }
+    }
+}
+
+/* For every token t (mask NULL or mask[t] == 0) and branch h < 4, with key_h = kv[t][h W ..],
+ * value = kv[t][4 W ..] (four keys, then the shared value, each width W):
+ *   dot = sum_i r[h,i] qn[h,i] kn[h,i] key[h,i]
+ *   dot *= 1/sqrt(mean(r[h,:]^2) + eps) * 1/sqrt(mean(key[h,:]^2) + eps) * 1/sqrt(W)
+ *   gate = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot))
+ *   r[h,i] = bf16(r[h,i] + gate * bf16(value[i]))
+ * in FP64 with one rounding to BF16 at each bf16(); masked tokens keep r unchanged.  resid is
+ * [T][4][W] BF16, updated in place; gate_out [T][4] (or NULL) receives the gates (0 for masked
+ * tokens). */
+void or_engram_gate(const double *kv, uint16_t *resid, const float *qn, const float *kn, const uint8_t *mask,
+                    int T, int W, double eps, double *gate_out)
+{
+    for (int t = 0; t < T; ++t) {
+        const double *kvt = kv + (int64_t)t * 5 * W;
+        for (int h = 0; h < 4; ++h) {
+            uint16_t *r = resid + ((int64_t)t * 4 + h) * W;
+            if (mask && mask[t]) {
+                if (gate_out)
+                    gate_out[t * 4 + h] = 0.0;
+                continue;
+            }
+            const double *key = kvt + (int64_t)h * W;
+            double dot = 0.0, rr = 0.0, kk = 0.0;
+            for (int i = 0; i < W; ++i) {
+                const double ri = (double)or_bf16_to_f32(r[i]);
+                dot += ri * (double)qn[h * W + i] * (double)kn[h * W + i] * key[i];
+                rr += ri * ri;
+                kk += key[i] * key[i];
+            }
+            dot *= 1.0 / sqrt(rr / W + eps);
+            dot *= 1.0 / sqrt(kk / W + eps);
+            dot *= 1.0 / sqrt((double)W);
+            const double m = sqrt(fabs(dot) > 1e-6 ? fabs(dot) : 1e-6);
+            const double g = 1.0 / (1.0 + exp(-copysign(m, dot)));
+            if (gate_out)
+                gate_out[t * 4 + h] = g;
+            const double *val = kvt + (int64_t)4 * W;
+            for (int i = 0; i < W; ++i) {
+                const double vb = (double)or_bf16_to_f32(or_bf16_rne_f64(val[i]));
+                r[i] = or_bf16_rne_f64((double)or_bf16_to_f32(r[i]) + g * vb);
+            }
+        }
+    }
+}

@@ -43,4 +43,8 @@ int or_moe_layer(const uint16_t *x, int T, int d, int E, int k, int F, const flo
 void or_residual(const uint16_t *x, const uint16_t *moe, int T, int d, float scale, uint16_t *x_new);
 void or_rmsnorm(const uint16_t *x, int T, int d, float eps, uint16_t *u);
 
+void or_engram_kv(const uint16_t *rows, const uint16_t *w, int T, int K, int N, double *kv);
+void or_engram_gate(const double *kv, uint16_t *resid, const float *qn, const float *kn, const uint8_t *mask,
+                    int T, int W, double eps, double *gate_out);
+
 #endif

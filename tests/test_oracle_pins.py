@@ -672,3 +672,103 @@ def test_verify_stack_literal_recurrence_overflows():
             break
         finite_layers += 1
     assert finite_layers < 6
+
+
+# --------------------------------------------------------------------------- #
+# Engram gate and residual injection (closed forms and invariants)
+# --------------------------------------------------------------------------- #
+
+def _bf16(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _sig(x):
+    return 1.0 / (1.0 + math.exp(-x))
+
+
+def test_engram_kv_is_a_plain_product():
+    """A selection matrix (one power of two per row) reproduces the chosen inputs exactly, and
+    a product with integer entries is exact in FP64."""
+    rng = np.random.default_rng(3)
+    T, K, N = 3, 96, 40
+    rows = _bf16(rng.standard_normal((T, K)))
+    pick = rng.integers(0, K, N)
+    w = np.zeros((N, K), dtype=np.float32)
+    w[np.arange(N), pick] = 2.0 ** rng.integers(-3, 4, N)
+    kv = oracle.engram_kv(rows, _bf16(w))
+    assert np.array_equal(kv, rows.float().numpy()[:, pick] * w[np.arange(N), pick])
+    ri = _bf16(rng.integers(-8, 9, (T, K)))
+    wi = _bf16(rng.integers(-8, 9, (N, K)))
+    assert np.array_equal(oracle.engram_kv(ri, wi), ri.double().numpy() @ wi.double().numpy().T)
+
+
+def _gate_case(T=2, W=64, seed=0):
+    rng = np.random.default_rng(seed)
+    kv = rng.standard_normal((T, 5 * W))
+    resid = _bf16(rng.standard_normal((T, 4, W)))
+    qn = (1 + 0.1 * rng.standard_normal((4, W))).astype(np.float32)
+    kn = (1 + 0.1 * rng.standard_normal((4, W))).astype(np.float32)
+    return kv, resid, qn, kn
+
+
+def test_engram_gate_known_dot():
+    """r = 1, qn = kn = 1, key = a: dot = W a / sqrt(1 + eps) / sqrt(a^2 + eps) / sqrt(W); the
+    update is bf16(1 + g * bf16(v)) for a constant value v."""
+    T, W, eps = 1, 5120, 1e-6
+    for a, v in ((0.75, 0.3), (-2.0, 1.5), (1e-3, -0.7)):
+        kv = np.zeros((T, 5 * W))
+        kv[:, :4 * W] = a
+        kv[:, 4 * W:] = v
+        resid = _bf16(np.ones((T, 4, W)))
+        ones = np.ones((4, W), dtype=np.float32)
+        out, g = oracle.engram_gate(kv, resid, ones, ones, eps=eps)
+        dot = W * a / math.sqrt(1 + eps) / math.sqrt(a * a + eps) / math.sqrt(W)
+        ref_g = _sig(math.copysign(math.sqrt(max(abs(dot), 1e-6)), dot))
+        assert np.allclose(g, ref_g, rtol=0, atol=1e-12)
+        vb = float(_bf16([v]).float()[0])
+        ref = _bf16(np.full((T, 4, W), 1.0 + ref_g * vb))
+        assert np.array_equal(out, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_engram_gate_zero_key_floor_and_zero_value_identity():
+    kv, resid, qn, kn = _gate_case()
+    W = resid.shape[-1]
+    kv0 = kv.copy()
+    kv0[:, :4 * W] = 0.0                                  # dot = 0 -> gate = sigmoid(+1e-3)
+    _, g = oracle.engram_gate(kv0, resid, qn, kn)
+    assert np.allclose(g, _sig(1e-3), rtol=0, atol=1e-15)
+    kv1 = kv.copy()
+    kv1[:, 4 * W:] = 0.0                                  # no value: the residual is unchanged
+    out, _ = oracle.engram_gate(kv1, resid, qn, kn)
+    assert np.array_equal(out, resid.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_engram_gate_masked_rows_unchanged():
+    kv, resid, qn, kn = _gate_case(T=3)
+    mask = np.array([0, 1, 0], dtype=np.uint8)
+    out, g = oracle.engram_gate(kv, resid, qn, kn, mask=mask)
+    rb = resid.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out[1], rb[1]) and np.all(g[1] == 0)
+    assert not np.array_equal(out[0], rb[0])
+
+
+def test_engram_gate_invariances():
+    """The gate does not change when a branch's residual or key is scaled (both norms divide the
+    scale out; exact up to eps), and negating the residual gives 1 - gate."""
+    kv, resid, qn, kn = _gate_case(T=2, W=256, seed=5)
+    W = 256
+    _, g = oracle.engram_gate(kv, resid, qn, kn)
+    _, g2 = oracle.engram_gate(kv, _bf16(resid.float().numpy() * 4.0), qn, kn)
+    # eps = 1e-6 against mean squares near 1 moves the gate by well under 1e-6
+    assert np.allclose(g, g2, rtol=0, atol=1e-6)
+    kvs = kv.copy()
+    kvs[:, :4 * W] *= 4.0
+    _, g3 = oracle.engram_gate(kvs, resid, qn, kn)
+    assert np.allclose(g, g3, rtol=0, atol=1e-6)
+    _, gn = oracle.engram_gate(kv, _bf16(-resid.float().numpy()), qn, kn)
+    assert np.allclose(g + gn, 1.0, rtol=0, atol=1e-12)
+    # the gate depends on the branch's own key only
+    kvb = kv.copy()
+    kvb[:, 1 * W:2 * W] = 3.0
+    _, g4 = oracle.engram_gate(kvb, resid, qn, kn)
+    assert np.array_equal(g4[:, [0, 2, 3]], g[:, [0, 2, 3]]) and not np.allclose(g4[:, 1], g[:, 1])
