@@ -530,6 +530,52 @@ def run_route(args, ws, rank, local):
             "clocks": clk}
 
 
+def run_engram_gate(args, ws, rank, local):
+    """Engram gate and residual injection for one layer at decode size: T = 8 tokens, R = 24 rows
+    of a 4,194,304-row table per token, engram_kv.weight [5 x 5120][24 x 256] BF16 (315 MB), four
+    hyper-connection branches of width 5120."""
+    dev = torch.device("cuda", local)
+    T, R, W = args.T, 24, 5120
+    K, N = 256 * R, 5 * W
+    table = synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, 0), ENGRAM_ROWS, device=dev)
+    ids = [synth.engram_ids_uniform(SEED + 31 * s + rank, T * R, ENGRAM_ROWS).view(T, R).to(dev) for s in range(8)]
+    w_kv = synth.engram_kv_weight(SEED, 0, N, K, device=dev)
+    resid0 = synth.engram_residual(SEED, 0, rank, T, W).to(dev)
+    qn = synth.engram_norm_weights(SEED, 0, 0, W).to(dev)
+    kn = synth.engram_norm_weights(SEED, 0, 1, W).to(dev)
+    resid = resid0.clone()
+    ws_e = torch.zeros(api.engram_inject_workspace(T, R, W), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    call = lambda i: api.engram_inject(table, ids[i % 8], w_kv, resid, qn, kn, dev_err=err, ws=ws_e)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    barrier(ws)
+    clocks.start()
+    ms = timed(call, args.steps, flush, stream)
+    clk = clocks.stop()
+    assert int(err) == 0
+    med = statistics.median(ms)
+    alg = N * K * 2 + T * R * (264 + 8) + T * 4 * W * 2 * 2 + 2 * 4 * W * 4
+    pk = peaks()
+    total = max_over_ranks(ws, sum(ms))
+    gbs = alg / (med * 1e-3) / 1e9
+    return {"metric": "Engram gate + residual injection, tokens/s (T=8 decode, 24 rows x 256, width 5120)",
+            "value": round(ws * T * args.steps / (total * 1e-3), 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "engram_inject: T=8, R=24 rows of a 4194304 x 264 B table, engram_kv.weight "
+                                   "[25600][6144] BF16, 4 branches x 5120",
+                       "algorithmic_bytes": alg, "l2": "flushed before every timed call"},
+            "roofline": {"bound": "hbm", "kernel": "engram_kv_kernel + engram_gate_kernel", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": pk["source"]},
+            "us_median": round(med * 1e3, 2), "clocks": clk}
+
+
 def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     T = args.T
@@ -711,7 +757,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--T", type=int, default=8)
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "verify", "engram", "route"],
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "verify", "engram", "route", "engram_gate"],
                     help="decode (default, the headline line) or one of the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-engram", action="store_true",
@@ -728,7 +775,7 @@ def main():
     ws, rank, local = dist_setup()
     if args.workload != "decode":
         res = {"prefill": run_prefill, "verify": run_verify, "engram": run_engram,
-               "route": run_route}[args.workload](args, ws, rank, local)
+               "route": run_route, "engram_gate": run_engram_gate}[args.workload](args, ws, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -21,6 +21,8 @@ SIGNATURES = {
     "bre_status_string": (C.c_char_p, [_I]),
     "moe_route_workspace": (_SZ, [_I, _I]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "engram_inject_workspace": (_SZ, [_I, _I, _I]),
+    "engram_inject": (_I, [_P, _I64, _P, _I, _P, _I, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),

@@ -191,6 +191,28 @@ def engram_gather_decode(tables, ids, dev_err=None, out=None, stream=None):
     return out
 
 
+def engram_inject_workspace(T: int, R: int, W: int) -> int:
+    return _lib.load().engram_inject_workspace(T, R, W)
+
+
+def engram_inject(table, row_ids, w_kv, resid, q_norm, k_norm, mask=None, eps: float = 1e-6, kv_out=None,
+                  gate_out=None, dev_err=None, ws=None, stream=None):
+    """Engram gate and residual injection for one layer: table uint8 [n_rows, 264]; row_ids int64
+    [T, R]; w_kv bf16 [5W, R*256]; resid bf16 [T, 4, W] (updated in place and returned); q_norm,
+    k_norm float32 [4, W]; mask uint8 [T] or None; kv_out float32 [T, 5W] / gate_out float32
+    [T, 4] optional outputs."""
+    L = _lib.load()
+    T, R = row_ids.shape
+    W = resid.shape[-1]
+    if ws is None:
+        ws = torch.zeros(L.engram_inject_workspace(T, R, W), dtype=torch.uint8, device=resid.device)
+    check(L.engram_inject(ptr(_dev(table, "table")), table.shape[0], ptr(_dev(row_ids, "row_ids")), R,
+                          ptr(_dev(w_kv, "w_kv")), W, ptr(_dev(resid, "resid")), ptr(q_norm), ptr(k_norm), ptr(mask), T,
+                          float(eps), ptr(kv_out), ptr(gate_out), ptr(dev_err), ptr(ws), ws.numel(),
+                          stream_handle(stream)), "engram_inject")
+    return resid
+
+
 def bre_dequant(fmt: int, blocks, stream=None):
     L = _lib.load()
     bb = 84 if fmt == BRE_FMT_Q2_K else 34

@@ -177,6 +177,28 @@ bre_status engram_gather_decode(const uint8_t* const* tables, const int64_t* n_r
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t engram_inject_workspace(int T, int R, int W) {
+  return (T > 0 && R > 0 && W > 0) ? engram_inject_ws_bytes(T, R, W) : 0;
+}
+
+bre_status engram_inject(const uint8_t* table, int64_t n_rows, const int64_t* row_ids, int R, const void* w_kv_bf16,
+                         int W, void* resid_bf16, const float* q_norm, const float* k_norm, const uint8_t* mask, int T,
+                         float eps, float* kv_out, float* gate_out, int32_t* dev_err, void* ws, size_t ws_bytes,
+                         bre_stream_t stream) {
+  if (!table || !row_ids || !w_kv_bf16 || !resid_bf16 || !q_norm || !k_norm || T <= 0 || R <= 0 || W <= 0 ||
+      n_rows <= 0 || !(eps >= 0.0f))
+    return BRE_ERR_ARG;
+  if (W % 16 != 0 || R > 28) return BRE_ERR_UNSUPPORTED;
+  if (!aligned(table, 8) || !aligned(row_ids, 8) || !aligned(w_kv_bf16, 16) || !aligned(resid_bf16, 2) ||
+      !aligned(q_norm, 4) || !aligned(k_norm, 4) || (kv_out && !aligned(kv_out, 4)) ||
+      (gate_out && !aligned(gate_out, 4)))
+    return BRE_ERR_ARG;
+  if (!ws || ws_bytes < engram_inject_ws_bytes(T, R, W) || !aligned(ws, 256)) return BRE_ERR_WORKSPACE;
+  return cuda_status(launch_engram_inject(table, n_rows, row_ids, R, static_cast<const uint16_t*>(w_kv_bf16), W,
+                                          static_cast<uint16_t*>(resid_bf16), q_norm, k_norm, mask, T, eps, kv_out,
+                                          gate_out, dev_err, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bre_status bre_dequant(int fmt, const void* blocks, int64_t n_blocks, float* out, bre_stream_t stream) {
   if (!blocks || !out || n_blocks <= 0) return BRE_ERR_ARG;
   if (fmt != BRE_FMT_Q2_K && fmt != BRE_FMT_Q8_0) return BRE_ERR_UNSUPPORTED;

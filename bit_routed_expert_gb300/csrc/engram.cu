@@ -2,6 +2,8 @@
 // row id, decoded to FP32, summed over heads in order and rounded to BF16.
 // (strix-llama.cpp issue, "Feature Description" and "DeepSeek V4.1 Engram graph
 // integration".)
+#include <mutex>
+
 #include "bre_common.cuh"
 #include "kernels.h"
 
@@ -105,6 +107,351 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
                                       n_tables, ids, T, H, out, err);
       if (le != cudaSuccess) return le;
     }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Engram gate and residual injection (strix-llama.cpp issue, "Placement"): the R gathered rows
+// of a token, concatenated ([R * 256] BF16), times engram_kv.weight [5W][R * 256] give four keys
+// and one shared value of width W; each of the four hyper-connection branches h then takes
+//   dot = sum_i r[h,i] qn[h,i] kn[h,i] key[h,i] / sqrt(mean r^2 + eps) / sqrt(mean key^2 + eps)
+//         / sqrt(W),
+//   gate = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot)),  r[h,i] = bf16(r[h,i] + gate bf16(v[i])).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int KV_WARPS = 8;
+constexpr int KV_NS = 3;                     // ring stages per warp
+constexpr int KV_STAGE = 4096;               // 16 rows x 128 K of W (two 64-K boxes, 128-byte swizzle)
+constexpr int KV_TOK = 8;                    // tokens per launch (MMA N)
+constexpr long long KV_WAIT = 2000000000LL;  // cycles before a wait gives up
+
+struct KvParams {
+  const uint8_t* table;
+  long long n_rows;
+  const int64_t* row_ids;  // [T][R]
+  int R, T, t0, tg;        // rows per token, tokens, this launch's first token and count (<= 8)
+  int K, N, KP;            // K = R * 256, N = 5W, K parts
+  float* part;             // [KP][T][N]
+  int* counter;
+  int32_t* err;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Persistent: each warp takes items (16 rows of W, one K part) from a counter and streams the
+// item's W through its own ring of 4 KB stages (TMA, 128-byte swizzle so that ldmatrix reads
+// are conflict-free); the launch's <= 8 tokens' rows are decoded into shared memory first (BF16,
+// row pitch K + 8 elements).  MMA m16n8k16: A = W rows, B = tokens.  Each item stores FP32
+// partial sums part[kp][t][n]; the gate kernel adds the parts in order.
+__global__ void __launch_bounds__(KV_WARPS * 32, 1) engram_kv_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                    const KvParams p) {
+  extern __shared__ __align__(1024) unsigned char kvs[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(kvs) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + KV_WARPS * KV_NS * KV_STAGE);
+  int* q_ids = reinterpret_cast<int*>(bars + KV_WARPS * KV_NS);       // [KV_WARPS][4] item ids in flight
+  uint16_t* xs = reinterpret_cast<uint16_t*>(q_ids + KV_WARPS * 4);   // [8][K + 8]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pitch = p.K + 8;
+  if (threadIdx.x < KV_WARPS * KV_NS) mbar_init(&bars[threadIdx.x], 1);
+  fence_mbar_init();
+  __syncthreads();
+  pdl_wait();
+  const int tiles = p.N / 16, kl = p.K / p.KP, spi = kl / 128;   // stages per item
+  const int n_items = tiles * p.KP;
+  unsigned char* my_ring = ring + warp * KV_NS * KV_STAGE;
+  uint64_t* my_bar = bars + warp * KV_NS;
+  int* my_q = q_ids + warp * 4;
+  // producer state (lane 0 issues): item being loaded, its stage, sequence number
+  int ld_item = 0, ld_c = 0, ld_seq = 0, q_tail = 0;
+  auto fetch = [&]() -> int {
+    int i = 0;
+    if (lane == 0) i = atomicAdd(p.counter, 1);
+    i = __shfl_sync(0xffffffffu, i, 0);
+    return i < n_items ? i : -1;
+  };
+  ld_item = fetch();
+  if (lane == 0) my_q[q_tail & 3] = ld_item;
+  ++q_tail;
+  auto issue_next = [&]() {
+    if (ld_item < 0) return;
+    if (lane == 0) {
+      const int slot = ld_seq % KV_NS;
+      unsigned char* dst = my_ring + slot * KV_STAGE;
+      const int tile = ld_item / p.KP, kp = ld_item - tile * p.KP;
+      const int k0 = kp * kl + ld_c * 128;
+      mbar_arrive_expect_tx(&my_bar[slot], KV_STAGE);
+      tma_load_2d(dst, &wmap, k0, tile * 16, &my_bar[slot]);
+      tma_load_2d(dst + 2048, &wmap, k0 + 64, tile * 16, &my_bar[slot]);
+    }
+    ++ld_seq;
+    if (++ld_c == spi) {
+      ld_c = 0;
+      ld_item = fetch();
+      if (lane == 0) my_q[q_tail & 3] = ld_item;
+      ++q_tail;
+    }
+  };
+  for (int i = 0; i < KV_NS - 1; ++i) issue_next();
+  // decode the launch's tokens' rows into shared memory (zeros past tg; bad ids decode as
+  // zeros); a thread's loads, eight slices at a time, are issued before their decodes
+  {
+    const int per_tok = p.R * 32;   // 8-value slices per token
+    const int total = KV_TOK * per_tok;
+    bool bad = false;
+    for (int q0 = 0; q0 < total; q0 += 8 * KV_WARPS * 32) {
+      uint2 v[8];
+      uint32_t sb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = q0 + u * KV_WARPS * 32 + threadIdx.x;
+        v[u] = make_uint2(0u, 0u);
+        sb[u] = 127u;
+        if (q < total) {
+          const int tt = q / per_tok, rem = q - tt * per_tok, j = rem >> 5, l = rem & 31;
+          if (tt < p.tg) {
+            const long long r = __ldg(p.row_ids + (size_t)(p.t0 + tt) * p.R + j);
+            const bool ok = r >= 0 && r < p.n_rows;
+            bad |= !ok;
+            if (ok) {
+              const uint8_t* row = p.table + r * ENGRAM_ROW;
+              v[u] = __ldg(reinterpret_cast<const uint2*>(row) + l);
+              sb[u] = __ldg(row + 256 + (l >> 2));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = q0 + u * KV_WARPS * 32 + threadIdx.x;
+        if (q < total) {
+          const int tt = q / per_tok, rem = q - tt * per_tok, j = rem >> 5, l = rem & 31;
+          float val[8];
+          decode8(v[u], sb[u], val);   // zeros for absent and bad rows
+          uint4 o;
+          o.x = f32_to_bf16_rne(val[0]) | (f32_to_bf16_rne(val[1]) << 16);
+          o.y = f32_to_bf16_rne(val[2]) | (f32_to_bf16_rne(val[3]) << 16);
+          o.z = f32_to_bf16_rne(val[4]) | (f32_to_bf16_rne(val[5]) << 16);
+          o.w = f32_to_bf16_rne(val[6]) | (f32_to_bf16_rne(val[7]) << 16);
+          *reinterpret_cast<uint4*>(xs + (size_t)tt * pitch + j * 256 + l * 8) = o;
+        }
+      }
+    }
+    if (bad) set_err(p.err, BRE_DEVERR_ROW_ID);
+  }
+  __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
+  // ldmatrix lane addresses: A (rows (lane & 7) + 8 ((lane >> 3) & 1), 16-byte chunk + (lane >> 4));
+  // B (token lane & 7, chunk + ((lane >> 3) & 1))
+  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, achk = lane >> 4;
+  const uint32_t xs_lane = smem_u32(xs) + (uint32_t)((lane & 7) * pitch * 2 + ((lane >> 3) & 1) * 16);
+  int cs = 0, q_head = 0;
+  while (true) {
+    __syncwarp();   // lane 0's queue write comes first for every lane
+    const int item = my_q[q_head & 3];
+    if (item < 0) break;
+    const int tile = item / p.KP, kp = item - tile * p.KP;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int c = 0; c < spi; ++c) {
+      const int slot = cs % KV_NS;
+      if (!mbar_wait_bounded(&my_bar[slot], (cs / KV_NS) & 1, KV_WAIT)) {
+        if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
+        for (int q = cs + 1; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % KV_NS], (q / KV_NS) & 1, KV_WAIT);
+        return;
+      }
+      const uint32_t st = smem_u32(my_ring + slot * KV_STAGE);
+      const int kg0 = kp * kl + c * 128;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int box = kk >> 2, chunk = (kk & 3) * 2 + achk;
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldsm_x4(st + box * 2048 + arow * 128 + ((chunk ^ (arow & 7)) << 4), a0, a1, a2, a3);
+        ldsm_x2(xs_lane + (uint32_t)(kg0 + kk * 16) * 2, b0, b1);
+        mma_bf16_16816(acc, a0, a1, a2, a3, b0, b1);
+      }
+      fence_proxy_async_smem();   // the stage's reads come before the copy that refills it
+      __syncwarp();
+      ++cs;
+      issue_next();
+    }
+    ++q_head;
+    // C fragment: rows tile*16 + g (+8), tokens 2t, 2t+1
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int tt = 2 * t + (i & 1), n = tile * 16 + g + 8 * (i >> 1);
+      if (tt < p.tg) p.part[((size_t)kp * p.T + p.t0 + tt) * p.N + n] = acc[i];
+    }
+  }
+}
+
+// One CTA per (token, branch).  Sums in a fixed order (thread-strided FMA chains, then the warp
+// butterfly and the warps in order), so the result does not depend on scheduling.
+constexpr int GATE_THREADS = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = red[0];
+  for (int w = 1; w < GATE_THREADS / 32; ++w) s = __fadd_rn(s, red[w]);
+  return s;
+}
+
+__global__ void __launch_bounds__(GATE_THREADS) engram_gate_kernel(const float* __restrict__ part, int KP, int T,
+                                                                   int W, uint16_t* __restrict__ resid,
+                                                                   const float* __restrict__ qn,
+                                                                   const float* __restrict__ kn,
+                                                                   const uint8_t* __restrict__ mask, float eps,
+                                                                   float* __restrict__ kv_out,
+                                                                   float* __restrict__ gate_out, int* counter) {
+  __shared__ float red[GATE_THREADS / 32];
+  pdl_wait();
+  const int t = blockIdx.x, h = blockIdx.y;
+  if (t == 0 && h == 0 && threadIdx.x == 0) *counter = 0;   // ready for the next projection
+  const size_t N = (size_t)5 * W;
+  auto kv_at = [&](size_t n) {
+    float v = __ldcg(part + (size_t)t * N + n);
+    for (int q = 1; q < KP; ++q) v = __fadd_rn(v, __ldcg(part + ((size_t)q * T + t) * N + n));
+    return v;
+  };
+  if (kv_out) {
+    for (int i = threadIdx.x; i < W; i += GATE_THREADS) kv_out[(size_t)t * N + (size_t)h * W + i] = kv_at((size_t)h * W + i);
+    if (h == 0)
+      for (int i = threadIdx.x; i < W; i += GATE_THREADS) kv_out[(size_t)t * N + (size_t)4 * W + i] = kv_at((size_t)4 * W + i);
+  }
+  if (mask && mask[t]) {
+    if (gate_out && threadIdx.x == 0) gate_out[t * 4 + h] = 0.0f;
+    return;
+  }
+  uint16_t* r = resid + ((size_t)t * 4 + h) * W;
+  float dot = 0.0f, rr = 0.0f, kk = 0.0f;
+  for (int i = threadIdx.x; i < W; i += GATE_THREADS) {
+    const float ri = bf16_bits_to_f32(r[i]);
+    const float key = kv_at((size_t)h * W + i);
+    const float pr = __fmul_rn(__fmul_rn(ri, __ldg(qn + (size_t)h * W + i)), __ldg(kn + (size_t)h * W + i));
+    dot = __fmaf_rn(pr, key, dot);
+    rr = __fmaf_rn(ri, ri, rr);
+    kk = __fmaf_rn(key, key, kk);
+  }
+  dot = block_sum(dot, red);
+  rr = block_sum(rr, red);
+  kk = block_sum(kk, red);
+  const float inv_w = 1.0f / (float)W;
+  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(rr, inv_w), eps)));
+  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(kk, inv_w), eps)));
+  dot = __fmul_rn(dot, 1.0f / sqrtf((float)W));
+  const float m = sqrtf(fmaxf(fabsf(dot), 1e-6f));
+  const float gate = 1.0f / (1.0f + expf(-copysignf(m, dot)));
+  if (gate_out && threadIdx.x == 0) gate_out[t * 4 + h] = gate;
+  __syncthreads();   // every read of r precedes its update
+  for (int i = threadIdx.x; i < W; i += GATE_THREADS) {
+    const float vb = bf16_bits_to_f32(f32_to_bf16_rne(kv_at((size_t)4 * W + i)));
+    r[i] = (uint16_t)f32_to_bf16_rne(__fmaf_rn(gate, vb, bf16_bits_to_f32(r[i])));
+  }
+}
+
+// K parts: the largest of 4, 2, 1 that leaves whole 128-element stages.
+int kv_parts(int K) {
+  for (int kp = 4; kp >= 1; kp >>= 1)
+    if (K % (128 * kp) == 0) return kp;
+  return 0;
+}
+
+}  // namespace
+
+size_t engram_inject_ws_bytes(int T, int R, int W) {
+  const int K = R * 256, KP = kv_parts(K);
+  if (KP == 0) return 0;
+  return 256 + (((size_t)KP * T * 5 * W * 4 + 255) & ~(size_t)255);
+}
+
+cudaError_t launch_engram_inject(const uint8_t* table, long long n_rows, const int64_t* row_ids, int R,
+                                 const uint16_t* w_kv, int W, uint16_t* resid, const float* q_norm,
+                                 const float* k_norm, const uint8_t* mask, int T, float eps, float* kv_out,
+                                 float* gate_out, int32_t* err, void* ws, cudaStream_t s) {
+  const int K = R * 256, N = 5 * W, KP = kv_parts(K);
+  if (KP == 0 || N % 16 != 0) return cudaErrorInvalidValue;
+  int* counter = reinterpret_cast<int*>(ws);
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
+  // W_kv as [N][K] BF16, box 64 K x 16 rows, 128-byte swizzle
+  struct Entry {
+    const void* w;
+    int K, N;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[8];
+  static int n_cached = 0, next = 0;
+  CUtensorMap map;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    bool found = false;
+    for (int i = 0; i < n_cached && !found; ++i)
+      if (cache[i].w == w_kv && cache[i].K == K && cache[i].N == N) {
+        map = cache[i].map;
+        found = true;
+      }
+    if (!found) {
+      const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+      const uint64_t strides[1] = {(uint64_t)K * 2};
+      const uint32_t box[2] = {64u, 16u};
+      if (!encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_kv, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+      cache[next] = Entry{w_kv, K, N, map};
+      next = (next + 1) % 8;
+      if (n_cached < 8) ++n_cached;
+    }
+  }
+  const size_t smem = 1024 + (size_t)KV_WARPS * KV_NS * KV_STAGE + (size_t)KV_WARPS * KV_NS * 8 + KV_WARPS * 16 +
+                      (size_t)KV_TOK * (K + 8) * 2;
+  if (smem > (size_t)device_max_smem_optin()) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(engram_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  for (int t0 = 0; t0 < T; t0 += KV_TOK) {
+    KvParams p;
+    p.table = table;
+    p.n_rows = n_rows;
+    p.row_ids = row_ids;
+    p.R = R;
+    p.T = T;
+    p.t0 = t0;
+    p.tg = T - t0 < KV_TOK ? T - t0 : KV_TOK;
+    p.K = K;
+    p.N = N;
+    p.KP = KP;
+    p.part = part;
+    p.counter = counter;
+    p.err = err;
+    if (t0 > 0) {
+      // each launch hands its items out from zero again
+      const cudaError_t me = cudaMemsetAsync(counter, 0, sizeof(int), s);
+      if (me != cudaSuccess) return me;
+    }
+    const cudaError_t le = launch_k(engram_kv_kernel, dim3(sms), dim3(KV_WARPS * 32), smem, s, map, p);
+    if (le != cudaSuccess) return le;
+  }
+  const cudaError_t le = launch_k(engram_gate_kernel, dim3(T, 4), dim3(GATE_THREADS), 0, s, (const float*)part, KP, T,
+                                  W, resid, q_norm, k_norm, mask, eps, kv_out, gate_out, counter);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

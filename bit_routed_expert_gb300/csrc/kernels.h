@@ -15,6 +15,11 @@ struct EngramTables {
 
 cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t* ids, int T, int H, uint16_t* out,
                           int32_t* err, cudaStream_t s);
+size_t engram_inject_ws_bytes(int T, int R, int W);
+cudaError_t launch_engram_inject(const uint8_t* table, long long n_rows, const int64_t* row_ids, int R,
+                                 const uint16_t* w_kv, int W, uint16_t* resid, const float* q_norm,
+                                 const float* k_norm, const uint8_t* mask, int T, float eps, float* kv_out,
+                                 float* gate_out, int32_t* err, void* ws, cudaStream_t s);
 
 // router
 size_t route_ws_bytes(int T, int E);

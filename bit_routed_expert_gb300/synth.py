@@ -53,6 +53,7 @@ ENGRAM_WORDS = 66   # 264 16-bit lanes
 # stream ids (tensor kinds); layer and set numbers are folded in by stream()
 S_X, S_WR, S_BIAS, S_GATE, S_UP, S_DOWN, S_SGATE, S_SUP, S_SDOWN = range(1, 10)
 S_ENGRAM_TABLE, S_ENGRAM_IDS, S_TOKENS, S_ZIPF_PERM = 16, 24, 25, 26
+S_EKV, S_ENORM, S_ERESID = 27, 28, 29
 
 
 def stream(kind: int, layer: int = 0, sub: int = 0) -> int:
@@ -202,6 +203,23 @@ def normal(seed: int, s: int, n: int, std: float = 1.0, start: int = 0) -> torch
 def x_bf16(seed: int, layer: int, tset: int, T: int, d: int) -> torch.Tensor:
     """Activations x ~ N(0, 1) rounded to BF16 (RNE), [T, d]."""
     return normal(seed, stream(S_X, layer, tset), T * d).to(torch.float32).to(torch.bfloat16).view(T, d)
+
+
+def engram_kv_weight(seed: int, layer: int, N: int, K: int, std: float = 1e-5, device="cpu") -> torch.Tensor:
+    """engram_kv.weight ~ N(0, std^2) rounded to BF16, [N = 5 W outputs][K = R * 256 inputs].  The
+    decoded Engram rows reach magnitudes of ~1e4 (e4m3 up to 448 times scales up to 2^7), so a
+    small std keeps the keys and the value near unit size."""
+    return normal(seed, stream(S_EKV, layer), N * K, std).to(torch.float32).to(torch.bfloat16).view(N, K).to(device)
+
+
+def engram_norm_weights(seed: int, layer: int, which: int, W: int) -> torch.Tensor:
+    """q_norm (which = 0) / k_norm (1) of the four hyper-connection branches: 1 + N(0, 0.1^2), FP32 [4, W]."""
+    return (1.0 + normal(seed, stream(S_ENORM, layer, which), 4 * W, 0.1)).to(torch.float32).view(4, W)
+
+
+def engram_residual(seed: int, layer: int, tset: int, T: int, W: int) -> torch.Tensor:
+    """The four hyper-connection residual branches ~ N(0, 1) rounded to BF16, [T, 4, W]."""
+    return normal(seed, stream(S_ERESID, layer, tset), T * 4 * W).to(torch.float32).to(torch.bfloat16).view(T, 4, W)
 
 
 def router_weight(seed: int, layer: int, d: int, E: int) -> torch.Tensor:

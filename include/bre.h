@@ -230,6 +230,29 @@ bre_status engram_gather_decode(const uint8_t *const *tables, const int64_t *n_r
                                 const int64_t *row_ids, int T, int H, void *out_bf16, int32_t *dev_err,
                                 bre_stream_t stream);
 
+/* Engram gate and residual injection (strix-llama.cpp issue, "Placement"), for one Engram layer:
+ *   rows: the R table rows of token t (row_ids [T][R] int64, device) decoded as
+ *     engram_gather_decode does (e4m3 x 2^(e8m0 - 127), BF16) and concatenated -> x_t [R * 256];
+ *   kv_t = engram_kv.weight . x_t, FP32 accumulation; w_kv_bf16 [5W][R * 256] BF16 (rows are the
+ *     outputs); kv_t = four keys [4][W] then one shared value [W];
+ *   for each hyper-connection branch h < 4 of resid_bf16 [T][4][W] (BF16, updated in place):
+ *     dot = sum_i r[h,i] q_norm[h,i] k_norm[h,i] key[h,i]
+ *           * 1/sqrt(mean(r[h,:]^2) + eps) * 1/sqrt(mean(key[h,:]^2) + eps) * 1/sqrt(W)
+ *     gate = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot))
+ *     r[h,i] = bf16(r[h,i] + gate * bf16(value[i]))        (FP32 arithmetic, one rounding each)
+ *   mask [T] uint8 or NULL: tokens with mask[t] != 0 keep their residual byte for byte.
+ *   q_norm, k_norm [4][W] FP32.  kv_out [T][5W] FP32 and gate_out [T][4] FP32 are optional
+ *   (NULL: not written; masked tokens get gate 0).  A row id outside [0, n_rows) decodes as
+ *   zeros and sets BRE_DEVERR_ROW_ID in dev_err (may be NULL).
+ *   ws: engram_inject_workspace(T, R, W) bytes, zero-filled once after allocation (each call
+ *   leaves its counter at zero).  Requires W % 16 == 0 and R <= 28 (the tokens' rows are held
+ *   in shared memory; batches of 8 tokens run one after the other, each reading w_kv once). */
+size_t engram_inject_workspace(int T, int R, int W);
+bre_status engram_inject(const uint8_t *table, int64_t n_rows, const int64_t *row_ids, int R, const void *w_kv_bf16,
+                         int W, void *resid_bf16, const float *q_norm, const float *k_norm, const uint8_t *mask, int T,
+                         float eps, float *kv_out, float *gate_out, int32_t *dev_err, void *ws, size_t ws_bytes,
+                         bre_stream_t stream);
+
 /* Dequantise n_blocks blocks of format fmt to FP32 on the device, with the
  * same decode the FFN kernels use (exact: every product is exact in FP32 and
  * the one rounding is the final subtraction).  out [n_blocks * 256 or * 32]. */

@@ -487,3 +487,89 @@ def test_verify_stack_24_layers_teacher_forced(cuda_dev):
         # the residual update is bit-exact given the layer output
         nxt = trace[l + 1][0] if l + 1 < L else xf
         assert np.array_equal(bf16_bits(nxt), oracle.residual(x_l.cpu(), out_l.cpu(), stack.scale))
+
+
+# --------------------------------------------------------------------------- #
+# Engram gate and residual injection
+# --------------------------------------------------------------------------- #
+
+def _bf16_ulp(a):
+    """Spacing of BF16 at |a| (2^(e-7) for normal values)."""
+    a = np.abs(np.asarray(a, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+@pytest.mark.parametrize("T,R,W", [(1, 24, 5120), (8, 24, 5120), (5, 2, 256), (11, 3, 512), (20, 1, 128)])
+def test_engram_inject_parity(cuda_dev, T, R, W):
+    """engram_inject against the FP64 oracle: kv within the FP32 dot-product bound, gates within
+    1e-4, every updated BF16 value within one BF16 step of the result plus one step of the value
+    times the gate (the two roundings either side may take), masked tokens byte for byte."""
+    nrows = 4096
+    table = synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 5), nrows)
+    ids = synth.engram_ids_uniform(SEED + T, T * R, nrows).view(T, R)
+    K, N = 256 * R, 5 * W
+    w_kv = synth.engram_kv_weight(SEED, R, N, K)
+    resid = synth.engram_residual(SEED, 0, T, T, W)
+    qn = synth.engram_norm_weights(SEED, 0, 0, W)
+    kn = synth.engram_norm_weights(SEED, 0, 1, W)
+    mask = (np.arange(T) % 3 == 2).astype(np.uint8)
+    rows_bits, err_ref = oracle.engram_gather([table] * R, ids.numpy().reshape(T, R, 1))
+    rows = torch.from_numpy(rows_bits.view(np.int16)).view(torch.bfloat16)
+    kv_ref = oracle.engram_kv(rows, w_kv)
+    out_ref, g_ref = oracle.engram_gate(kv_ref, resid, qn, kn, mask=mask)
+    dv = cuda_dev
+    r_gpu = resid.to(dv).clone()
+    kv = torch.empty((T, N), dtype=torch.float32, device=dv)
+    g = torch.empty((T, 4), dtype=torch.float32, device=dv)
+    err = torch.zeros(1, dtype=torch.int32, device=dv)
+    api.engram_inject(table.to(dv), ids.to(dv), w_kv.to(dv), r_gpu, qn.to(dv), kn.to(dv),
+                      mask=torch.from_numpy(mask).to(dv), kv_out=kv, gate_out=g, dev_err=err)
+    assert int(err) == err_ref == 0
+    # kv: FP32 accumulation of K exact products (tensor-core sums, then K parts in order)
+    mag = np.abs(rows.double().numpy()) @ np.abs(w_kv.double().numpy()).T
+    bound = (K + 8) * 2.0 ** -23 * mag
+    assert np.all(np.abs(kv.cpu().double().numpy() - kv_ref) <= bound)
+    gg = g.cpu().double().numpy()
+    assert np.all(gg[mask == 1] == 0)
+    assert np.max(np.abs(gg - g_ref)[mask == 0]) <= 1e-4
+    got = r_gpu.cpu()
+    rb = resid.view(torch.int16).numpy().view(np.uint16)
+    gb = got.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(gb[mask == 1], rb[mask == 1])
+    ref_f = torch.from_numpy(out_ref.view(np.int16)).view(torch.bfloat16).double().numpy()
+    got_f = got.double().numpy()
+    v_ref = kv_ref[:, 4 * W:][:, None, :]
+    tol = _bf16_ulp(ref_f) + g_ref[:, :, None] * _bf16_ulp(v_ref) + 1e-4 * np.abs(v_ref)
+    assert np.all(np.abs(got_f - ref_f)[mask == 0] <= tol[mask == 0])
+
+
+def test_engram_inject_bad_rows_and_repeat(cuda_dev):
+    """Row ids outside the table decode as zeros and set BRE_DEVERR_ROW_ID (as the oracle's
+    gather); a second call on the same workspace gives the same bits."""
+    T, R, W, nrows = 4, 2, 256, 512
+    table = synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 6), nrows)
+    ids = synth.engram_ids_uniform(SEED, T * R, nrows).view(T, R).clone()
+    ids[1, 0] = nrows
+    ids[2, 1] = -5
+    w_kv = synth.engram_kv_weight(SEED, 9, 5 * W, 256 * R)
+    resid = synth.engram_residual(SEED, 1, 0, T, W)
+    qn = synth.engram_norm_weights(SEED, 1, 0, W)
+    kn = synth.engram_norm_weights(SEED, 1, 1, W)
+    rows_bits, err_ref = oracle.engram_gather([table] * R, ids.numpy().reshape(T, R, 1))
+    assert err_ref == 2
+    kv_ref = oracle.engram_kv(torch.from_numpy(rows_bits.view(np.int16)).view(torch.bfloat16), w_kv)
+    _, g_ref = oracle.engram_gate(kv_ref, resid, qn, kn)
+    dv = cuda_dev
+    ws = torch.zeros(api.engram_inject_workspace(T, R, W), dtype=torch.uint8, device=dv)
+    outs = []
+    for _ in range(2):
+        r_gpu = resid.to(dv).clone()
+        g = torch.empty((T, 4), dtype=torch.float32, device=dv)
+        err = torch.zeros(1, dtype=torch.int32, device=dv)
+        api.engram_inject(table.to(dv), ids.to(dv), w_kv.to(dv), r_gpu, qn.to(dv), kn.to(dv), gate_out=g,
+                          dev_err=err, ws=ws)
+        assert int(err) == 2
+        assert np.max(np.abs(g.cpu().double().numpy() - g_ref)) <= 1e-4
+        outs.append(r_gpu.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
