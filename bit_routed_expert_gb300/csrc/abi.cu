@@ -188,7 +188,7 @@ bre_status engram_inject(const uint8_t* table, int64_t n_rows, const int64_t* ro
   if (!table || !row_ids || !w_kv_bf16 || !resid_bf16 || !q_norm || !k_norm || T <= 0 || R <= 0 || W <= 0 ||
       n_rows <= 0 || !(eps >= 0.0f))
     return BRE_ERR_ARG;
-  if (W % 16 != 0 || R > 28) return BRE_ERR_UNSUPPORTED;
+  if (W % 16 != 0 || W > 8192 || R > 24) return BRE_ERR_UNSUPPORTED;
   if (!aligned(table, 8) || !aligned(row_ids, 8) || !aligned(w_kv_bf16, 16) || !aligned(resid_bf16, 2) ||
       !aligned(q_norm, 4) || !aligned(k_norm, 4) || (kv_out && !aligned(kv_out, 4)) ||
       (gate_out && !aligned(gate_out, 4)))

@@ -121,8 +121,9 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
 namespace {
 
 constexpr int KV_WARPS = 8;
-constexpr int KV_NS = 3;                     // ring stages per warp
-constexpr int KV_STAGE = 4096;               // 16 rows x 128 K of W (two 64-K boxes, 128-byte swizzle)
+constexpr int KV_NS = 4;                     // ring stages per warp (three copies in flight)
+constexpr int KV_KS = 128;                   // K per stage (4 warps with 256-K stages measured slower)
+constexpr int KV_STAGE = 16 * KV_KS * 2;     // 16 rows x 128 K of W (two 64-K boxes, 128-byte swizzle)
 constexpr int KV_TOK = 8;                    // tokens per launch (MMA N)
 constexpr long long KV_WAIT = 2000000000LL;  // cycles before a wait gives up
 
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(KV_WARPS * 32, 1) engram_kv_kernel(const __gri
   fence_mbar_init();
   __syncthreads();
   pdl_wait();
-  const int tiles = p.N / 16, kl = p.K / p.KP, spi = kl / 128;   // stages per item
+  const int tiles = p.N / 16, kl = p.K / p.KP, spi = kl / KV_KS;   // stages per item
   const int n_items = tiles * p.KP;
   unsigned char* my_ring = ring + warp * KV_NS * KV_STAGE;
   uint64_t* my_bar = bars + warp * KV_NS;
@@ -193,10 +194,10 @@ __global__ void __launch_bounds__(KV_WARPS * 32, 1) engram_kv_kernel(const __gri
       const int slot = ld_seq % KV_NS;
       unsigned char* dst = my_ring + slot * KV_STAGE;
       const int tile = ld_item / p.KP, kp = ld_item - tile * p.KP;
-      const int k0 = kp * kl + ld_c * 128;
+      const int k0 = kp * kl + ld_c * KV_KS;
       mbar_arrive_expect_tx(&my_bar[slot], KV_STAGE);
-      tma_load_2d(dst, &wmap, k0, tile * 16, &my_bar[slot]);
-      tma_load_2d(dst + 2048, &wmap, k0 + 64, tile * 16, &my_bar[slot]);
+#pragma unroll
+      for (int bx = 0; bx < KV_KS / 64; ++bx) tma_load_2d(dst + bx * 2048, &wmap, k0 + bx * 64, tile * 16, &my_bar[slot]);
     }
     ++ld_seq;
     if (++ld_c == spi) {
@@ -274,9 +275,9 @@ __global__ void __launch_bounds__(KV_WARPS * 32, 1) engram_kv_kernel(const __gri
         return;
       }
       const uint32_t st = smem_u32(my_ring + slot * KV_STAGE);
-      const int kg0 = kp * kl + c * 128;
+      const int kg0 = kp * kl + c * KV_KS;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < KV_KS / 16; ++kk) {
         const int box = kk >> 2, chunk = (kk & 3) * 2 + achk;
         uint32_t a0, a1, a2, a3, b0, b1;
         ldsm_x4(st + box * 2048 + arow * 128 + ((chunk ^ (arow & 7)) << 4), a0, a1, a2, a3);
@@ -298,8 +299,12 @@ __global__ void __launch_bounds__(KV_WARPS * 32, 1) engram_kv_kernel(const __gri
   }
 }
 
-// One CTA per (token, branch).  Sums in a fixed order (thread-strided FMA chains, then the warp
-// butterfly and the warps in order), so the result does not depend on scheduling.
+// The gate in two fully parallel launches.  engram_reduce_kernel: one CTA per (token, 256-element
+// slice of a key or of the value): adds the K parts in part order (kv), and for key slices
+// forms the slice's three sums (r q_norm k_norm key, r^2, key^2) in a fixed order (thread FMA,
+// warp butterfly, warps in order).  engram_apply_kernel: one CTA per (token, branch, slice):
+// adds the branch's slice sums in slice order -- every CTA of a branch gets the same gate -- and
+// updates its slice.  Deterministic, with no atomics.
 constexpr int GATE_THREADS = 256;
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -314,72 +319,104 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-__global__ void __launch_bounds__(GATE_THREADS) engram_gate_kernel(const float* __restrict__ part, int KP, int T,
-                                                                   int W, uint16_t* __restrict__ resid,
-                                                                   const float* __restrict__ qn,
-                                                                   const float* __restrict__ kn,
-                                                                   const uint8_t* __restrict__ mask, float eps,
-                                                                   float* __restrict__ kv_out,
-                                                                   float* __restrict__ gate_out, int* counter) {
+struct GateParams {
+  const float* part;   // [KP][T][5W]
+  int KP, T, W, NSL;   // NSL = slices of 256 per branch
+  float* kv;           // [T][5W] (workspace, or the caller's kv_out)
+  float* sums;         // [T][4][NSL][3]
+  uint16_t* resid;
+  const float* qn;
+  const float* kn;
+  const uint8_t* mask;
+  float eps;
+  float* gate_out;
+  int* counter;
+};
+
+__global__ void __launch_bounds__(GATE_THREADS) engram_reduce_kernel(const GateParams g) {
   __shared__ float red[GATE_THREADS / 32];
   pdl_wait();
-  const int t = blockIdx.x, h = blockIdx.y;
-  if (t == 0 && h == 0 && threadIdx.x == 0) *counter = 0;   // ready for the next projection
-  const size_t N = (size_t)5 * W;
-  auto kv_at = [&](size_t n) {
-    float v = __ldcg(part + (size_t)t * N + n);
-    for (int q = 1; q < KP; ++q) v = __fadd_rn(v, __ldcg(part + ((size_t)q * T + t) * N + n));
-    return v;
-  };
-  if (kv_out) {
-    for (int i = threadIdx.x; i < W; i += GATE_THREADS) kv_out[(size_t)t * N + (size_t)h * W + i] = kv_at((size_t)h * W + i);
-    if (h == 0)
-      for (int i = threadIdx.x; i < W; i += GATE_THREADS) kv_out[(size_t)t * N + (size_t)4 * W + i] = kv_at((size_t)4 * W + i);
+  const int t = blockIdx.x, b = blockIdx.y / g.NSL, sl = blockIdx.y % g.NSL;   // b = 0..3 keys, 4 value
+  if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) *g.counter = 0;   // ready for the next projection
+  const int i = sl * 256 + threadIdx.x;
+  const size_t N = (size_t)5 * g.W, n = (size_t)b * g.W + i;
+  float v = 0.0f;
+  if (i < g.W) {
+    float pv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) pv[q] = q < g.KP ? __ldcg(g.part + ((size_t)q * g.T + t) * N + n) : 0.0f;
+    v = pv[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q)
+      if (q < g.KP) v = __fadd_rn(v, pv[q]);
+    g.kv[(size_t)t * N + n] = v;
   }
-  if (mask && mask[t]) {
-    if (gate_out && threadIdx.x == 0) gate_out[t * 4 + h] = 0.0f;
-    return;
-  }
-  uint16_t* r = resid + ((size_t)t * 4 + h) * W;
+  if (b == 4) return;   // value slices: the sum only
   float dot = 0.0f, rr = 0.0f, kk = 0.0f;
-  for (int i = threadIdx.x; i < W; i += GATE_THREADS) {
-    const float ri = bf16_bits_to_f32(r[i]);
-    const float key = kv_at((size_t)h * W + i);
-    const float pr = __fmul_rn(__fmul_rn(ri, __ldg(qn + (size_t)h * W + i)), __ldg(kn + (size_t)h * W + i));
-    dot = __fmaf_rn(pr, key, dot);
-    rr = __fmaf_rn(ri, ri, rr);
-    kk = __fmaf_rn(key, key, kk);
+  if (i < g.W) {
+    const float ri = bf16_bits_to_f32(g.resid[((size_t)t * 4 + b) * g.W + i]);
+    const float qk = __fmul_rn(__ldg(g.qn + (size_t)b * g.W + i), __ldg(g.kn + (size_t)b * g.W + i));
+    dot = __fmul_rn(__fmul_rn(ri, qk), v);
+    rr = __fmul_rn(ri, ri);
+    kk = __fmul_rn(v, v);
   }
   dot = block_sum(dot, red);
   rr = block_sum(rr, red);
   kk = block_sum(kk, red);
-  const float inv_w = 1.0f / (float)W;
-  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(rr, inv_w), eps)));
-  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(kk, inv_w), eps)));
-  dot = __fmul_rn(dot, 1.0f / sqrtf((float)W));
-  const float m = sqrtf(fmaxf(fabsf(dot), 1e-6f));
-  const float gate = 1.0f / (1.0f + expf(-copysignf(m, dot)));
-  if (gate_out && threadIdx.x == 0) gate_out[t * 4 + h] = gate;
-  __syncthreads();   // every read of r precedes its update
-  for (int i = threadIdx.x; i < W; i += GATE_THREADS) {
-    const float vb = bf16_bits_to_f32(f32_to_bf16_rne(kv_at((size_t)4 * W + i)));
-    r[i] = (uint16_t)f32_to_bf16_rne(__fmaf_rn(gate, vb, bf16_bits_to_f32(r[i])));
+  if (threadIdx.x == 0) {
+    float* s = g.sums + (((size_t)t * 4 + b) * g.NSL + sl) * 3;
+    s[0] = dot;
+    s[1] = rr;
+    s[2] = kk;
   }
 }
 
-// K parts: the largest of 4, 2, 1 that leaves whole 128-element stages.
+__global__ void __launch_bounds__(GATE_THREADS) engram_apply_kernel(const GateParams g) {
+  pdl_wait();
+  const int t = blockIdx.x, h = blockIdx.y / g.NSL, sl = blockIdx.y % g.NSL;
+  if (g.mask && g.mask[t]) {
+    if (g.gate_out && sl == 0 && threadIdx.x == 0) g.gate_out[t * 4 + h] = 0.0f;
+    return;
+  }
+  const float* s = g.sums + ((size_t)t * 4 + h) * g.NSL * 3;
+  float dot = s[0], rr = s[1], kk = s[2];
+  for (int q = 1; q < g.NSL; ++q) {
+    dot = __fadd_rn(dot, s[q * 3 + 0]);
+    rr = __fadd_rn(rr, s[q * 3 + 1]);
+    kk = __fadd_rn(kk, s[q * 3 + 2]);
+  }
+  const float inv_w = 1.0f / (float)g.W;
+  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(rr, inv_w), g.eps)));
+  dot = __fmul_rn(dot, 1.0f / sqrtf(__fadd_rn(__fmul_rn(kk, inv_w), g.eps)));
+  dot = __fmul_rn(dot, 1.0f / sqrtf((float)g.W));
+  const float m = sqrtf(fmaxf(fabsf(dot), 1e-6f));
+  const float gate = 1.0f / (1.0f + expf(-copysignf(m, dot)));
+  if (g.gate_out && sl == 0 && threadIdx.x == 0) g.gate_out[t * 4 + h] = gate;
+  const int i = sl * 256 + threadIdx.x;
+  if (i < g.W) {
+    uint16_t* r = g.resid + ((size_t)t * 4 + h) * g.W + i;
+    const float vb = bf16_bits_to_f32(f32_to_bf16_rne(__ldcg(g.kv + (size_t)t * 5 * g.W + (size_t)4 * g.W + i)));
+    *r = (uint16_t)f32_to_bf16_rne(__fmaf_rn(gate, vb, bf16_bits_to_f32(*r)));
+  }
+}
+
+// K parts: the largest of 8, 4, 2, 1 that leaves whole stages (at R = 24, 12,800 items of
+// 24 KB: ~10 per warp, so the last wave is short); K must be a multiple of KV_KS.
 int kv_parts(int K) {
-  for (int kp = 4; kp >= 1; kp >>= 1)
-    if (K % (128 * kp) == 0) return kp;
+  for (int kp = 8; kp >= 1; kp >>= 1)
+    if (K % (KV_KS * kp) == 0) return kp;
   return 0;
 }
 
 }  // namespace
 
+// workspace: counter | K-part sums [KP][T][5W] | kv [T][5W] | slice sums [T][4][NSL][3]
 size_t engram_inject_ws_bytes(int T, int R, int W) {
   const int K = R * 256, KP = kv_parts(K);
   if (KP == 0) return 0;
-  return 256 + (((size_t)KP * T * 5 * W * 4 + 255) & ~(size_t)255);
+  const size_t nsl = (size_t)(W + 255) / 256;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  return 256 + up((size_t)KP * T * 5 * W * 4) + up((size_t)T * 5 * W * 4) + up((size_t)T * 4 * nsl * 3 * 4);
 }
 
 cudaError_t launch_engram_inject(const uint8_t* table, long long n_rows, const int64_t* row_ids, int R,
@@ -449,9 +486,30 @@ cudaError_t launch_engram_inject(const uint8_t* table, long long n_rows, const i
     const cudaError_t le = launch_k(engram_kv_kernel, dim3(sms), dim3(KV_WARPS * 32), smem, s, map, p);
     if (le != cudaSuccess) return le;
   }
-  const cudaError_t le = launch_k(engram_gate_kernel, dim3(T, 4), dim3(GATE_THREADS), 0, s, (const float*)part, KP, T,
-                                  W, resid, q_norm, k_norm, mask, eps, kv_out, gate_out, counter);
-  if (le != cudaSuccess) return le;
+  GateParams gp;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  gp.part = part;
+  gp.KP = KP;
+  gp.T = T;
+  gp.W = W;
+  gp.NSL = (W + 255) / 256;
+  gp.kv = kv_out ? kv_out : reinterpret_cast<float*>(reinterpret_cast<char*>(part) + up((size_t)KP * T * N * 4));
+  gp.sums = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + up((size_t)KP * T * N * 4) + up((size_t)T * N * 4));
+  gp.resid = resid;
+  gp.qn = q_norm;
+  gp.kn = k_norm;
+  gp.mask = mask;
+  gp.eps = eps;
+  gp.gate_out = gate_out;
+  gp.counter = counter;
+  {
+    const cudaError_t le = launch_k(engram_reduce_kernel, dim3(T, 5 * gp.NSL), dim3(GATE_THREADS), 0, s, gp);
+    if (le != cudaSuccess) return le;
+  }
+  {
+    const cudaError_t le = launch_k(engram_apply_kernel, dim3(T, 4 * gp.NSL), dim3(GATE_THREADS), 0, s, gp);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

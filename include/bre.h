@@ -245,8 +245,9 @@ bre_status engram_gather_decode(const uint8_t *const *tables, const int64_t *n_r
  *   (NULL: not written; masked tokens get gate 0).  A row id outside [0, n_rows) decodes as
  *   zeros and sets BRE_DEVERR_ROW_ID in dev_err (may be NULL).
  *   ws: engram_inject_workspace(T, R, W) bytes, zero-filled once after allocation (each call
- *   leaves its counter at zero).  Requires W % 16 == 0 and R <= 28 (the tokens' rows are held
- *   in shared memory; batches of 8 tokens run one after the other, each reading w_kv once). */
+ *   leaves its counter at zero).  Requires W % 16 == 0, W <= 8192 and R <= 24 (the tokens' rows
+ *   are held in shared memory; batches of 8 tokens run one after the other, each reading w_kv
+ *   once). */
 size_t engram_inject_workspace(int T, int R, int W);
 bre_status engram_inject(const uint8_t *table, int64_t n_rows, const int64_t *row_ids, int R, const void *w_kv_bf16,
                          int W, void *resid_bf16, const float *q_norm, const float *k_norm, const uint8_t *mask, int T,
