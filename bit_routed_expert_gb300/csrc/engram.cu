@@ -34,6 +34,68 @@ __device__ __forceinline__ void decode8(uint2 v, uint32_t sb, float (&val)[8]) {
   val[6] = __fmul_rn(f67.x, sc); val[7] = __fmul_rn(f67.y, sc);
 }
 
+// decode8 with the scale already decoded (2^(e-127) as a float).
+__device__ __forceinline__ void decode8s(uint2 v, float sc, float (&val)[8]) {
+  const float2 f01 = e4m3x2_to_f32x2(v.x & 0xFFFFu), f23 = e4m3x2_to_f32x2(v.x >> 16);
+  const float2 f45 = e4m3x2_to_f32x2(v.y & 0xFFFFu), f67 = e4m3x2_to_f32x2(v.y >> 16);
+  val[0] = __fmul_rn(f01.x, sc); val[1] = __fmul_rn(f01.y, sc);
+  val[2] = __fmul_rn(f23.x, sc); val[3] = __fmul_rn(f23.y, sc);
+  val[4] = __fmul_rn(f45.x, sc); val[5] = __fmul_rn(f45.y, sc);
+  val[6] = __fmul_rn(f67.x, sc); val[7] = __fmul_rn(f67.y, sc);
+}
+
+// Eight heads (the configuration's H): one warp per (token, table); lanes 0..7 load the eight
+// row ids with one instruction and check them with one unsigned compare; every row's loads are
+// issued before any decode; the E8M0 scales come from a 256-entry table in shared memory; the
+// first head starts the sum.  Same arithmetic as the general kernel below.
+__global__ void __launch_bounds__(256) engram_gather8_kernel(EngramTables tabs, int n_tables,
+                                                             const int64_t* __restrict__ ids, int T,
+                                                             uint16_t* __restrict__ out, int32_t* err) {
+  __shared__ float sc_tab[256];
+  sc_tab[threadIdx.x] = e8m0_to_f32(threadIdx.x);   // blockDim.x == 256
+  __syncthreads();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)T * n_tables) return;
+  const int tau = (int)(w % n_tables);
+  const uint8_t* table = tabs.ptr[0];
+  long long nrows = tabs.n_rows[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q)
+    if (tau == q) {
+      table = tabs.ptr[q];
+      nrows = tabs.n_rows[q];
+    }
+  const long long myid = lane < 8 ? __ldg(ids + w * 8 + lane) : 0;
+  const unsigned okm = __ballot_sync(0xffffffffu, (unsigned long long)myid < (unsigned long long)nrows);
+  if ((okm & 0xFFu) != 0xFFu && lane == 0) set_err(err, BRE_DEVERR_ROW_ID);
+  uint2 v[8];
+  uint32_t sb[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const long long r = __shfl_sync(0xffffffffu, myid, h);
+    const bool ok = (okm >> h) & 1u;
+    const uint8_t* row = table + (ok ? r : 0) * ENGRAM_ROW;
+    v[h] = ok ? __ldg(reinterpret_cast<const uint2*>(row) + lane) : make_uint2(0u, 0u);
+    sb[h] = ok ? __ldg(row + 256 + (lane >> 2)) : 127u;
+  }
+  float acc[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    float val[8];
+    decode8s(v[h], sc_tab[sb[h]], val);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = (h == 0) ? val[i] : __fadd_rn(acc[i], val[i]);
+  }
+  uint4 o;
+  o.x = f32_to_bf16_rne(acc[0]) | (f32_to_bf16_rne(acc[1]) << 16);
+  o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
+  o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
+  o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
+  reinterpret_cast<uint4*>(out + w * 256)[lane] = o;
+}
+
 // One warp per (token, table); HC heads per pass with every row load of the pass issued
 // before any decode.  HC is a compile-time count so that the row registers stay registers.
 template <int HC>
@@ -95,7 +157,11 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
   const long long warps = (long long)T * n_tables;
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
-  if (H == 1)
+  if (H == 8) {
+    const cudaError_t le = launch_k(engram_gather8_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, tabs,
+                                    n_tables, ids, T, out, err);
+    if (le != cudaSuccess) return le;
+  } else if (H == 1)
     {
       const cudaError_t le = launch_k(engram_gather_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0, s, tabs,
                                       n_tables, ids, T, H, out, err);
