@@ -42,7 +42,7 @@ constexpr int MAX_WARPS_P2 = 16;      // phase 2 (at most 128 registers a thread
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
-constexpr int BAR_BYTES = 512;                  // mbarrier region: MAX_WARPS * NS ring barriers + package
+constexpr int BAR_BYTES = 512;                  // mbarrier region: MAX_WARPS * NS ring barriers + package barrier
 static_assert((MAX_WARPS * NS + 1) * 8 <= BAR_BYTES, "mbarrier region too small");
 
 // n / d as a multiply and shift, for 0 <= n < 2^31 (round-up multiplier m = ceil(2^(31+l) / d),
@@ -867,9 +867,10 @@ __global__ void __launch_bounds__((PHASE == 1 ? MAX_WARPS : MAX_WARPS_P2) * 32, 
 
 // ----------------------------------------------------------------------------
 // finish: for every (pair or token, row) add the K-part partial sums of gate and up in order
-// 0..KP-1, form h = silu(gate) * up and store it in the layouts phase 2 reads (routed: two BF16
-// limbs of h * 4^-min(s,2) in the fragment order plus three limbs of each 16-row sum; shared:
-// two limbs in natural order plus FP32 16-row sums).  One warp per 32 rows of one pair/token.
+// 0..KP-1, form h = silu(gate) * up and store it in the layouts phase 2 reads (routed: BF16 of
+// h * 4^-min(s,2) in the (lane-rotated) fragment order plus three limbs of each 16-row sum of
+// the BF16 h; shared: two limbs in natural order plus FP32 16-row sums).  One warp per 32 rows
+// of one pair/token.
 // ----------------------------------------------------------------------------
 struct FinishParams {
   const float* part_r;

@@ -31,7 +31,8 @@ cudaError_t launch_route_ex(const uint16_t* x, const float* w_r, const float* bi
                             cudaStream_t s);
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
                            int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s);
-// route, then permute; for small batches the router kernel's last merging warp permutes too
+// route, then permute; for small batches the router kernel's last CTA (the one that merges every
+// token) permutes too
 cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,
                                  int32_t* ids, float* w, int32_t* offsets, int32_t* perm, int32_t* inv,
                                  int32_t* active, int32_t* n_active, int32_t* err, void* ws, cudaStream_t s);
