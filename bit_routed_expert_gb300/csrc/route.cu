@@ -710,13 +710,59 @@ __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t
   const int t0 = blockIdx.x * TILE_T, e0 = blockIdx.y * TILE_E;
   const int tsub = (warp >> 2) * 8, esub = (warp & 3) * 8;
   const int nst = (d + TR - 1) / TR;
-  float acc[8][8];
+  // accumulators of experts (2q, 2q+1) in one 64-bit register pair: fma.rn.f32x2 performs the two
+  // IEEE fmaf of each row in one instruction (the same bits as two fmaf)
+  unsigned long long acc2[8][4];
 #pragma unroll
   for (int a = 0; a < 8; ++a)
 #pragma unroll
-    for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
+    for (int q = 0; q < 4; ++q) acc2[a][q] = 0ull;
+  auto row_fma = [&](const uint16_t* X, const float* W, int c) {
+    unsigned long long xx[8], ww[4];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const float xv = bf16_bits_to_f32(X[(tsub + a) * TR + c]);
+      asm("mov.b64 %0, {%1, %1};" : "=l"(xx[a]) : "f"(xv));
+    }
+    const float4 w4 = *reinterpret_cast<const float4*>(W + c * TW + esub);
+    const float4 v4 = *reinterpret_cast<const float4*>(W + c * TW + esub + 4);
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ww[0]) : "f"(w4.x), "f"(w4.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ww[1]) : "f"(w4.z), "f"(w4.w));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ww[2]) : "f"(v4.x), "f"(v4.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ww[3]) : "f"(v4.z), "f"(v4.w));
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[a][q]) : "l"(xx[a]), "l"(ww[q]));
+  };
+
+  // full tile (every token, expert and row in range, 16-byte W rows): each thread copies the
+  // same pieces of every stage, so their addresses are set up once
+  constexpr int NWP = TR * (TILE_E / 4) / TTHREADS, NXP = TILE_T * (TR / 8) / TTHREADS;
+  static_assert(NWP * TTHREADS == TR * (TILE_E / 4) && NXP * TTHREADS == TILE_T * (TR / 8), "piece split");
+  const bool full = (t0 + TILE_T <= T) && (e0 + TILE_E <= E) && ((E & 3) == 0) && (d % TR == 0);
+  const float* gW = w_r + (size_t)(tid >> 3) * E + e0 + (tid & 7) * 4;
+  const int sW = (tid >> 3) * TW + (tid & 7) * 4;
+  const uint16_t* gX = x + (size_t)(t0 + tid / (TR / 8)) * d + (tid % (TR / 8)) * 8;
+  const int sX = (tid / (TR / 8)) * TR + (tid % (TR / 8)) * 8;
+  auto issue_full = [&](int st, int slot) {
+    float* W = Wst + slot * TR * TW;
+    uint16_t* X = Xst + slot * TILE_T * TR;
+    const float* gw = gW + (size_t)st * TR * E;
+#pragma unroll
+    for (int i = 0; i < NWP; ++i)
+      cp_async16(W + sW + i * (TTHREADS / 8) * TW, gw + (size_t)i * (TTHREADS / 8) * E, 16);
+    const uint16_t* gx = gX + (size_t)st * TR;
+#pragma unroll
+    for (int i = 0; i < NXP; ++i)
+      cp_async16(X + sX + i * (TTHREADS / (TR / 8)) * TR, gx + (size_t)i * (TTHREADS / (TR / 8)) * d, 16);
+  };
 
   auto issue = [&](int st) {
+    if (full) {
+      issue_full(st, st % TSTAGES);
+      return;
+    }
     const int c0 = st * TR;
     float* W = Wst + (size_t)(st % TSTAGES) * TR * TW;
     uint16_t* X = Xst + (size_t)(st % TSTAGES) * TILE_T * TR;
@@ -759,40 +805,42 @@ __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t
     const float* W = Wst + (size_t)(st % TSTAGES) * TR * TW;
     const uint16_t* X = Xst + (size_t)(st % TSTAGES) * TILE_T * TR;
     const int rows = min(TR, d - st * TR);
-    for (int u = 0; u < rows; u += 32) {
-      const int c = u + lane;
-      float xv[8], wv[8];
+    if (rows == TR) {
 #pragma unroll
-      for (int a = 0; a < 8; ++a) xv[a] = bf16_bits_to_f32(X[(tsub + a) * TR + c]);
-      const float4 w4 = *reinterpret_cast<const float4*>(W + c * TW + esub);
-      const float4 v4 = *reinterpret_cast<const float4*>(W + c * TW + esub + 4);
-      wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-      wv[4] = v4.x; wv[5] = v4.y; wv[6] = v4.z; wv[7] = v4.w;
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+      for (int u = 0; u < TR; u += 32) row_fma(X, W, u + lane);
+    } else {
+      for (int u = 0; u < rows; u += 32) row_fma(X, W, u + lane);
     }
   }
-  // butterfly over the 32 partials (lanes); every lane ends with the same sums
+  float v[64];   // v[a*8 + b]
 #pragma unroll
   for (int a = 0; a < 8; ++a)
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      float v = acc[a][b];
+    for (int q = 0; q < 4; ++q) asm("mov.b64 {%0, %1}, %2;" : "=f"(v[a * 8 + 2 * q]), "=f"(v[a * 8 + 2 * q + 1]) : "l"(acc2[a][q]));
+  // the butterfly over the 32 partials (xor 16, 8, 4, 2, 1) as a reduce-scatter: at each level a
+  // lane keeps the half of its sums selected by that lane bit and adds its partner's copy of them
+  // (the same pairs as the full butterfly, so the same bits); lane L ends with sums 2L and 2L+1
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-      acc[a][b] = v;
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int m = 16 >> lvl, h = 32 >> lvl;
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
     }
-#pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (lane == ((a * 8 + b) & 31)) {
-        const int t = t0 + tsub + a, e = e0 + esub + b;
-        if (t < T && e < E) S[(size_t)t * E + e] = score_ref(acc[a][b], score_fn);
-      }
+  }
+  const int t = t0 + tsub + (lane >> 2), e = e0 + esub + (lane & 3) * 2;
+  if (t < T) {
+    float* dst = S + (size_t)t * E + e;
+    if (e + 1 < E && (E & 1) == 0) {
+      *reinterpret_cast<float2*>(dst) = make_float2(score_ref(v[0], score_fn), score_ref(v[1], score_fn));
+    } else {
+      if (e < E) dst[0] = score_ref(v[0], score_fn);
+      if (e + 1 < E) dst[1] = score_ref(v[1], score_fn);
     }
+  }
 }
 
 template <int NI>
