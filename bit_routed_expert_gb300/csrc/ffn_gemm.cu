@@ -259,7 +259,44 @@ __device__ __forceinline__ void store_q80_row(const RawQ80& r, unsigned char* b_
   }
 }
 
-__device__ __forceinline__ float silu_mul(float gv, float uv) { return gv / (1.0f + expf(-gv)) * uv; }
+// silu(g) * u with the hardware exponential and a fast divide (relative error ~1e-6, far below
+// the BF16 rounding of h that follows; for g below about -88 the quotient is 0)
+__device__ __forceinline__ float silu_mul(float gv, float uv) { return __fdividef(gv, 1.0f + __expf(-gv)) * uv; }
+
+// Within each group of four lanes (rows 4q .. 4q+3 of the warp's 32 accumulator rows), a 4 x 4
+// transpose of NW-word blocks: lane 4q+p enters with the four blocks of its own row (block b =
+// v[b*NW .. b*NW+NW-1], columns b*NW ..) and leaves with block p of row 4q+k in slot k.  Two
+// exchange rounds (lane ^ 2, then lane ^ 1), each moving half of the words.  Four lanes then
+// write one row's consecutive columns, so a store instruction touches 8 rows, not 32.
+template <int NW, typename V>
+__device__ __forceinline__ void quad_transpose(V (&v)[4 * NW], int lane) {
+  const bool hi = (lane & 2) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      V& lo_s = v[j * NW + w];
+      V& hi_s = v[(2 + j) * NW + w];
+      const V recv = __shfl_xor_sync(0xffffffffu, hi ? lo_s : hi_s, 2);
+      if (hi) lo_s = recv; else hi_s = recv;
+    }
+  const bool pl = (lane & 1) != 0;
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      V& s0 = v[(2 * a) * NW + w];
+      V& s1 = v[(2 * a + 1) * NW + w];
+      const V recv = __shfl_xor_sync(0xffffffffu, pl ? s0 : s1, 1);
+      if (pl) s0 = recv; else s1 = recv;
+    }
+}
+
+__device__ __forceinline__ void st_v8(float* dst, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
+               "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
 
 struct GemmParams {
   const Plan* plan;
@@ -277,6 +314,7 @@ struct GemmParams {
   float* y_r;            // phase 2 outputs [P][d], [T][d]
   float* y_s;
   int out_ld_r, out_ld_s;
+  int out_v8;            // phase 2 outputs 32-byte aligned: 32-byte stores
   int32_t* err;
 };
 
@@ -530,41 +568,53 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const TileInfo ti = find_tile<PHASE>(p, tile);
       if (!mbar_wait_bounded(tfull, tcount & 1, G_WAIT)) { fail(); break; }
       tc_fence_after();
+      const int q4 = lane >> 2, p4 = lane & 3;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        const int mrow = ti.mt * G_BM + h * 128 + warp * 32 + lane;   // row within the group
-        const bool valid = mrow < ti.n;
+        // after the quad transpose this lane writes rows 4*q4 + k (k = 0..3) of the warp's 32
+        const int mrow0 = ti.mt * G_BM + h * 128 + warp * 32 + 4 * q4;   // row within the group
         const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + h * 256;
         if (PHASE == 1) {
-          uint16_t* out = (ti.expert < 0) ? p.h_s + (size_t)mrow * p.out_ld_s
-                                          : p.h_r + (size_t)(ti.a_row0 + mrow) * p.out_ld_r;
+          uint16_t* out0 = (ti.expert < 0) ? p.h_s + (size_t)mrow0 * p.out_ld_s
+                                           : p.h_r + (size_t)(ti.a_row0 + mrow0) * p.out_ld_r;
+          const int ld = (ti.expert < 0) ? p.out_ld_s : p.out_ld_r;
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
             float gv[32], uv[32];
             tmem_ld32(tbase + c, gv);
             tmem_ld32(tbase + 128 + c, uv);
-            if (valid) {
-              uint32_t o[16];
+            uint32_t o[16];
 #pragma unroll
-              for (int q = 0; q < 16; ++q)
-                o[q] = pack_bf16x2(silu_mul(gv[2 * q], uv[2 * q]), silu_mul(gv[2 * q + 1], uv[2 * q + 1]));
-              uint4* dst = reinterpret_cast<uint4*>(out + ti.nt * 128 + c);
+            for (int q = 0; q < 16; ++q)
+              o[q] = pack_bf16x2(silu_mul(gv[2 * q], uv[2 * q]), silu_mul(gv[2 * q + 1], uv[2 * q + 1]));
+            quad_transpose<4>(o, lane);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            }
+            for (int k = 0; k < 4; ++k)
+              if (mrow0 + k < ti.n)
+                *reinterpret_cast<uint4*>(out0 + (size_t)k * ld + ti.nt * 128 + c + 8 * p4) =
+                    make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
           }
         } else {
-          float* out = (ti.expert < 0) ? p.y_s + (size_t)mrow * p.out_ld_s
-                                       : p.y_r + (size_t)(ti.a_row0 + mrow) * p.out_ld_r;
+          float* out0 = (ti.expert < 0) ? p.y_s + (size_t)mrow0 * p.out_ld_s
+                                        : p.y_r + (size_t)(ti.a_row0 + mrow0) * p.out_ld_r;
+          const int ld = (ti.expert < 0) ? p.out_ld_s : p.out_ld_r;
 #pragma unroll 1
           for (int c = 0; c < 256; c += 32) {
             float v[32];
             tmem_ld32(tbase + c, v);
-            if (valid) {
-              float4* dst = reinterpret_cast<float4*>(out + ti.nt * 256 + c);
+            quad_transpose<8>(v, lane);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int k = 0; k < 4; ++k)
+              if (mrow0 + k < ti.n) {
+                float* dst = out0 + (size_t)k * ld + ti.nt * 256 + c + 8 * p4;
+                if (p.out_v8) {
+                  st_v8(dst, v + 8 * k);
+                } else {
+                  reinterpret_cast<float4*>(dst)[0] = make_float4(v[8 * k], v[8 * k + 1], v[8 * k + 2], v[8 * k + 3]);
+                  reinterpret_cast<float4*>(dst)[1] =
+                      make_float4(v[8 * k + 4], v[8 * k + 5], v[8 * k + 6], v[8 * k + 7]);
+                }
+              }
           }
         }
       }
@@ -690,6 +740,8 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   g.y_s = a.y_shared;
   g.out_ld_r = d;
   g.out_ld_s = d;
+  g.out_v8 = ((reinterpret_cast<uintptr_t>(a.y_pairs) | reinterpret_cast<uintptr_t>(a.y_shared)) & 31) == 0 &&
+             (d % 8) == 0;
   {
     const cudaError_t le = launch_k(ffn_gemm_kernel<2>, dim3(sms), dim3(G_THREADS), smem, s, m_hr, m_hs, g);
     if (le != cudaSuccess) return le;
