@@ -6,11 +6,13 @@
 // BF16 (w = d*sc*q - dmin*m exactly in FP32, then rounded to nearest even) straight into
 // shared memory and multiplied on tcgen05 with FP32 accumulators in tensor memory.
 //
-// Per CTA (persistent, one per SM), 10 warps:
-//   warps 0-3  epilogue: tensor memory -> registers -> SwiGLU (gate/up) or FP32 rows (down)
-//   warps 4-7  B producers: Q2_K / Q8_0 rows -> BF16, 128-byte swizzled K-major tiles
-//   warp  8    A producer: TMA 2-D tiles of the gathered activations (128-byte swizzle)
-//   warp  9    tensor-memory allocator and the single MMA-issuing thread
+// Per CTA (persistent, one per SM), 12 warps (three per scheduler, so 168 registers fit):
+//   warps 0-3   epilogue: tensor memory -> registers -> SwiGLU (gate/up) or FP32 rows (down);
+//               warp 0 also allocates tensor memory and its lane 0 issues the MMAs of a tile
+//               before the warp turns to that tile's epilogue
+//   warps 4-11  B producers: Q2_K / Q8_0 rows -> BF16, 128-byte swizzled K-major tiles, one
+//               row per thread per K step; the first producer thread also issues the TMA 2-D
+//               loads of the gathered activations (128-byte swizzle) for each stage
 // Tile: M = 256 tokens (two 128-row accumulators), N = 256 weight rows, K step = 64.
 // Phase 1: the 256 rows are 128 gate rows + the same 128 up rows, so the epilogue forms
 // h = silu(g) * u for 128 columns of the intermediate.  Phase 2: 256 down rows.
@@ -27,7 +29,8 @@ constexpr int G_STAGES = 3;
 constexpr int G_BM = 256, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 32 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
-constexpr int G_THREADS = 320;
+constexpr int G_THREADS = 384;
+constexpr int G_PRODUCERS = 256;   // B-producer threads (warps 4-11)
 constexpr int G_MAX_GROUPS = 1025;
 constexpr long long G_WAIT = 4000000000LL;   // cycles before a wait gives up (~2 s)
 
@@ -359,13 +362,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   uint64_t* tempty = tfull + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-  unsigned char* stage_raw = reinterpret_cast<unsigned char*>(full) + 256;   // [4 warps][64 rows][84 B]
+  unsigned char* stage_raw = reinterpret_cast<unsigned char*>(full) + 256;   // [8 warps][32 rows][84 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   if (threadIdx.x == 0) {
     for (int s = 0; s < G_STAGES; ++s) {
-      mbar_init(&full[s], 1 + 128);
+      mbar_init(&full[s], 1 + G_PRODUCERS);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     *abort_flag = 0;
   }
   fence_mbar_init();
-  if (warp == 9) {
+  if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_holder))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -390,88 +393,77 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
 
-  if (warp == 8) {
-    // ---------------- A producer (TMA)
-    if (lane == 0) {
-      int it = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !aborted(); tile += gridDim.x) {
-        const TileInfo ti = find_tile<PHASE>(p, tile);
-        const CUtensorMap* map = (ti.expert < 0) ? &map_s : &map_r;
-        const int row = (PHASE == 1) ? ti.a_row0 + ti.mt * G_BM : (ti.expert < 0 ? 0 : ti.a_row0) + ti.mt * G_BM;
-        const int KS = ti.K / G_BK;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % G_STAGES;
-          if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) { fail(); break; }
-          mbar_arrive_expect_tx(&full[s], G_A_BYTES);
-          tma_load_2d(a_st + s * G_A_BYTES, map, ks * G_BK, row, &full[s]);
-          tma_load_2d(a_st + s * G_A_BYTES + G_A_BYTES / 2, map, ks * G_BK, row + 128, &full[s]);
-        }
-      }
-    }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- B producers (dequantise into swizzled shared memory)
-    const int i = threadIdx.x - 128;   // rows i and i + 128 of the B tile
+  if (warp >= 4) {
+    // ---------------- B producers (dequantise into swizzled shared memory); thread i owns row i
+    // of the B tile.  The first producer thread also loads the A tile of every stage it opens.
+    const int i = threadIdx.x - 128;
+    const bool a_loader = (i == 0);
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles && !aborted(); tile += gridDim.x) {
       const TileInfo ti = find_tile<PHASE>(p, tile);
       const int KS = ti.K / G_BK;
-      const uint8_t *rowA, *rowB;
+      const CUtensorMap* amap = (ti.expert < 0) ? &map_s : &map_r;
+      const int arow = (PHASE == 1) ? ti.a_row0 + ti.mt * G_BM : (ti.expert < 0 ? 0 : ti.a_row0) + ti.mt * G_BM;
+      // wait until stage s is free, then (first thread) start its A tile
+      auto open_stage = [&](int s, int ks) -> bool {
+        if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) {
+          fail();
+          return false;
+        }
+        if (a_loader) {
+          mbar_arrive_expect_tx(&full[s], G_A_BYTES);
+          tma_load_2d(a_st + s * G_A_BYTES, amap, ks * G_BK, arow, &full[s]);
+          tma_load_2d(a_st + s * G_A_BYTES + G_A_BYTES / 2, amap, ks * G_BK, arow + 128, &full[s]);
+        }
+        return true;
+      };
+      const int pw = warp - 4;
+      unsigned char* stg = stage_raw + pw * 32 * Q2K_BB;
       if (ti.expert >= 0) {
         const int rb = (p.K_r / 256) * Q2K_BB;
-        if (PHASE == 1) {
-          rowA = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 128 + i) * rb;
-          rowB = p.r1 + (long long)ti.expert * p.rs1 + (long long)(ti.nt * 128 + i) * rb;
-        } else {
-          rowA = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + i) * rb;
-          rowB = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + 128 + i) * rb;
-        }
+        const uint8_t* row;
+        if (PHASE == 1)
+          row = (i < 128) ? p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 128 + i) * rb
+                          : p.r1 + (long long)ti.expert * p.rs1 + (long long)(ti.nt * 128 + i - 128) * rb;
+        else
+          row = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + i) * rb;
         // Whole blocks (4 K steps each) reach the warp's staging area by coalesced copies: lanes
         // 0..20 copy the 21 words of one row per instruction (a row pointer that advances by the
-        // row pitch), 64 rows per warp.  Each thread then reads its two rows into registers, and
-        // the copy of the next block runs while this one is dequantised.
+        // row pitch), 32 rows per warp, which never straddle the gate / up boundary.  Each thread
+        // then reads its row into registers, and the copy of the next block runs while this one
+        // is dequantised.
         const int NBK = KS / 4;
-        const int pw = warp - 4;
-        unsigned char* stg = stage_raw + pw * 64 * Q2K_BB;
-        const uint8_t* pa0 = rowA - (long long)lane * rb + 4 * lane;   // row 32*pw of the A set
-        const uint8_t* pb0 = rowB - (long long)lane * rb + 4 * lane;   // row 32*pw of the B set
+        const uint8_t* pr0 = row - (long long)lane * rb + 4 * lane;   // row 32*pw of the tile
         auto stage_copy = [&](int blk) {
           if (lane < 21) {
-            const uint8_t* pa = pa0 + blk * Q2K_BB;
-            const uint8_t* pb = pb0 + blk * Q2K_BB;
+            const uint8_t* pr = pr0 + blk * Q2K_BB;
             unsigned char* dst = stg + 4 * lane;
 #pragma unroll 8
-            for (int r = 0; r < 32; ++r) cp_async4(dst + r * Q2K_BB, pa + (long long)r * rb, 4);
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) cp_async4(dst + (32 + r) * Q2K_BB, pb + (long long)r * rb, 4);
+            for (int r = 0; r < 32; ++r) cp_async4(dst + r * Q2K_BB, pr + (long long)r * rb, 4);
           }
           cp_async_commit();
         };
-        auto stage_read = [&](RawBlk& a, RawBlk& b) {
+        auto stage_read = [&](RawBlk& a) {
           cp_async_wait<0>();
           __syncwarp();
 #pragma unroll
-          for (int w = 0; w < 21; ++w) {
-            a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * Q2K_BB + 4 * w);
-            b.w[w] = *reinterpret_cast<const uint32_t*>(stg + (32 + lane) * Q2K_BB + 4 * w);
-          }
+          for (int w = 0; w < 21; ++w) a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * Q2K_BB + 4 * w);
           __syncwarp();
         };
-        RawBlk ca, cb;
+        RawBlk ca;
         stage_copy(0);
         bool ok = true;
         for (int bk = 0; bk < NBK && ok; ++bk) {
-          stage_read(ca, cb);
+          stage_read(ca);
           if (bk + 1 < NBK) stage_copy(bk + 1);
 #pragma unroll
           for (int kq = 0; kq < 4; ++kq, ++it) {
             const int s = it % G_STAGES;
-            if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) {
-              fail();
+            if (!open_stage(s, bk * 4 + kq)) {
               ok = false;
               break;
             }
             store_q2k_row(quarter(ca, kq), b_st + s * G_B_BYTES, i);
-            store_q2k_row(quarter(cb, kq), b_st + s * G_B_BYTES, i + 128);
             fence_proxy_async_smem();
             mbar_arrive(&full[s]);
           }
@@ -479,93 +471,84 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         cp_async_wait<0>();   // no copy stays in flight past the tile
       } else {
         const int rb = (p.K_s / 32) * Q80_BB;
-        if (PHASE == 1) {
-          rowA = p.s0 + (long long)(ti.nt * 128 + i) * rb;
-          rowB = p.s1 + (long long)(ti.nt * 128 + i) * rb;
-        } else {
-          rowA = p.s0 + (long long)(ti.nt * 256 + i) * rb;
-          rowB = p.s0 + (long long)(ti.nt * 256 + 128 + i) * rb;
-        }
+        const uint8_t* row;
+        if (PHASE == 1)
+          row = (i < 128) ? p.s0 + (long long)(ti.nt * 128 + i) * rb : p.s1 + (long long)(ti.nt * 128 + i - 128) * rb;
+        else
+          row = p.s0 + (long long)(ti.nt * 256 + i) * rb;
         // The two Q8_0 blocks (68 bytes) of each row for a K step reach the warp's staging area
         // by coalesced copies (lanes 0..16 copy one row's 17 words per instruction); the copy of
         // the next K step runs while this one is dequantised.
-        const int pw = warp - 4;
-        unsigned char* stg = stage_raw + pw * 64 * Q2K_BB;
-        const uint8_t* pa0 = rowA - (long long)lane * rb + 4 * lane;
-        const uint8_t* pb0 = rowB - (long long)lane * rb + 4 * lane;
+        const uint8_t* pr0 = row - (long long)lane * rb + 4 * lane;
         auto stage_copy = [&](int ks) {
           if (lane < 17) {
-            const uint8_t* pa = pa0 + ks * 2 * Q80_BB;
-            const uint8_t* pb = pb0 + ks * 2 * Q80_BB;
+            const uint8_t* pr = pr0 + ks * 2 * Q80_BB;
             unsigned char* dst = stg + 4 * lane;
 #pragma unroll 8
-            for (int r = 0; r < 32; ++r) cp_async4(dst + r * 68, pa + (long long)r * rb, 4);
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) cp_async4(dst + (32 + r) * 68, pb + (long long)r * rb, 4);
+            for (int r = 0; r < 32; ++r) cp_async4(dst + r * 68, pr + (long long)r * rb, 4);
           }
           cp_async_commit();
         };
-        auto stage_read = [&](RawQ80& a, RawQ80& b) {
+        auto stage_read = [&](RawQ80& a) {
           cp_async_wait<0>();
           __syncwarp();
 #pragma unroll
-          for (int w = 0; w < 17; ++w) {
-            a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * 68 + 4 * w);
-            b.w[w] = *reinterpret_cast<const uint32_t*>(stg + (32 + lane) * 68 + 4 * w);
-          }
+          for (int w = 0; w < 17; ++w) a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * 68 + 4 * w);
           __syncwarp();
         };
-        RawQ80 ca, cb;
+        RawQ80 ca;
         stage_copy(0);
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          stage_read(ca, cb);
+          stage_read(ca);
           if (ks + 1 < KS) stage_copy(ks + 1);
           const int s = it % G_STAGES;
-          if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) { fail(); break; }
+          if (!open_stage(s, ks)) break;
           store_q80_row(ca, b_st + s * G_B_BYTES, i);
-          store_q80_row(cb, b_st + s * G_B_BYTES, i + 128);
           fence_proxy_async_smem();
           mbar_arrive(&full[s]);
         }
         cp_async_wait<0>();   // no copy stays in flight past the tile
       }
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      // kind::f16, D = F32, A = B = BF16, both K-major, M = 128, N = 256
-      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(G_BN >> 3) << 17) |
-                             ((uint32_t)(128 >> 4) << 24);
-      int it = 0, tcount = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !aborted(); tile += gridDim.x, ++tcount) {
-        const TileInfo ti = find_tile<PHASE>(p, tile);
-        const int KS = ti.K / G_BK;
-        if (!mbar_wait_bounded(tempty, (tcount & 1) ^ 1, G_WAIT)) { fail(); break; }
-        tc_fence_after();
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % G_STAGES;
-          if (!mbar_wait_bounded(&full[s], (it / G_STAGES) & 1, G_WAIT)) { fail(); break; }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(a_st + s * G_A_BYTES);
-          const uint32_t b0 = smem_u32(b_st + s * G_B_BYTES);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int kk = 0; kk < G_BK / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(a0 + h * (G_A_BYTES / 2) + kk * 32);
-              const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
-              mma_f16_ss(tmem + h * 256, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-            }
-          mma_commit(&empty[s]);
-        }
-        mma_commit(tfull);
-      }
-    }
   } else {
-    // ---------------- epilogue (warps 0-3: tensor-memory lanes 32*warp .. +31)
-    int tcount = 0;
+    // ---------------- MMA issue (warp 0, lane 0) and epilogue (warps 0-3: tensor-memory lanes
+    // 32*warp .. +31)
+    // kind::f16, D = F32, A = B = BF16, both K-major, M = 128, N = 256
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(G_BN >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    int it = 0, tcount = 0;
     for (int tile = blockIdx.x; tile < n_tiles && !aborted(); tile += gridDim.x, ++tcount) {
       const TileInfo ti = find_tile<PHASE>(p, tile);
+      if (warp == 0 && lane == 0) {
+        const int KS = ti.K / G_BK;
+        // the previous tile's epilogue has drained the accumulators
+        if (!mbar_wait_bounded(tempty, (tcount & 1) ^ 1, G_WAIT)) {
+          fail();
+        } else {
+          tc_fence_after();
+          for (int ks = 0; ks < KS; ++ks, ++it) {
+            const int s = it % G_STAGES;
+            if (!mbar_wait_bounded(&full[s], (it / G_STAGES) & 1, G_WAIT)) {
+              fail();
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(a_st + s * G_A_BYTES);
+            const uint32_t b0 = smem_u32(b_st + s * G_B_BYTES);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int kk = 0; kk < G_BK / 16; ++kk) {
+                const uint64_t ad = smem_desc_sw128(a0 + h * (G_A_BYTES / 2) + kk * 32);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
+                mma_f16_ss(tmem + h * 256, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+              }
+            mma_commit(&empty[s]);
+          }
+          mma_commit(tfull);
+        }
+      }
+      __syncwarp();
       if (!mbar_wait_bounded(tfull, tcount & 1, G_WAIT)) { fail(); break; }
       tc_fence_after();
       const int q4 = lane >> 2, p4 = lane & 3;
@@ -624,7 +607,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
@@ -679,7 +662,7 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const size_t smem = G_STAGES * (G_A_BYTES + G_B_BYTES) + 1024 + 256 + 4 * 64 * Q2K_BB;
+  const size_t smem = G_STAGES * (G_A_BYTES + G_B_BYTES) + 1024 + 256 + 8 * 32 * Q2K_BB;
   static int configured = -1;
   int dev;
   cudaGetDevice(&dev);
