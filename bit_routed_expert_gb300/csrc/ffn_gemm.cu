@@ -6,10 +6,11 @@
 // BF16 (w = d*sc*q - dmin*m exactly in FP32, then rounded to nearest even) straight into
 // shared memory and multiplied on tcgen05 with FP32 accumulators in tensor memory.
 //
-// Per CTA (persistent, one per SM), 12 warps (three per scheduler, so 168 registers fit):
-//   warps 0-3   epilogue: tensor memory -> registers -> SwiGLU (gate/up) or FP32 rows (down);
-//               warp 0 also allocates tensor memory and its lane 0 issues the MMAs of a tile
-//               before the warp turns to that tile's epilogue
+// Per CTA (persistent, one per SM), 16 warps (128 registers a thread):
+//   warps 0-3, 12-15  epilogue: tensor memory -> registers -> SwiGLU (gate/up) or FP32 rows
+//               (down); warps w and w+12 share tensor-memory lanes 32w .. +31 and take one half
+//               of the columns each; warp 0 also allocates tensor memory and its lane 0 issues
+//               the MMAs of a tile before the warp turns to that tile's epilogue
 //   warps 4-11  B producers: Q2_K / Q8_0 rows -> BF16, 128-byte swizzled K-major tiles, one
 //               row per thread per K step; the first producer thread also issues the TMA 2-D
 //               loads of the gathered activations (128-byte swizzle) for each stage
@@ -29,7 +30,7 @@ constexpr int G_STAGES = 3;
 constexpr int G_BM = 256, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 32 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
-constexpr int G_THREADS = 384;
+constexpr int G_THREADS = 512;
 constexpr int G_PRODUCERS = 256;   // B-producer threads (warps 4-11)
 constexpr int G_MAX_GROUPS = 1025;
 constexpr long long G_WAIT = 4000000000LL;   // cycles before a wait gives up (~2 s)
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 128);
+    mbar_init(tempty, 256);
     *abort_flag = 0;
   }
   fence_mbar_init();
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
 
-  if (warp >= 4) {
+  if (warp >= 4 && warp < 12) {
     // ---------------- B producers (dequantise into swizzled shared memory); thread i owns row i
     // of the B tile.  The first producer thread also loads the A tile of every stage it opens.
     const int i = threadIdx.x - 128;
@@ -511,8 +512,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       }
     }
   } else {
-    // ---------------- MMA issue (warp 0, lane 0) and epilogue (warps 0-3: tensor-memory lanes
-    // 32*warp .. +31)
+    // ---------------- MMA issue (warp 0, lane 0) and epilogue (warps 0-3 and 12-15: tensor-memory
+    // lanes 32*(warp & 3) .. +31, column half warp >= 12)
     // kind::f16, D = F32, A = B = BF16, both K-major, M = 128, N = 256
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(G_BN >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
@@ -552,17 +553,18 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!mbar_wait_bounded(tfull, tcount & 1, G_WAIT)) { fail(); break; }
       tc_fence_after();
       const int q4 = lane >> 2, p4 = lane & 3;
+      const int eq = warp & 3, part = warp >> 3;   // lane quarter, column half
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         // after the quad transpose this lane writes rows 4*q4 + k (k = 0..3) of the warp's 32
-        const int mrow0 = ti.mt * G_BM + h * 128 + warp * 32 + 4 * q4;   // row within the group
-        const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + h * 256;
+        const int mrow0 = ti.mt * G_BM + h * 128 + eq * 32 + 4 * q4;   // row within the group
+        const uint32_t tbase = tmem + ((uint32_t)(eq * 32) << 16) + h * 256;
         if (PHASE == 1) {
           uint16_t* out0 = (ti.expert < 0) ? p.h_s + (size_t)mrow0 * p.out_ld_s
                                            : p.h_r + (size_t)(ti.a_row0 + mrow0) * p.out_ld_r;
           const int ld = (ti.expert < 0) ? p.out_ld_s : p.out_ld_r;
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = part * 64; c < part * 64 + 64; c += 32) {
             float gv[32], uv[32];
             tmem_ld32(tbase + c, gv);
             tmem_ld32(tbase + 128 + c, uv);
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                                         : p.y_r + (size_t)(ti.a_row0 + mrow0) * p.out_ld_r;
           const int ld = (ti.expert < 0) ? p.out_ld_s : p.out_ld_r;
 #pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
+          for (int c = part * 128; c < part * 128 + 128; c += 32) {
             float v[32];
             tmem_ld32(tbase + c, v);
             quad_transpose<8>(v, lane);
