@@ -90,24 +90,38 @@ __global__ void plan_kernel(const int32_t* __restrict__ offsets, const int32_t* 
   plan->tiles2 = t2;
 }
 
-// X_perm[q] = x[perm[q] / k] for valid pairs q < offsets[E]; X_perm[P + t] = x[t].
+// X_perm[q] = x[perm[q] / k] for valid pairs q < offsets[E]; X_perm[P + t] = x[t].  One warp per
+// row, eight 16-byte loads in flight per lane before their stores.
 __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                               const int32_t* __restrict__ offsets, int E, int k, int T, int P, int d,
                               uint16_t* __restrict__ xp, int has_shared) {
   pdl_wait();
   const int per_row = d / 8;
   const int nvalid = __ldg(offsets + E);
-  const long long total = (long long)(P + T) * per_row;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int q = (int)(i / per_row), c = (int)(i % per_row);
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int q = blockIdx.x * wpb + (threadIdx.x >> 5); q < P + T; q += gridDim.x * wpb) {
     int src = -1;
     if (q < nvalid)
       src = __ldg(perm + q) / k;
     else if (q >= P && has_shared)
       src = q - P;
     if (src < 0) continue;
-    reinterpret_cast<uint4*>(xp + (size_t)q * d)[c] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)src * d) + c);
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)src * d);
+    uint4* out = reinterpret_cast<uint4*>(xp + (size_t)q * d);
+    for (int c0 = 0; c0 < per_row; c0 += 8 * 32) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < per_row) v[u] = __ldg(in + c);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < per_row) out[c] = v[u];
+      }
+    }
   }
 }
 

@@ -29,8 +29,11 @@ cudaError_t launch_route_ex(const uint16_t* x, const float* w_r, const float* bi
                             int score, const float* vision_bias, const uint8_t* is_media, const int32_t* tid2eid,
                             const int32_t* token_ids, int vocab, int32_t* ids, float* w, int32_t* err, void* ws,
                             cudaStream_t s);
+// scratch (device, >= ceil(T k / 1024) (E + 1) int32) lets more than 1,024 pairs be permuted by
+// three grid-wide launches instead of one CTA; without it (or when too small) one CTA does all
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
-                           int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s);
+                           int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s, void* scratch = nullptr,
+                           size_t scratch_bytes = 0);
 // route, then permute; for small batches the router kernel's last CTA (the one that merges every
 // token) permutes too
 cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const float* bias, int T, int d, int E, int k,

@@ -980,6 +980,136 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) permute_kernel(const int32_t*
   }
 }
 
+// Large P: the same stable order from three launches over chunks of PERM_THREADS pairs (the
+// one-CTA kernel's chunks): per-chunk histograms; one CTA turns them into each chunk's first
+// position per key (global base of the key + the key's count in earlier chunks) and writes the
+// offsets and the active list; then every chunk places its pairs with the warp-match rank.
+__global__ void __launch_bounds__(PERM_THREADS) perm_count_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                                  int32_t* __restrict__ counts, int32_t* err) {
+  extern __shared__ __align__(16) int hist[];   // [E+1]
+  pdl_wait();
+  const int tid = threadIdx.x;
+  for (int i = tid; i <= E; i += PERM_THREADS) hist[i] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * PERM_THREADS + tid;
+  if (p < P) {
+    const int e = ids[p];
+    const bool ok = (e >= 0 && e < E);
+    if (!ok) set_err(err, BRE_DEVERR_EXPERT_ID);
+    atomicAdd(&hist[ok ? e : E], 1);
+  }
+  __syncthreads();
+  for (int i = tid; i <= E; i += PERM_THREADS) counts[(size_t)blockIdx.x * (E + 1) + i] = hist[i];
+}
+
+__global__ void __launch_bounds__(PERM_THREADS, 1) perm_scan_kernel(int32_t* __restrict__ counts, int nch, int E,
+                                                                    int32_t* __restrict__ offsets,
+                                                                    int32_t* __restrict__ active,
+                                                                    int32_t* __restrict__ n_active) {
+  __shared__ int tot[PERM_EMAX + 1];
+  __shared__ int wsum[32];
+  __shared__ int wflag[32];
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // per key: counts of earlier chunks (in place), and the key's total
+  for (int e = tid; e <= E; e += PERM_THREADS) {
+    int run = 0;
+#pragma unroll 4
+    for (int c = 0; c < nch; ++c) {
+      const int v = counts[(size_t)c * (E + 1) + e];
+      counts[(size_t)c * (E + 1) + e] = run;
+      run += v;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of tot[0..E) -> base; active flags scan -> active list (E <= 1024: one per thread)
+  const int c = (tid < E) ? tot[tid] : 0;
+  const int f = (tid < E && c > 0) ? 1 : 0;
+  int ic = c, iff = f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, o);
+    const int b = __shfl_up_sync(0xffffffffu, iff, o);
+    if (lane >= o) {
+      ic += a;
+      iff += b;
+    }
+  }
+  if (lane == 31) {
+    wsum[warp] = ic;
+    wflag[warp] = iff;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int sm = wsum[lane], g = wflag[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, sm, o);
+      const int b = __shfl_up_sync(0xffffffffu, g, o);
+      if (lane >= o) {
+        sm += a;
+        g += b;
+      }
+    }
+    wsum[lane] = sm;   // inclusive over warps
+    wflag[lane] = g;
+  }
+  __syncthreads();
+  const int prev_c = (warp > 0 ? wsum[warp - 1] : 0) + ic - c;
+  const int prev_f = (warp > 0 ? wflag[warp - 1] : 0) + iff - f;
+  const int total_valid = wsum[31], total_active = wflag[31];
+  __syncthreads();   // every thread has read tot[tid] before it is overwritten with the base
+  if (tid < E) {
+    tot[tid] = prev_c;
+    offsets[tid] = prev_c;
+    if (f) active[prev_f] = tid;
+  }
+  if (tid == 0) {
+    tot[E] = total_valid;   // invalid ids go after every valid pair
+    offsets[E] = total_valid;
+    *n_active = total_active;
+  }
+  for (int i = total_active + tid; i < E; i += PERM_THREADS) active[i] = -1;
+  __syncthreads();
+  for (int e = tid; e <= E; e += PERM_THREADS) {
+    const int b = tot[e];
+#pragma unroll 4
+    for (int cc = 0; cc < nch; ++cc) counts[(size_t)cc * (E + 1) + e] += b;
+  }
+}
+
+__global__ void __launch_bounds__(PERM_THREADS) perm_place_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                                  const int32_t* __restrict__ cbase,
+                                                                  int32_t* __restrict__ perm,
+                                                                  int32_t* __restrict__ inv) {
+  extern __shared__ __align__(16) int place_smem[];
+  int* base = place_smem;                                                       // [E+1]
+  unsigned short* wcnt = reinterpret_cast<unsigned short*>(base + (E + 1));     // [32][E+1]
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i <= E; i += PERM_THREADS) base[i] = cbase[(size_t)blockIdx.x * (E + 1) + i];
+  for (int i = tid; i < 32 * (E + 1); i += PERM_THREADS) wcnt[i] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * PERM_THREADS + tid;
+  int key = -1;
+  if (p < P) {
+    const int e = ids[p];
+    key = (e >= 0 && e < E) ? e : E;
+  }
+  const unsigned m = __match_any_sync(0xffffffffu, key);
+  const int lrank = __popc(m & ((1u << lane) - 1u));
+  if (p < P && lrank == 0) wcnt[warp * (E + 1) + key] = (unsigned short)__popc(m);
+  __syncthreads();
+  if (p < P) {
+    int pre = 0;
+    for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * (E + 1) + key];
+    const int pos = base[key] + pre + lrank;
+    perm[pos] = p;
+    inv[p] = pos;
+  }
+}
+
 }  // namespace
 
 size_t route_ws_bytes(int T, int E) {
@@ -1029,7 +1159,9 @@ cudaError_t launch_route_permute(const uint16_t* x, const float* w_r, const floa
       route_impl(x, w_r, bias, T, d, E, k, ids, w, ws, PermOut{offsets, perm, inv, active, n_active}, rv, &permuted,
                  s);
   if (e != cudaSuccess || permuted) return e;
-  return launch_permute(ids, T, k, E, offsets, perm, inv, active, n_active, err, s);
+  // the score buffer is dead once the top k are chosen: it holds the chunk counts
+  return launch_permute(ids, T, k, E, offsets, perm, inv, active, n_active, err, s,
+                        static_cast<char*>(ws) + 256, route_ws_bytes(T, E) - 256);
 }
 
 namespace {
@@ -1138,7 +1270,32 @@ cudaError_t route_impl(const uint16_t* x, const float* w_r, const float* bias, i
 }  // namespace
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
-                           int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s) {
+                           int32_t* active, int32_t* n_active, int32_t* err, cudaStream_t s, void* scratch,
+                           size_t scratch_bytes) {
+  const int P = T * k;
+  const int nch = (P + PERM_THREADS - 1) / PERM_THREADS;
+  if (nch > 1 && scratch != nullptr && (size_t)nch * (E + 1) * sizeof(int32_t) <= scratch_bytes) {
+    int32_t* counts = static_cast<int32_t*>(scratch);
+    const size_t place_smem = (size_t)(E + 1) * sizeof(int) + (size_t)32 * (E + 1) * sizeof(unsigned short);
+    static int place_dev = -1;
+    int dev;
+    cudaGetDevice(&dev);
+    if (dev != place_dev) {
+      const int max_smem = (int)((size_t)(PERM_EMAX + 1) * sizeof(int) + (size_t)32 * (PERM_EMAX + 1) * 2);
+      cudaError_t e = cudaFuncSetAttribute(perm_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+      place_dev = dev;
+    }
+    cudaError_t le = launch_k(perm_count_kernel, dim3(nch), dim3(PERM_THREADS), (size_t)(E + 1) * sizeof(int), s, ids,
+                              P, E, counts, err);
+    if (le != cudaSuccess) return le;
+    le = launch_k(perm_scan_kernel, dim3(1), dim3(PERM_THREADS), 0, s, counts, nch, E, offsets, active, n_active);
+    if (le != cudaSuccess) return le;
+    le = launch_k(perm_place_kernel, dim3(nch), dim3(PERM_THREADS), place_smem, s, ids, P, E,
+                  static_cast<const int32_t*>(counts), perm, inv);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)3 * (E + 1) * sizeof(int) + (size_t)32 * (E + 1) * sizeof(unsigned short);
   static int configured_dev = -1;
   int dev;
