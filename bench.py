@@ -314,8 +314,10 @@ def timed(fn, K, flush, stream, per_call_events=False):
 
 
 def layer_breakdown(layer, xs, out, n, flush):
-    """Median time of each call of a layer forward (route, permute, expert FFN, combine), in us."""
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    """Median time of each call of a layer forward, in us: route_permute (the fused call the
+    layer makes), expert FFN, combine; and, timed on their own, route alone and the rest of
+    route_permute (its permutation)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
     for i, ev in enumerate(evs):
         flush_l2(flush)
         x = xs[i % len(xs)]
@@ -323,18 +325,22 @@ def layer_breakdown(layer, xs, out, n, flush):
         ev[0].record()
         ids, w = api.moe_route(x, layer.w_r, layer.bias, layer.k, ws=layer.route_ws)
         ev[1].record()
-        perm = api.moe_permute(ids, layer.E, dev_err=layer.dev_err)
+        flush_l2(flush)
         ev[2].record()
+        ids, w, perm = api.moe_route_permute(x, layer.w_r, layer.bias, layer.k, ws=layer.route_ws,
+                                             dev_err=layer.dev_err)
+        ev[3].record()
         yp, ys = api.moe_expert_ffn(layer.routed, layer.shared, x, layer.k, perm, ws=layer.ffn_ws,
                                     dev_err=layer.dev_err, y_pairs=layer.y_pairs[:T * layer.k],
                                     y_shared=None if layer.y_shared is None else layer.y_shared[:T])
-        ev[3].record()
-        api.moe_combine(yp, w, perm["inv"], perm["offsets"], layer.E, ys, layer.k, out=out)
         ev[4].record()
+        api.moe_combine(yp, w, perm["inv"], perm["offsets"], layer.E, ys, layer.k, out=out)
+        ev[5].record()
     torch.cuda.synchronize()
-    names = ["route", "permute", "expert_ffn", "combine"]
-    return {nm: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in evs) * 1e3, 2)
-            for q, nm in enumerate(names)}
+    med = lambda a, b: round(statistics.median(e[a].elapsed_time(e[b]) for e in evs) * 1e3, 2)
+    bd = {"route_permute": med(2, 3), "expert_ffn": med(3, 4), "combine": med(4, 5), "route": med(0, 1)}
+    bd["permute"] = round(bd["route_permute"] - bd["route"], 2)
+    return bd
 
 
 def run_prefill(args, ws, rank, local):
