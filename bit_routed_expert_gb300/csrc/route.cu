@@ -981,9 +981,9 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) permute_kernel(const int32_t*
 }
 
 // Large P: the same stable order from three launches over chunks of PERM_THREADS pairs (the
-// one-CTA kernel's chunks): per-chunk histograms; one CTA turns them into each chunk's first
-// position per key (global base of the key + the key's count in earlier chunks) and writes the
-// offsets and the active list; then every chunk places its pairs with the warp-match rank.
+// one-CTA kernel's chunks): per-chunk histograms; one CTA turns each key's counts into the
+// counts of earlier chunks and writes the offsets (the keys' global bases) and the active list;
+// then every chunk places its pairs at offset + earlier-chunk count + warp-match rank.
 __global__ void __launch_bounds__(PERM_THREADS) perm_count_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                                   int32_t* __restrict__ counts, int32_t* err) {
   extern __shared__ __align__(16) int hist[];   // [E+1]
@@ -1011,14 +1011,20 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) perm_scan_kernel(int32_t* __r
   __shared__ int wflag[32];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // per key: counts of earlier chunks (in place), and the key's total
+  // per key: counts of earlier chunks (in place), and the key's total; twelve chunks' counts
+  // are loaded before any is rewritten
   for (int e = tid; e <= E; e += PERM_THREADS) {
     int run = 0;
-#pragma unroll 4
-    for (int c = 0; c < nch; ++c) {
-      const int v = counts[(size_t)c * (E + 1) + e];
-      counts[(size_t)c * (E + 1) + e] = run;
-      run += v;
+    for (int c0 = 0; c0 < nch; c0 += 12) {
+      int v[12];
+#pragma unroll
+      for (int u = 0; u < 12; ++u) v[u] = (c0 + u < nch) ? counts[(size_t)(c0 + u) * (E + 1) + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 12; ++u)
+        if (c0 + u < nch) {
+          counts[(size_t)(c0 + u) * (E + 1) + e] = run;
+          run += v[u];
+        }
     }
     tot[e] = run;
   }
@@ -1059,28 +1065,20 @@ __global__ void __launch_bounds__(PERM_THREADS, 1) perm_scan_kernel(int32_t* __r
   const int prev_c = (warp > 0 ? wsum[warp - 1] : 0) + ic - c;
   const int prev_f = (warp > 0 ? wflag[warp - 1] : 0) + iff - f;
   const int total_valid = wsum[31], total_active = wflag[31];
-  __syncthreads();   // every thread has read tot[tid] before it is overwritten with the base
   if (tid < E) {
-    tot[tid] = prev_c;
     offsets[tid] = prev_c;
     if (f) active[prev_f] = tid;
   }
   if (tid == 0) {
-    tot[E] = total_valid;   // invalid ids go after every valid pair
-    offsets[E] = total_valid;
+    offsets[E] = total_valid;   // invalid ids go after every valid pair
     *n_active = total_active;
   }
   for (int i = total_active + tid; i < E; i += PERM_THREADS) active[i] = -1;
-  __syncthreads();
-  for (int e = tid; e <= E; e += PERM_THREADS) {
-    const int b = tot[e];
-#pragma unroll 4
-    for (int cc = 0; cc < nch; ++cc) counts[(size_t)cc * (E + 1) + e] += b;
-  }
 }
 
 __global__ void __launch_bounds__(PERM_THREADS) perm_place_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                                                  const int32_t* __restrict__ cbase,
+                                                                  const int32_t* __restrict__ earlier,
+                                                                  const int32_t* __restrict__ offsets,
                                                                   int32_t* __restrict__ perm,
                                                                   int32_t* __restrict__ inv) {
   extern __shared__ __align__(16) int place_smem[];
@@ -1088,7 +1086,7 @@ __global__ void __launch_bounds__(PERM_THREADS) perm_place_kernel(const int32_t*
   unsigned short* wcnt = reinterpret_cast<unsigned short*>(base + (E + 1));     // [32][E+1]
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i <= E; i += PERM_THREADS) base[i] = cbase[(size_t)blockIdx.x * (E + 1) + i];
+  for (int i = tid; i <= E; i += PERM_THREADS) base[i] = offsets[i] + earlier[(size_t)blockIdx.x * (E + 1) + i];
   for (int i = tid; i < 32 * (E + 1); i += PERM_THREADS) wcnt[i] = 0;
   __syncthreads();
   const int p = blockIdx.x * PERM_THREADS + tid;
@@ -1292,7 +1290,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
     le = launch_k(perm_scan_kernel, dim3(1), dim3(PERM_THREADS), 0, s, counts, nch, E, offsets, active, n_active);
     if (le != cudaSuccess) return le;
     le = launch_k(perm_place_kernel, dim3(nch), dim3(PERM_THREADS), place_smem, s, ids, P, E,
-                  static_cast<const int32_t*>(counts), perm, inv);
+                  static_cast<const int32_t*>(counts), static_cast<const int32_t*>(offsets), perm, inv);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
   }
