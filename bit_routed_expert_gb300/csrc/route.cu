@@ -693,8 +693,8 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
 // and widens in registers.  One barrier per stage.  (Measured on GB300: an 8-token x 16-expert
 // tile per thread with 8 warps, and widening x once per stage into a transposed FP32 tile, were
 // both slower than this.)
-constexpr int TR = 128;
-constexpr int TSTAGES = 3;
+constexpr int TR = 512;
+constexpr int TSTAGES = 2;
 constexpr int TTHREADS = 512;
 constexpr int TW = TILE_E + 4;   // padded W row (words)
 constexpr size_t TILED_SMEM = (size_t)TSTAGES * (TR * TW * 4 + TILE_T * TR * 2);
