@@ -612,7 +612,9 @@ __host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
 //   three BF16 limbs; X32: 32-value sums (Q8_0 shared expert).
 __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restrict__ x, int T, int d,
                                                        unsigned char* __restrict__ pkg) {
-  pdl_wait();
+  // x was final before the preceding launch (the router) passed its own wait, and nothing before
+  // this kernel touches the package, so the work runs first and the wait (which the kernels
+  // after this one rely on) comes last: behind a router that triggers early, it overlaps it
   const int b = blockIdx.x, t = blockIdx.y, i = threadIdx.x, lane = i & 31;
   const int nbx = d / 256;
   const PkgLayout L = pkg_layout(T, d);
@@ -648,6 +650,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
     dst[4] = (uint16_t)mid;
     dst[8] = (uint16_t)lo;
   }
+  pdl_wait();
 }
 
 // ----------------------------------------------------------------------------

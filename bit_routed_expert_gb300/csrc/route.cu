@@ -422,6 +422,9 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
     for (int i = 0; i < n; ++i) cp_async4(dst + (size_t)i * RC_J * 32, src + i * rstride, e < E ? 4 : 0);
   }
   pdl_wait();
+  // the next launch may start now: every kernel that follows waits for this grid before it uses
+  // anything this grid writes (the decode FFN's prep reads only x, which the wait above covers)
+  pdl_launch_dependents();
   // stage x: item q = (i, tt) reads the RC_J values x[t0+tt][32 i + RC_J jb ...] (8 bytes); a
   // thread's loads (eight at a time) are all issued before their stores, so their latencies
   // overlap instead of adding up

@@ -188,7 +188,10 @@ bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *
  *   ws: moe_expert_ffn_workspace(T, ...) bytes, zero-filled once after allocation.
  *   Its leading part holds counters that each call leaves at zero again; a
  *   workspace sized for T serves every call with T' <= T (same k, d, d_ff,
- *   d_ff_shared).  Calls sharing one workspace must be ordered.
+ *   d_ff_shared).  Calls sharing one workspace must be ordered.  The workspace
+ *   must not overlap any buffer of the call enqueued just before this one on the
+ *   stream (for T <= 8 its first kernel packs x into the workspace while a
+ *   preceding moe_route_permute may still be running; it reads only x_bf16).
  * Shapes: d and d_ff multiples of 256; for T <= 8 each of d, d_ff either
  * <= 1024 or a multiple of 1024 (Q2_K rows reach shared memory as whole
  * 16-row tiles or as 4-block tensor-copy pieces with a 16-byte row pitch). */
