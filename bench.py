@@ -199,15 +199,24 @@ class DecodeWorkload:
         self.ids_h = [torch.from_numpy(ids_all[s * T:(s + 1) * T].copy()) for s in range(N_SETS)]
         self.xs = [x.to(dev) for x in self.xs_h]
         self.ids = [i.to(dev) for i in self.ids_h]
-        self.out = torch.empty((T, sh.d), dtype=torch.bfloat16, device=dev)
-        self.eout = torch.empty((T, 512), dtype=torch.bfloat16, device=dev)
-        # pinned host buffers for the end-to-end measurement
-        self.xs_pin = [x.pin_memory() for x in self.xs_h]
-        self.ids_pin = [i.pin_memory() for i in self.ids_h]
-        self.x_dev = torch.empty((T, sh.d), dtype=torch.bfloat16, device=dev)
-        self.ids_dev = torch.empty((T, 2, ENGRAM_H), dtype=torch.int64, device=dev)
-        self.out_pin = torch.empty((T, sh.d), dtype=torch.bfloat16).pin_memory()
-        self.eout_pin = torch.empty((T, 512), dtype=torch.bfloat16).pin_memory()
+        # the end-to-end step moves its inputs in one host-to-device copy and its outputs in one
+        # device-to-host copy: x and the Engram ids share one byte buffer, the layer output and
+        # the Engram rows another (views below), on the device and in pinned host memory
+        xb, ib = T * sh.d * 2, T * 2 * ENGRAM_H * 8
+        ob, eb = T * sh.d * 2, T * 512 * 2
+        self.in_dev = torch.empty(xb + ib, dtype=torch.uint8, device=dev)
+        self.x_dev = self.in_dev[:xb].view(torch.bfloat16).view(T, sh.d)
+        self.ids_dev = self.in_dev[xb:].view(torch.int64).view(T, 2, ENGRAM_H)
+        self.in_pin = []
+        for s in range(N_SETS):
+            buf = torch.empty(xb + ib, dtype=torch.uint8).pin_memory()
+            buf[:xb].view(torch.bfloat16).view(T, sh.d).copy_(self.xs_h[s])
+            buf[xb:].view(torch.int64).view(T, 2, ENGRAM_H).copy_(self.ids_h[s])
+            self.in_pin.append(buf)
+        self.res_dev = torch.empty(ob + eb, dtype=torch.uint8, device=dev)
+        self.out = self.res_dev[:ob].view(torch.bfloat16).view(T, sh.d)
+        self.eout = self.res_dev[ob:].view(torch.bfloat16).view(T, 512)
+        self.res_pin = torch.empty(ob + eb, dtype=torch.uint8).pin_memory()
         self.ffn_events = None
         self.side = torch.cuda.Stream(device=dev)
 
@@ -237,15 +246,13 @@ class DecodeWorkload:
 
     def step_e2e(self, i: int):
         s = i % N_SETS
-        self.x_dev.copy_(self.xs_pin[s], non_blocking=True)
-        self.ids_dev.copy_(self.ids_pin[s], non_blocking=True)
+        self.in_dev.copy_(self.in_pin[s], non_blocking=True)
         if self.engram:
             self._engram_fork(self.ids_dev)
         self.layer.forward(self.x_dev, out=self.out)
         if self.engram:
             self._engram_join()
-        self.out_pin.copy_(self.out, non_blocking=True)
-        self.eout_pin.copy_(self.eout, non_blocking=True)
+        self.res_pin.copy_(self.res_dev, non_blocking=True)
 
     @property
     def h2d_bytes(self):
