@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ y_shared, int T, int k, int d,
                                                       uint16_t* __restrict__ out, float* __restrict__ out_f32) {
   pdl_wait();
+  pdl_launch_dependents();   // the next launch waits for this grid before it reads anything
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int per_row = d / 4;
   if (i >= (long long)T * per_row) return;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(256) residual_norm_kernel(const uint16_t* __re
   extern __shared__ float xs[];  // [d]
   __shared__ float r_s;
   pdl_wait();
+  pdl_launch_dependents();   // the next launch waits for this grid before it reads anything
   const int t = blockIdx.x;
   const uint16_t* xr = x + (size_t)t * d;
   const uint16_t* mr = moe + (size_t)t * d;
