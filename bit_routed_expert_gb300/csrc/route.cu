@@ -724,7 +724,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) route_tiled_kernel(const uint16_t
     unsigned long long xx[8], ww[4];
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
-      const float xv = bf16_bits_to_f32(X[(tsub + a) * TR + c]);
+      // BF16 -> FP32 by one byte permute (integer pipe; the FMA pipe is the busy one)
+      uint32_t xf;
+      asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(xf) : "r"((uint32_t)X[(tsub + a) * TR + c]));
+      const float xv = __uint_as_float(xf);
       asm("mov.b64 %0, {%1, %1};" : "=l"(xx[a]) : "f"(xv));
     }
     const float4 w4 = *reinterpret_cast<const float4*>(W + c * TW + esub);
