@@ -177,10 +177,12 @@ def test_route_odd_shapes(cuda_dev, T, d, E, k):
 
 
 @pytest.mark.parametrize("shape,T", [(synth.TINY, 4), (synth.V41, 1), (synth.V41, 8), (synth.V41, 5),
-                                     (synth.V41, 17), (synth.V41, 32), (synth.V41, 33), (synth.TINY, 300)])
+                                     (synth.V41, 17), (synth.V41, 32), (synth.V41, 33), (synth.TINY, 300),
+                                     (synth.TINY, 1000), (synth.TINY, 2731), (synth.V41, 700)])
 def test_route_permute_fused(cuda_dev, shape, T):
     """moe_route_permute equals the oracle's route followed by its permutation (one launch up to
-    32 tokens, two above)."""
+    32 tokens; above, the scores and top k, then a permutation that takes three grid-wide
+    launches over chunks of 1,024 pairs once there are more than 1,024 pairs)."""
     x = synth.x_bf16(SEED, 0, 9, T, shape.d)
     w_r = synth.router_weight(SEED, 0, shape.d, shape.E)
     b = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width)
