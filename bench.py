@@ -17,6 +17,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -308,6 +309,12 @@ def flush_l2(buf):
     buf.fill_(1)
 
 
+def spread_us(ms):
+    """p10 / p50 / p90 of per-call times given in ms, in us."""
+    q = np.percentile(np.asarray(ms, dtype=np.float64) * 1e3, [10, 50, 90])
+    return {"p10": round(float(q[0]), 2), "p50": round(float(q[1]), 2), "p90": round(float(q[2]), 2)}
+
+
 def timed(fn, K, flush, stream, per_call_events=False):
     """K timed calls of fn(i) with an L2 flush before each; returns per-call ms."""
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -392,6 +399,7 @@ def run_prefill(args, ws, rank, local):
                          "traffic": measured_traffic("prefill_T8192_ffn_traffic", "ffn_gemm.cu"),
                          "peak_source": pk["source"]},
             "ffn_ms_median": round(statistics.median(ffn_ms), 4), "step_ms_median": round(statistics.median(ms), 4),
+            "step_us_spread": spread_us(ms), "ffn_us_spread": spread_us(ffn_ms),
             "breakdown_us_median": bd, "clocks": clk}
 
 
@@ -439,6 +447,7 @@ def run_verify(args, ws, rank, local):
                        "distinct_experts_first_pass": ub, "l2": "flushed before every timed pass",
                        "launch": "each pass replayed as one captured CUDA graph"},
             "eager_pass_us_median": round(statistics.median(eager_ms) * 1e3, 1),
+            "pass_us_spread": spread_us(ms),
             "expert_gbs": round(expert_bytes / (med * 1e-3) / 1e9, 1),
             "all_bytes_gbs": round(all_bytes / (med * 1e-3) / 1e9, 1),
             "roofline": {"bound": "hbm", "kernel": "whole pass", "achieved": round(all_bytes / (med * 1e-3) / 1e9, 1),
@@ -481,7 +490,7 @@ def run_engram(args, ws, rank, local):
             "roofline": {"bound": "hbm", "kernel": "engram_gather_kernel", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "traffic": None, "peak_source": pk["source"]},
-            "us_median": round(med * 1e3, 2), "clocks": clk}
+            "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms), "clocks": clk}
 
 
 def run_route(args, ws, rank, local):
@@ -586,7 +595,7 @@ def run_engram_gate(args, ws, rank, local):
             "roofline": {"bound": "hbm", "kernel": "engram_kv_kernel + engram_gate_kernel", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "traffic": None, "peak_source": pk["source"]},
-            "us_median": round(med * 1e3, 2), "clocks": clk}
+            "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms), "clocks": clk}
 
 
 def run_ours(args, ws, rank, local):
@@ -660,14 +669,7 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "decode MoE layer T=8" + ("" if args.no_engram else " + Engram gather") +
-                   " (V4.1 shape)", "T": T, "d": 4096, "E": 384,
-                   "k": 6, "d_ff": 2048, "shared_d_ff": 2048, "route_bias": "U(-0.5,0.5)",
-                   "expert_format": "Q2_K (84 B / 256)", "shared_format": "Q8_0 (34 B / 32)",
-                   "engram": "2 tables x 4194304 rows x 264 B, 8 heads/table", "token_sets": N_SETS,
-                   "launch": "each step replayed as one captured CUDA graph" +
-                             ("" if args.no_engram else "; the Engram gather runs on a parallel branch"),
-                   "l2": "flushed by a 256 MiB write before every timed step", "parallelism": f"replicas{ws}"},
+        "config": decode_config(T, not args.no_engram, ws),
         "e2e": {"value": round(job_throughput(ws, T, K, total_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": K * wl.launches_per_step,
@@ -679,6 +681,9 @@ def run_ours(args, ws, rank, local):
         "step_hbm_gbs": round(sum(step_bytes) / (sum(step_ms) * 1e-3) / 1e9, 1),
         "ffn_us_median": round(statistics.median(ffn_ms) * 1e3, 2),
         "step_us_median": round(statistics.median(step_ms) * 1e3, 2),
+        "step_us_spread": spread_us(step_ms),
+        "ffn_us_spread": spread_us(ffn_ms),
+        "e2e_step_us_spread": spread_us(e2e_ms),
         "eager_step_us_median": round(statistics.median(eager_ms) * 1e3, 2),
         "active_experts_per_set": counts,
         "breakdown_us_median_eager": breakdown,
@@ -740,7 +745,36 @@ def cpu_baseline(T: int, n_steps: int = 2):
     return {"value": round(T * n_steps / tot, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{n_steps} full decode steps (T={T} MoE layer + Engram gather of the same tokens), "
                       f"single-threaded C oracle, FP64 FFN; expert bytes generated outside the timed part",
-            "seconds": round(tot, 2)}
+            "seconds": round(tot, 2), "host": host_cpu()}
+
+
+def host_cpu():
+    """The host's CPU model and core count ("1 of N cores" for the single-threaded oracle)."""
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    model = {"0xd4f": "Arm Neoverse V2 (CPU part 0xd4f)", "0xd40": "Arm Neoverse V1 (CPU part 0xd40)",
+             "0xd0c": "Arm Neoverse N1 (CPU part 0xd0c)"}.get(model, model)
+    return {"model": model, "arch": platform.machine(), "nproc": os.cpu_count(),
+            "used": f"1 of {os.cpu_count()} cores"}
+
+
+def decode_config(T: int, engram: bool, ws: int) -> dict:
+    """The decode line's config (the reference arm reports the same)."""
+    return {"workload": "decode MoE layer T=8" + (" + Engram gather" if engram else "") + " (V4.1 shape)",
+            "T": T, "d": 4096, "E": 384, "k": 6, "d_ff": 2048, "shared_d_ff": 2048, "route_bias": "U(-0.5,0.5)",
+            "expert_format": "Q2_K (84 B / 256)", "shared_format": "Q8_0 (34 B / 32)",
+            "engram": "2 tables x 4194304 rows x 264 B, 8 heads/table", "token_sets": N_SETS,
+            "launch": "each step replayed as one captured CUDA graph" +
+                      ("; the Engram gather runs on a parallel branch" if engram else ""),
+            "l2": "flushed by a 256 MiB write before every timed step", "parallelism": f"replicas{ws}"}
 
 
 def run_reference(args, ws, rank):
@@ -757,9 +791,10 @@ def run_reference(args, ws, rank):
             "value": round(v, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode MoE layer T=8 + Engram gather (V4.1 shape)", "T": T},
+            "config": decode_config(T, True, 1),
             "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: one full decode step (T={T}) of the single-threaded C oracle"},
+                             "sample": f"each step: one full decode step (T={T}) of the single-threaded C oracle",
+                             "host": host_cpu()},
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
