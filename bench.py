@@ -89,7 +89,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the clock record goes to $BRE_OUT_DIR (default: out/ beside this file)
+        self.path = os.path.join(os.environ.get("BRE_OUT_DIR", os.path.join(ROOT, "out")), f"clocks_gpu{gpu_index}.csv")
 
     def _query_once(self):
         try:

@@ -76,7 +76,7 @@ def log_error(ratio: float, shape):
     """Record the achieved max|err|/rms of a layer comparison (evidence for the design notes)."""
     import inspect
     import os
-    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+    out = os.environ.get("BRE_OUT_DIR", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "out"))
     if os.path.isdir(out):
         caller = inspect.stack()[2].function
         with open(os.path.join(out, "parity_errors.txt"), "a") as f:
