@@ -167,8 +167,11 @@ bre_status moe_route_ex(const void *x_bf16, const float *w_r, const float *bias,
 /* moe_route followed by moe_permute, with the same arguments and outputs as the two calls
  * (ws: moe_route_workspace(T, E) bytes, zero-filled once after allocation).  For batches of
  * at most 32 tokens the router kernel's last CTA (the one that merges every token's
- * candidates) also builds the permutation, so the pair is one launch; otherwise the two kernels run back to back on `stream`.  Router ids are
- * always in [0, E), so dev_err is only touched by the second form. */
+ * candidates) also builds the permutation, so the pair is one launch.  Otherwise the router's
+ * launches are followed by the permutation; above 1,024 pairs it runs as three grid-wide
+ * launches over chunks of 1,024 pairs that keep their per-chunk key counts in ws (the router's
+ * score buffer, no longer needed by then), with the same result as moe_permute.  Router ids
+ * are always in [0, E), so dev_err is only touched by the second form. */
 bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
                              int32_t *topk_ids, float *topk_w, int32_t *offsets, int32_t *perm, int32_t *inv,
                              int32_t *active, int32_t *n_active, int32_t *dev_err, void *ws, size_t ws_bytes,
