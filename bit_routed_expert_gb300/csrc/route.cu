@@ -171,63 +171,47 @@ template <int NI>
 __device__ void topk_warp(const float* __restrict__ s_row, const float* __restrict__ bias, int E, int k,
                           int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
   const int lane = threadIdx.x & 31;
-  float sv[NI], kv[NI];
+  float sv[NI];
+  // selection code of each candidate, ordered as the selection order (larger key first, NaN
+  // last, -0 equal to +0; ties go to the lower id): finite and infinite keys map monotonically
+  // to codes >= 0x007FFFFF, NaN to 1, a slot past E to 0 (never selected)
+  uint32_t kc[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
+    sv[i] = 0.0f;
+    kc[i] = 0u;
     if (e < E) {
       sv[i] = __ldcg(s_row + e);
-      kv[i] = __fadd_rn(sv[i], bias ? __ldg(bias + e) : 0.0f);
-    } else {
-      sv[i] = 0.0f;
-      kv[i] = 0.0f;
+      const float key = __fadd_rn(__fadd_rn(sv[i], bias ? __ldg(bias + e) : 0.0f), 0.0f);   // -0 -> +0
+      const uint32_t b = __float_as_uint(key);
+      kc[i] = isnan(key) ? 1u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
     }
   }
   uint32_t used = 0;
   float my_sel_s = 0.0f;
   int my_sel_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bk = 0.0f, bs = 0.0f;
-    int bid = -1;
+    // lane-local best (the first of equal codes is the lowest id), then the warp's: the largest
+    // code, and among the lanes holding it the lowest id
+    uint32_t bc = 0u;
+    int bi = -1;
+    float bs = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((used >> i) & 1u)) {
-        if (bid < 0 || ranks_before(kv[i], e, bk, bid)) {
-          bk = kv[i];
-          bid = e;
-          bs = sv[i];
-        }
+    for (int i = 0; i < NI; ++i)
+      if (!((used >> i) & 1u) && kc[i] > bc) {
+        bc = kc[i];
+        bi = i;
+        bs = sv[i];
       }
-    }
-    // warp arg-best; lanes with no candidate carry id = INT_MAX and rank last
-    float wk = bk;
-    int wid = bid < 0 ? 0x7FFFFFFF : bid;
-    bool has = bid >= 0;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, wk, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, wid, o);
-      const bool ohas = __shfl_xor_sync(0xffffffffu, (int)has, o) != 0;
-      bool take;
-      if (has != ohas)
-        take = ohas;
-      else if (!has)
-        take = oid < wid;
-      else
-        take = ranks_before(ok, oid, wk, wid);
-      if (take) {
-        wk = ok;
-        wid = oid;
-        has = ohas;
-      }
-    }
-    const int owner = wid & 31;
+    const uint32_t wc = __reduce_max_sync(0xffffffffu, bc);
+    const uint32_t wid = __reduce_min_sync(0xffffffffu, (bi >= 0 && bc == wc) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+    const int owner = (int)(wid & 31u);
     const float ws = __shfl_sync(0xffffffffu, bs, owner);
     if (lane == owner) used |= 1u << (wid >> 5);
     if (lane == j) {
       my_sel_s = ws;
-      my_sel_id = wid;
+      my_sel_id = (int)wid;
     }
   }
   float S = 0.0f;
