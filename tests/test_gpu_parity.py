@@ -282,14 +282,22 @@ def test_route_ex_hash_errors(cuda_dev, T):
     assert int(err) == err_ref
 
 
-def test_route_ties_and_zero_bias(cuda_dev):
+@pytest.mark.parametrize("T", [3, 40])
+def test_route_ties_and_zero_bias(cuda_dev, T):
+    """Equal keys go to the lower id, NaN keys rank after every number (T = 3: the small-batch
+    kernel; T = 40: the tiled logits and the warp top k)."""
     d, E, k = 64, 16, 6
-    x = synth.x_bf16(2, 0, 0, 3, d)
+    x = synth.x_bf16(2, 0, 0, T, d)
     w_r = torch.zeros((d, E))
     b = torch.zeros(E)
     b[9] = 0.25
     b[12] = 0.25
-    for bias in (None, b):
+    bn = torch.full((E,), float("nan"))   # only experts 2, 7, 11 and 14 have a number
+    bn[2] = 0.1
+    bn[7] = -0.2
+    bn[11] = 0.1
+    bn[14] = 0.3
+    for bias in (None, b, bn):
         ids_ref, w_ref = oracle.route(x, w_r, bias, k)
         ids, w = api.moe_route(x.to(cuda_dev), w_r.to(cuda_dev), None if bias is None else bias.to(cuda_dev), k)
         assert np.array_equal(ids.cpu().numpy(), ids_ref)
