@@ -1,5 +1,4 @@
 // extern "C" entry points of libbre: host-side argument checks, then the launchers.
-#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "bre.h"
@@ -25,14 +24,6 @@ const DevAttr& attr() {
   return a;
 }
 }  // namespace
-
-bool pdl_enabled() {
-  static const bool on = [] {
-    const char* v = getenv("BRE_PDL");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
 
 int device_sm_count() { return attr().sms; }
 int device_max_smem_optin() { return attr().smem_optin; }

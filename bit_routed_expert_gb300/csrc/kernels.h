@@ -77,11 +77,9 @@ cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t n_blocks, flo
 bool encode_tiled(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 
-// Launch with programmatic dependent launch allowed (unless BRE_PDL=0 in the environment): the
-// kernel may be scheduled while the previous kernel on the stream drains, so every kernel
-// launched this way calls pdl_wait() before it reads another kernel's results or writes
-// memory an earlier kernel may still read.
-bool pdl_enabled();
+// Launch with programmatic dependent launch allowed: the kernel may be scheduled while the
+// previous kernel on the stream drains, so every kernel launched this way calls pdl_wait()
+// before it reads another kernel's results or writes memory an earlier kernel may still read.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -93,7 +91,7 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 

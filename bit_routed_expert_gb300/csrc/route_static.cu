@@ -1,13 +1,13 @@
 // moe_route_static: the router with its scratch in a fixed device array instead of a
 // caller-provided workspace, for callers that cannot allocate device memory.
 //
-// Who needs it: code that runs inside a CUDA stream capture in global capture mode (where
-// cudaMalloc is refused), serving loops that may not call cudaMalloc because it can
-// synchronise the whole device, and host integrations that are handed only pre-allocated
-// input and output buffers with no access to an allocator.  This call allocates nothing:
-// it neither calls cudaMalloc/cudaFree nor any library routine that allocates.
+// Who needs it: serving loops that may not call cudaMalloc on the hot path because it can
+// synchronise the whole device and stall every stream, and host integrations (plugins, runtimes
+// that own the allocator) that are handed only pre-allocated input and output buffers and have
+// no way to ask for scratch.  This call allocates nothing: it neither calls cudaMalloc/cudaFree
+// nor any library routine that allocates.
 //
-// The scratch is one file-scope device array of ROUTE_STATIC_SCRATCH bytes (about 384 KB),
+// The scratch is one file-scope device array of ROUTE_STATIC_SCRATCH bytes (about 388 KB),
 // loaded with the library and held by every GPU that loads it until the process exits.  All calls share
 // it, so calls that overlap on the GPU (other streams, other host threads) race and must be
 // ordered by the caller.  The selection tickets at its start must be zero before a call; they are
@@ -21,10 +21,12 @@
 
 namespace {
 
-// tickets, then either the scores of a large batch (T*E floats) or the selection candidates
-// of a small batch (at most 32 tokens x 1024 expert slots x 12 bytes)
+// tickets, then either the scores of a large batch (T*E floats) or, for a small batch (at most
+// 32 tokens), the selection candidates (1024 expert slots x 12 bytes a token) followed by the hash
+// rows' table scores (32 floats a token): the largest moe_route_workspace of any shape the call
+// accepts (T * E <= BRE_ROUTE_STATIC_MAX_TE, E <= 1024), less its 256-byte ticket area
 constexpr size_t ROUTE_STATIC_SCORES = (size_t)BRE_ROUTE_STATIC_MAX_TE * sizeof(float);
-constexpr size_t ROUTE_STATIC_CANDIDATES = (size_t)32 * 1024 * 12;
+constexpr size_t ROUTE_STATIC_CANDIDATES = (size_t)32 * 1024 * 12 + (size_t)32 * 32 * 4;
 constexpr size_t ROUTE_STATIC_SCRATCH =
     256 + (ROUTE_STATIC_SCORES > ROUTE_STATIC_CANDIDATES ? ROUTE_STATIC_SCORES : ROUTE_STATIC_CANDIDATES);
 

@@ -107,15 +107,16 @@ size_t moe_route_workspace(int T, int E);
 bre_status moe_route(const void *x_bf16, const float *w_r, const float *bias, int T, int d, int E, int k,
                      int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, bre_stream_t stream);
 
-/* moe_route without a workspace argument, for callers that cannot allocate device memory
- * (code running under stream capture in global mode, where cudaMalloc is refused; serving
- * loops that must not call cudaMalloc because it may synchronise the device; integrations
- * handed only pre-allocated buffers).  The pages have no counterpart: it is an interface
+/* moe_route without a workspace argument, for callers that cannot allocate device memory:
+ * serving loops that must not call cudaMalloc on the hot path (it may synchronise the whole
+ * device), and integrations that are handed only pre-allocated input and output buffers with
+ * no allocator to ask for scratch.  The pages have no counterpart: it is an interface
  * convenience of this library.  It computes exactly what moe_route computes.
  *   Scratch: one fixed device array inside the library (256 bytes plus the larger of
- *   4 * BRE_ROUTE_STATIC_MAX_TE and 384 KB), held by every GPU that loads the library until
- *   the process exits.  T * E above BRE_ROUTE_STATIC_MAX_TE, or a shape whose
- *   moe_route_workspace exceeds the array, returns BRE_ERR_WORKSPACE.  Allocates nothing.
+ *   4 * BRE_ROUTE_STATIC_MAX_TE and 397,312 bytes, about 388 KB), held by every GPU that
+ *   loads the library until the process exits.  T * E above BRE_ROUTE_STATIC_MAX_TE, or a
+ *   shape whose moe_route_workspace exceeds the array, returns BRE_ERR_WORKSPACE.  Allocates
+ *   nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   The first call on a device looks up the array's device address (and may load the
  *   library's device code); make that first call before any stream capture.
  *   Every call shares the array: calls that overlap on the GPU (different streams or host

@@ -27,10 +27,14 @@ def device_layer(seed: int, layer: int, shape: synth.MoeShape, T_max: int, dev, 
 
 
 def oracle_layer(seed: int, layer: int, shape: synth.MoeShape, x: torch.Tensor, with_shared: bool = True,
-                 ids_hint=None):
-    """Oracle MoE layer on CPU; experts are generated only for the experts the oracle's router selects."""
+                 ids_hint=None, bias=None, threads: int = 1):
+    """Oracle MoE layer on CPU; experts are generated only for the experts the oracle's router selects.
+    bias: overrides the shape's route bias.  threads > 1 splits the tokens into that many chunks run
+    on threads (the oracle is plain C without shared state, and ctypes releases the GIL; each token's
+    output depends on that token alone)."""
     w_r = synth.router_weight(seed, layer, shape.d, shape.E)
-    bias = synth.route_bias(seed, layer, shape.E, shape.bias_half_width, shape.zipf)
+    if bias is None:
+        bias = synth.route_bias(seed, layer, shape.E, shape.bias_half_width, shape.zipf)
     ids, _ = oracle.route(x, w_r, bias, shape.k)
     need = sorted(set(int(e) for e in ids.reshape(-1)))
     gate, up, down = [None] * shape.E, [None] * shape.E, [None] * shape.E
@@ -45,7 +49,17 @@ def oracle_layer(seed: int, layer: int, shape: synth.MoeShape, x: torch.Tensor, 
         su = synth.shared_matrix(seed, layer, synth.S_SUP, shape).numpy()
         sd = synth.shared_matrix(seed, layer, synth.S_SDOWN, shape).numpy()
         Fs = shape.F_shared
-    return oracle.moe_layer(x.cpu(), w_r, bias, shape.k, shape.F, gate, up, down, sg, su, sd, Fs)
+    x = x.cpu()
+    T = x.shape[0]
+    if threads <= 1 or T < 2:
+        return oracle.moe_layer(x, w_r, bias, shape.k, shape.F, gate, up, down, sg, su, sd, Fs)
+    import concurrent.futures as cf
+    bounds = np.linspace(0, T, min(threads, T) + 1).astype(int)
+    parts = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    with cf.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        res = list(ex.map(lambda ab: oracle.moe_layer(x[ab[0]:ab[1]].contiguous(), w_r, bias, shape.k, shape.F, gate,
+                                                      up, down, sg, su, sd, Fs), parts))
+    return {key: np.concatenate([r[key] for r in res]) for key in res[0]}
 
 
 def run_layer(layer: MoeLayer, x: torch.Tensor):

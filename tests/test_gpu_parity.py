@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from bit_routed_expert_gb300 import api, synth
-from bit_routed_expert_gb300.api import BRE_FMT_Q2_K, BRE_FMT_Q8_0
+from bit_routed_expert_gb300.api import BRE_FMT_Q2_K, BRE_FMT_Q8_0, FfnWeights, MoeLayer
 from helpers import assert_layer_close, bf16_bits, device_layer, oracle_layer, run_layer
 
 pytestmark = pytest.mark.gpu
@@ -469,6 +469,58 @@ def test_layer_prefill_full_shape_sampled(cuda_dev):
     ref = oracle_layer(SEED, 0, shape, x[sample])
     assert np.array_equal(ids[sample], ref["ids"])
     assert_layer_close(out[sample], of[sample], ref)
+    assert int(layer.dev_err) == 0
+
+
+def test_layer_prefill_every_m_tile_sampled(cuda_dev):
+    """The prefill layer (T = 8192, Zipf-skewed routing) on a sample that reaches every 256-pair
+    M tile of every active expert's group (one pair at a varying row inside each tile, plus each
+    group's last pair, so the ragged last tiles are in) and every 256-token tile of the shared
+    expert; the oracle runs on the sampled tokens."""
+    shape, T = synth.V41_PREFILL, 8192
+    layer = device_layer(SEED, 0, shape, T, cuda_dev)
+    x = synth.x_bf16(SEED, 0, 0, T, shape.d)
+    out, of, info = run_layer(layer, x.to(cuda_dev))
+    ids = info["ids"].cpu().numpy()
+    offsets = info["offsets"].cpu().numpy()
+    perm = info["perm"].cpu().numpy()
+    k = shape.k
+    chosen = set()
+    for e in range(shape.E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for m, start in enumerate(range(lo, hi, 256)):
+            n = min(256, hi - start)
+            chosen.add(int(perm[start + (37 * m + 11) % n]) // k)
+        if hi > lo:
+            chosen.add(int(perm[hi - 1]) // k)
+    n_group_tiles = len(chosen)
+    for m in range(T // 256):                       # the shared expert's M tiles (all tokens)
+        chosen.add(256 * m + (53 * m) % 256)
+    sample = np.array(sorted(chosen))
+    assert n_group_tiles >= (T * k) // 256
+    ref = oracle_layer(SEED, 0, shape, x[sample], threads=16)
+    assert np.array_equal(ids[sample], ref["ids"])
+    assert_layer_close(out[sample], of[sample], ref)
+    assert int(layer.dev_err) == 0
+
+
+def test_layer_gemm_tiny_dominant_expert(cuda_dev):
+    """Grouped-GEMM path with one expert holding every token: 900 pairs = three full 256-pair M
+    tiles and a ragged fourth; the whole [T, d] output is compared with the oracle."""
+    shape, T = synth.TINY, 900
+    lw = synth.layer_weights(SEED, 0, shape, device=cuda_dev)
+    bias = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width).clone()
+    bias[5] += 4.0                                  # sigmoid scores lie in (0, 1): expert 5 always wins
+    layer = MoeLayer(lw.w_r.to(cuda_dev), bias.to(cuda_dev),
+                     FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, shape.d, shape.F),
+                     FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, shape.d, shape.F_shared), shape.k, T)
+    x = synth.x_bf16(SEED, 0, 61, T, shape.d)
+    out, of, info = run_layer(layer, x.to(cuda_dev))
+    offsets = info["offsets"].cpu().numpy()
+    assert offsets[6] - offsets[5] == T
+    ref = oracle_layer(SEED, 0, shape, x, bias=bias, threads=8)
+    assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+    assert_layer_close(out, of, ref)
     assert int(layer.dev_err) == 0
 
 

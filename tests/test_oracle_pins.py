@@ -730,6 +730,40 @@ def test_engram_gate_known_dot():
         assert np.array_equal(out, ref.view(torch.int16).numpy().view(np.uint16))
 
 
+def test_engram_gate_known_dot_with_norm_weights():
+    """The q_norm and k_norm factors of the dot product (strix-llama.cpp issue, "Placement":
+    dot = sum_i residual * q_norm * k_norm * key), pinned with weights that differ by branch and
+    by index: r = 1, key = a, q_norm[h,i] = 2^((i+h) mod 3), k_norm[h,i] = 2^-((i+2h) mod 5).
+    Then dot_h = a * S_h / sqrt(1 + eps) / sqrt(a^2 + eps) / sqrt(W) with S_h = sum_i
+    q_norm[h,i] k_norm[h,i], an exact dyadic sum.  Dropping either factor, using one of them
+    twice, or reading another branch's weights changes S_h (the four S_h differ, and differ from
+    sum q_norm^2, sum k_norm^2 and W)."""
+    from fractions import Fraction
+    T, W, eps = 1, 64, 1e-6
+    i = np.arange(W)
+    qn = np.stack([2.0 ** ((i + h) % 3) for h in range(4)]).astype(np.float32)
+    kn = np.stack([2.0 ** -((i + 2 * h) % 5) for h in range(4)]).astype(np.float32)
+    S = [sum(Fraction(2) ** (((j + h) % 3) - ((j + 2 * h) % 5)) for j in range(W)) for h in range(4)]
+    assert len(set(S)) == 4
+    for h in range(4):
+        others = {sum(Fraction(2) ** (2 * ((j + h) % 3)) for j in range(W)),
+                  sum(Fraction(2) ** (-2 * ((j + 2 * h) % 5)) for j in range(W)), Fraction(W)}
+        assert S[h] not in others
+    for a, v in ((0.75, 0.3), (-2.0, 1.5)):
+        kv = np.zeros((T, 5 * W))
+        kv[:, :4 * W] = a
+        kv[:, 4 * W:] = v
+        resid = _bf16(np.ones((T, 4, W)))
+        out, g = oracle.engram_gate(kv, resid, qn, kn, eps=eps)
+        vb = float(_bf16([v]).float()[0])
+        for h in range(4):
+            dot = a * float(S[h]) / math.sqrt(1 + eps) / math.sqrt(a * a + eps) / math.sqrt(W)
+            ref_g = _sig(math.copysign(math.sqrt(max(abs(dot), 1e-6)), dot))
+            assert abs(g[0, h] - ref_g) <= 1e-12
+            ref = _bf16(np.full(W, 1.0 + ref_g * vb))
+            assert np.array_equal(out[0, h], ref.view(torch.int16).numpy().view(np.uint16))
+
+
 def test_engram_gate_zero_key_floor_and_zero_value_identity():
     kv, resid, qn, kn = _gate_case()
     W = resid.shape[-1]
