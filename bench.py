@@ -8,8 +8,12 @@ plus the Engram gather-decode of the same 8 tokens (2 tables x 4,194,304 rows x 
 8 hash heads per table).  Eight token sets rotate; L2 is flushed (a 256 MiB write)
 before every timed step.  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|engram|verify]
+The default line also carries "sub_records": decode at T = 1, 2, 4, the prefill layer
+(T = 8192, Zipf-skewed routing), the Engram gather at T = 8192 and the 24-layer verify pass
+(T = 5), each timed the same way with its own clock record and its own oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-sub]
+                  [--workload decode|prefill|verify|engram|route|engram_gate]
 """
 from __future__ import annotations
 
@@ -184,18 +188,23 @@ def job_throughput(ws: int, units_per_rank: float, steps: int, total_ms_max: flo
 class DecodeWorkload:
     """MoE layer at the V4.1 decode shape (T tokens) + Engram gather of the same tokens."""
 
-    def __init__(self, dev, T: int, rank: int, engram: bool = True):
+    def __init__(self, dev, T: int, rank: int, engram: bool = True, lw=None, tables=None):
+        """lw / tables: the layer's weights and the Engram tables of another workload, reused
+        (the same seeded bytes) so that other batch sizes need no second copy."""
         self.dev, self.T = dev, T
         self.engram = engram
         self.shape = synth.V41
         sh = self.shape
-        lw = synth.layer_weights(SEED, 0, sh, device=dev)
+        if lw is None:
+            lw = synth.layer_weights(SEED, 0, sh, device=dev)
         self.lw = lw
         self.layer = MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d,
                                                                           sh.F),
                               FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
-        self.tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
-                       for tau in range(2)] if engram else None
+        if engram and tables is None:
+            tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
+                      for tau in range(2)]
+        self.tables = tables if engram else None
         ids_all = synth.engram_ids_ngram(SEED + rank, N_SETS * T, 2, ENGRAM_H, ENGRAM_ROWS)
         self.xs_h = [synth.x_bf16(SEED + 1000 * rank, 0, 200 + s, T, sh.d) for s in range(N_SETS)]
         self.ids_h = [torch.from_numpy(ids_all[s * T:(s + 1) * T].copy()) for s in range(N_SETS)]
@@ -358,12 +367,15 @@ def layer_breakdown(layer, xs, out, n, flush):
     return bd
 
 
-def run_prefill(args, ws, rank, local):
-    """One MoE layer at T = 8192 with Zipf(1.1)-skewed routing (grouped GEMM on tcgen05)."""
+def run_prefill(args, ws, rank, local, lw=None):
+    """One MoE layer at T = 8192 with Zipf(1.1)-skewed routing (grouped GEMM on tcgen05).
+    lw: the decode layer's weights (the same seeded experts), reused with the skewed bias."""
     dev = torch.device("cuda", local)
     sh, T = synth.V41_PREFILL, 8192
-    lw = synth.layer_weights(SEED, 0, sh, device=dev)
-    layer = MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
+    if lw is None:
+        lw = synth.layer_weights(SEED, 0, sh, device=dev)
+    bias = synth.route_bias(SEED, 0, sh.E, sh.bias_half_width, sh.zipf)
+    layer = MoeLayer(lw.w_r.to(dev), bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
                      FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
     xs = [synth.x_bf16(SEED + 1000 * rank, 0, s, T, sh.d).to(dev) for s in range(2)]
     out = torch.empty((T, sh.d), dtype=torch.bfloat16, device=dev)
@@ -397,6 +409,8 @@ def run_prefill(args, ws, rank, local):
             "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (plan, gather, grouped GEMM x2)",
                          "achieved": round(tfl, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tfl / pk["bf16_tflops"], 4),
+                         "peak_sustained": pk["bf16_tflops_sustained"],
+                         "frac_of_sustained": round(tfl / pk["bf16_tflops_sustained"], 4),
                          "traffic": measured_traffic("prefill_T8192_ffn_traffic", "ffn_gemm.cu"),
                          "peak_source": pk["source"]},
             "ffn_ms_median": round(statistics.median(ffn_ms), 4), "step_ms_median": round(statistics.median(ms), 4),
@@ -404,13 +418,14 @@ def run_prefill(args, ws, rank, local):
             "breakdown_us_median": bd, "clocks": clk}
 
 
-def run_verify(args, ws, rank, local):
-    """Speculative-verify batch: T = 5 rows through 24 MoE layers (76 GB of experts resident)."""
+def run_verify(args, ws, rank, local, lw0=None):
+    """Speculative-verify batch: T = 5 rows through 24 MoE layers (76 GB of experts resident).
+    lw0: layer 0's weights when already resident (the decode layer is layer 0)."""
     dev = torch.device("cuda", local)
     sh, T, L = synth.V41, 5, 24
     layers = []
     for l in range(L):
-        lw = synth.layer_weights(SEED, l, sh, device=dev)
+        lw = lw0 if (l == 0 and lw0 is not None) else synth.layer_weights(SEED, l, sh, device=dev)
         layers.append(MoeLayer(lw.w_r.to(dev), lw.bias.to(dev),
                                FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
                                FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T))
@@ -458,12 +473,13 @@ def run_verify(args, ws, rank, local):
             "gpu_launches_per_pass": 1 + L * 8, "clocks": clk}
 
 
-def run_engram(args, ws, rank, local):
+def run_engram(args, ws, rank, local, tables=None):
     """Engram gather-decode at scale: T = 8192 tokens x 2 tables x 8 heads over 4,194,304-row tables."""
     dev = torch.device("cuda", local)
     T = 8192
-    tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
-              for tau in range(2)]
+    if tables is None:
+        tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
+                  for tau in range(2)]
     ids = [torch.from_numpy(synth.engram_ids_ngram(SEED + 17 * s + rank, T, 2, ENGRAM_H, ENGRAM_ROWS)).to(dev)
            for s in range(4)]
     out = torch.empty((T, 512), dtype=torch.bfloat16, device=dev)
@@ -599,22 +615,28 @@ def run_engram_gate(args, ws, rank, local):
             "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms), "clocks": clk}
 
 
-def run_ours(args, ws, rank, local):
+def run_ours(args, ws, rank, local, T=None, lw=None, tables=None, full=True):
+    """The decode step at batch T (default --T): graph replays of the whole step, the same step
+    end to end with its host copies (full=True), and the expert FFN call alone for the roofline.
+    full=False (the other decode batch sizes) leaves out the end-to-end loop and the per-call
+    breakdown.  Returns (record, workload)."""
     dev = torch.device("cuda", local)
-    T = args.T
-    wl = DecodeWorkload(dev, T, rank, engram=not args.no_engram)
+    T = args.T if T is None else T
+    wl = DecodeWorkload(dev, T, rank, engram=not args.no_engram, lw=lw, tables=tables)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):
         wl.step(i)
-        wl.step_e2e(i)
+        if full:
+            wl.step_e2e(i)
     torch.cuda.synchronize()
     # one captured graph per token set: the step, and the step with its host copies
     graphs = [api.StepGraph(lambda s=s: wl.step(s)) for s in range(N_SETS)]
-    graphs_e2e = [api.StepGraph(lambda s=s: wl.step_e2e(s)) for s in range(N_SETS)]
+    graphs_e2e = [api.StepGraph(lambda s=s: wl.step_e2e(s)) for s in range(N_SETS)] if full else []
     for i in range(args.warmup):
         graphs[i % N_SETS].replay()
-        graphs_e2e[i % N_SETS].replay()
+        if full:
+            graphs_e2e[i % N_SETS].replay()
     torch.cuda.synchronize()
     K = args.steps
     clocks = ClockSampler(local)
@@ -624,7 +646,7 @@ def run_ours(args, ws, rank, local):
     t_wall = time.perf_counter()
     step_ms = timed(lambda i: graphs[i % N_SETS].replay(), K, flush, stream)
     wall = time.perf_counter() - t_wall
-    e2e_ms = timed(lambda i: graphs_e2e[i % N_SETS].replay(), K, flush, stream)
+    e2e_ms = timed(lambda i: graphs_e2e[i % N_SETS].replay(), K, flush, stream) if full else None
     clk = clocks.stop()
     barrier(ws)
     # the expert FFN alone (its own flush-separated loop) for the roofline line
@@ -637,19 +659,7 @@ def run_ours(args, ws, rank, local):
     ffn_ms = timed(lambda i: api.moe_expert_ffn(L.routed, L.shared, wl.xs[i % N_SETS], L.k, perms[i % N_SETS],
                                                 ws=L.ffn_ws, dev_err=L.dev_err, y_pairs=L.y_pairs[:T * L.k],
                                                 y_shared=L.y_shared[:T]), K, flush, stream)
-    eager_ms = timed(lambda i: wl.step(i), min(K, 50), flush, stream)
-    # per-call breakdown (eager, separate pass)
-    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(min(K, 50))]
-    for i, evs in enumerate(bev):
-        flush_l2(flush)
-        wl.step_breakdown(i, evs)
-    torch.cuda.synchronize()
-    names = ["route_permute", "", "expert_ffn", "combine", "engram"]
-    breakdown = {n: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in bev) * 1e3, 2)
-                 for q, n in enumerate(names) if n}
-
     total_ms = max_over_ranks(ws, sum(step_ms))
-    total_e2e = max_over_ranks(ws, sum(e2e_ms))
     counts = wl.active_counts()
     nact = [counts[i % N_SETS] for i in range(K)]
     ffn_bytes = [wl.ffn_bytes(n) for n in nact]
@@ -658,7 +668,7 @@ def run_ours(args, ws, rank, local):
     achieved = sum(ffn_bytes) / (sum(ffn_ms) * 1e-3) / 1e9
     value = job_throughput(ws, T, K, total_ms)
     res = {
-        "metric": "MoE-layer tokens/s (decode, V4.1 shape, T=8) + expert HBM GB/s, % roofline",
+        "metric": f"MoE-layer tokens/s (decode, V4.1 shape, T={T}) + expert HBM GB/s, % roofline",
         "value": round(value, 1),
         "unit": "tokens/s",
         "n_gpus": ws,
@@ -671,27 +681,42 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": decode_config(T, not args.no_engram, ws),
-        "e2e": {"value": round(job_throughput(ws, T, K, total_e2e), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-        "gpu_launches": K * wl.launches_per_step,
+    }
+    if full:
+        total_e2e = max_over_ranks(ws, sum(e2e_ms))
+        res["e2e"] = {"value": round(job_throughput(ws, T, K, total_e2e), 1), "unit": "tokens/s",
+                      "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes}
+    res["gpu_launches"] = K * wl.launches_per_step
+    traffic = measured_traffic("decode_T8_ffn_traffic", "ffn_decode.cu") if T == 8 else None
+    res.update({
         "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (prep, gate/up, finish, down launches)",
                      "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4),
-                     "traffic": measured_traffic("decode_T8_ffn_traffic", "ffn_decode.cu"),
-                     "peak_source": pk["source"], "bytes_per_launch_avg": int(np.mean(ffn_bytes))},
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "frac_of_8tbs": round(achieved / 8000.0, 4),
+                     "traffic": traffic, "peak_source": pk["source"], "bytes_per_launch_avg": int(np.mean(ffn_bytes))},
         "step_hbm_gbs": round(sum(step_bytes) / (sum(step_ms) * 1e-3) / 1e9, 1),
         "ffn_us_median": round(statistics.median(ffn_ms) * 1e3, 2),
         "step_us_median": round(statistics.median(step_ms) * 1e3, 2),
         "step_us_spread": spread_us(step_ms),
         "ffn_us_spread": spread_us(ffn_ms),
-        "e2e_step_us_spread": spread_us(e2e_ms),
-        "eager_step_us_median": round(statistics.median(eager_ms) * 1e3, 2),
         "active_experts_per_set": counts,
-        "breakdown_us_median_eager": breakdown,
         "clocks": clk,
         "wall_s_timed_loop": round(wall, 3),
-    }
-    return res
+    })
+    if full:
+        eager_ms = timed(lambda i: wl.step(i), min(K, 50), flush, stream)
+        # per-call breakdown (eager, separate pass)
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(min(K, 50))]
+        for i, evs in enumerate(bev):
+            flush_l2(flush)
+            wl.step_breakdown(i, evs)
+        torch.cuda.synchronize()
+        names = ["route_permute", "", "expert_ffn", "combine", "engram"]
+        res["e2e_step_us_spread"] = spread_us(e2e_ms)
+        res["eager_step_us_median"] = round(statistics.median(eager_ms) * 1e3, 2)
+        res["breakdown_us_median_eager"] = {n: round(statistics.median(e[q].elapsed_time(e[q + 1]) for e in bev) * 1e3, 2)
+                                            for q, n in enumerate(names) if n}
+    del graphs, graphs_e2e, flush
+    return res, wl
 
 
 # --------------------------------------------------------------------------- #
@@ -747,6 +772,109 @@ def cpu_baseline(T: int, n_steps: int = 2):
             "sample": f"{n_steps} full decode steps (T={T} MoE layer + Engram gather of the same tokens), "
                       f"single-threaded C oracle, FP64 FFN; expert bytes generated outside the timed part",
             "seconds": round(tot, 2), "host": host_cpu()}
+
+
+def _timed_call(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return r, time.perf_counter() - t0
+
+
+def cpu_baseline_prefill(n_route: int = 1024, n_ffn: int = 32):
+    """The oracle on a bounded sample of the prefill layer (T = 8192, Zipf-skewed routing), single
+    threaded: routing of the first n_route tokens, and the FFN (route + expert FFN + shared expert
+    + combine) on n_ffn tokens chosen to reach every expert those tokens select; each part is
+    scaled to 8192 tokens.  Expert bytes are generated outside the timed parts."""
+    import oracle
+    oracle.build()
+    sh, T = synth.V41_PREFILL, 8192
+    w_r = synth.router_weight(SEED, 0, sh.d, sh.E)
+    bias = synth.route_bias(SEED, 0, sh.E, sh.bias_half_width, sh.zipf)
+    x = synth.x_bf16(SEED, 0, 0, n_route, sh.d)
+    (ids, _), t_route = _timed_call(lambda: oracle.route(x, w_r, bias, sh.k))
+    chosen, seen = [], set()
+    for t in range(n_route):                     # cover every expert the routed sample selects
+        new = set(int(e) for e in ids[t]) - seen
+        if new:
+            chosen.append(t)
+            seen |= new
+    for t in np.linspace(0, n_route - 1, 4 * n_ffn).astype(int):
+        if len(chosen) >= n_ffn:
+            break
+        if int(t) not in chosen:
+            chosen.append(int(t))
+    chosen = sorted(chosen)
+    xs = x[chosen].contiguous()
+    need = sorted(set(int(e) for e in ids[chosen].reshape(-1)))
+    gate, up, down = [None] * sh.E, [None] * sh.E, [None] * sh.E
+    for e in need:
+        gate[e], up[e], down[e] = (synth.expert_matrix(SEED, 0, kd, sh, e, 1)[0].numpy()
+                                   for kd in (synth.S_GATE, synth.S_UP, synth.S_DOWN))
+    shared = tuple(synth.shared_matrix(SEED, 0, kd, sh).numpy() for kd in (synth.S_SGATE, synth.S_SUP, synth.S_SDOWN))
+    _, t_ffn = _timed_call(lambda: oracle.moe_layer(xs, w_r, bias, sh.k, sh.F, gate, up, down, *shared, sh.F_shared))
+    step_s = t_route * T / n_route + t_ffn * T / len(chosen)
+    flops = 2 * 3 * sh.d * sh.F * T * sh.k + 2 * 3 * sh.d * sh.F_shared * T
+    return {"value": round(flops / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"routing of {n_route} tokens (x{T // n_route}) and the layer's FFN on {len(chosen)} tokens "
+                      f"reaching all {len(need)} experts they select (x{T / len(chosen):.0f}); single-threaded C "
+                      f"oracle, FP64 FFN; extrapolated to one T={T} step",
+            "tokens_per_s": round(T / step_s, 3), "extrapolated_step_s": round(step_s, 1),
+            "seconds": round(t_route + t_ffn, 2), "host": host_cpu()}
+
+
+def cpu_baseline_verify(sample_layers=(0, 12, 23)):
+    """The oracle on a bounded sample of the 24-layer verify pass (T = 5): the MoE layer, the
+    residual update and the next norm of three of the 24 layers, each on the normalised first token
+    set, single threaded; the mean per layer is scaled to 24 layers.  Expert bytes are generated
+    outside the timed parts."""
+    import oracle
+    oracle.build()
+    sh, T, L = synth.V41, 5, 24
+    x0 = synth.x_bf16(SEED, 0, 500, T, sh.d)
+    to_bf16 = lambda u16: torch.from_numpy(u16.astype(np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+    u = to_bf16(oracle.rmsnorm(x0, 1e-6))
+    scale = float(np.float32(1.0 / math.sqrt(2.0)))
+    per_layer = []
+    for l in sample_layers:
+        w_r = synth.router_weight(SEED, l, sh.d, sh.E)
+        bias = synth.route_bias(SEED, l, sh.E, sh.bias_half_width)
+        ids, _ = oracle.route(u, w_r, bias, sh.k)
+        gate, up, down = [None] * sh.E, [None] * sh.E, [None] * sh.E
+        for e in sorted(set(int(v) for v in ids.reshape(-1))):
+            gate[e], up[e], down[e] = (synth.expert_matrix(SEED, l, kd, sh, e, 1)[0].numpy()
+                                       for kd in (synth.S_GATE, synth.S_UP, synth.S_DOWN))
+        shared = tuple(synth.shared_matrix(SEED, l, kd, sh).numpy() for kd in (synth.S_SGATE, synth.S_SUP, synth.S_SDOWN))
+
+        def one():
+            r = oracle.moe_layer(u, w_r, bias, sh.k, sh.F, gate, up, down, *shared, sh.F_shared)
+            xn = oracle.residual(x0, to_bf16(r["out"]), scale)
+            oracle.rmsnorm(to_bf16(xn), 1e-6)
+        per_layer.append(_timed_call(one)[1])
+    pass_s = statistics.mean(per_layer) * L
+    return {"value": round(pass_s * 1e6, 1), "unit": "us/pass", "cores": 1, "kind": "oracle",
+            "sample": f"layers {list(sample_layers)} of {L} (MoE layer + residual + norm, T={T}), mean x{L}; "
+                      "single-threaded C oracle, FP64 FFN",
+            "seconds": round(sum(per_layer), 2), "host": host_cpu()}
+
+
+def cpu_baseline_engram():
+    """The oracle on the whole Engram configuration (T = 8192 x 2 tables x 8 heads), single threaded.
+    The rows the ids reach are generated outside the timed part (the tables are not materialised
+    on the host)."""
+    import oracle
+    oracle.build()
+    T = 8192
+    ids = synth.engram_ids_ngram(SEED + 0, T, 2, ENGRAM_H, ENGRAM_ROWS)   # the first id set of the GPU run
+    tabs, remap = [], np.empty_like(ids)
+    for tau in range(2):
+        u, inv = np.unique(ids[:, tau, :], return_inverse=True)
+        tabs.append(synth.engram_rows_at(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), torch.from_numpy(u)).numpy())
+        remap[:, tau, :] = inv.reshape(T, ENGRAM_H)
+    _, t = _timed_call(lambda: oracle.engram_gather(tabs, remap))
+    alg = T * 2 * ENGRAM_H * 264 + T * 2 * ENGRAM_H * 8 + T * 512 * 2
+    return {"value": round(alg / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole configuration (T={T}, 2 tables x {ENGRAM_H} heads), single-threaded C oracle",
+            "seconds": round(t, 3), "host": host_cpu()}
 
 
 def host_cpu():
@@ -812,6 +940,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-engram", action="store_true",
                     help="leave the Engram gather out of the step (smaller device footprint, for profiling)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="decode line only: leave out the sub-records (decode T=1,2,4, prefill, Engram, verify)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -828,10 +958,37 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    res = run_ours(args, ws, rank, local)
+    res, wl = run_ours(args, ws, rank, local)
+    sub = {}
+    if not args.no_sub:
+        # the rest of the metric, each record timed the same way with its own clock record: decode
+        # at the other batch sizes, the prefill layer, the Engram gather at scale, the verify pass
+        for T in (1, 2, 4):
+            if T != args.T:
+                sub[f"decode_T{T}"], _ = run_ours(args, ws, rank, local, T=T, lw=wl.lw, tables=wl.tables, full=False)
+        sub["prefill_T8192"] = run_prefill(args, ws, rank, local, lw=wl.lw)
+        torch.cuda.empty_cache()
+        sub["engram_T8192"] = run_engram(args, ws, rank, local, tables=wl.tables)
+        lw0 = wl.lw
+        del wl
+        torch.cuda.empty_cache()
+        sub["verify_T5_24layers"] = run_verify(args, ws, rank, local, lw0=lw0)
+        del lw0
+        torch.cuda.empty_cache()
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             res["cpu_baseline"] = cpu_baseline(args.T)
+            for key, rec in sub.items():
+                if key.startswith("decode_T"):
+                    rec["cpu_baseline"] = cpu_baseline(int(key[len("decode_T"):]), n_steps=1)
+            if "prefill_T8192" in sub:
+                sub["prefill_T8192"]["cpu_baseline"] = cpu_baseline_prefill()
+            if "engram_T8192" in sub:
+                sub["engram_T8192"]["cpu_baseline"] = cpu_baseline_engram()
+            if "verify_T5_24layers" in sub:
+                sub["verify_T5_24layers"]["cpu_baseline"] = cpu_baseline_verify()
+        if sub:
+            res["sub_records"] = sub
         print(json.dumps(res), flush=True)
     if ws > 1:
         import torch.distributed as dist
