@@ -486,14 +486,15 @@ def test_layer_prefill_every_m_tile_sampled(cuda_dev):
     perm = info["perm"].cpu().numpy()
     k = shape.k
     chosen = set()
+    n_group_tiles = 0
     for e in range(shape.E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         for m, start in enumerate(range(lo, hi, 256)):
             n = min(256, hi - start)
             chosen.add(int(perm[start + (37 * m + 11) % n]) // k)
+            n_group_tiles += 1
         if hi > lo:
             chosen.add(int(perm[hi - 1]) // k)
-    n_group_tiles = len(chosen)
     for m in range(T // 256):                       # the shared expert's M tiles (all tokens)
         chosen.add(256 * m + (53 * m) % 256)
     sample = np.array(sorted(chosen))
