@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from bit_routed_expert_gb300 import api, synth  # noqa: E402
-from bit_routed_expert_gb300.api import BRE_FMT_Q2_K, BRE_FMT_Q8_0, FfnWeights, MoeLayer  # noqa: E402
+from bit_routed_expert_gb300.api import BRE_FMT_Q8_0, FfnWeights, MoeLayer  # noqa: E402
 
 SEED = 1
 ENGRAM_ROWS = 4194304
@@ -188,18 +188,21 @@ def job_throughput(ws: int, units_per_rank: float, steps: int, total_ms_max: flo
 class DecodeWorkload:
     """MoE layer at the V4.1 decode shape (T tokens) + Engram gather of the same tokens."""
 
-    def __init__(self, dev, T: int, rank: int, engram: bool = True, lw=None, tables=None):
-        """lw / tables: the layer's weights and the Engram tables of another workload, reused
-        (the same seeded bytes) so that other batch sizes need no second copy."""
+    def __init__(self, dev, T: int, rank: int, engram: bool = True, lw=None, tables=None, routed=None):
+        """lw / routed / tables: the layer's weights (the routed experts already regrouped into the
+        Q2_K_R16 layout) and the Engram tables of another workload, reused (the same seeded bytes)
+        so that other batch sizes need no second copy."""
         self.dev, self.T = dev, T
         self.engram = engram
         self.shape = synth.V41
         sh = self.shape
         if lw is None:
             lw = synth.layer_weights(SEED, 0, sh, device=dev)
-        self.lw = lw
-        self.layer = MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d,
-                                                                          sh.F),
+        if routed is None:
+            routed = api.routed_weights(lw.gate, lw.up, lw.down, sh.d, sh.F)
+            lw.gate = lw.up = lw.down = None          # the Q2_K copies are not needed on the device
+        self.lw, self.routed = lw, routed
+        self.layer = MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), routed,
                               FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
         if engram and tables is None:
             tables = [synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE, 0, tau), ENGRAM_ROWS, device=dev)
@@ -367,15 +370,17 @@ def layer_breakdown(layer, xs, out, n, flush):
     return bd
 
 
-def run_prefill(args, ws, rank, local, lw=None):
+def run_prefill(args, ws, rank, local, lw=None, routed=None):
     """One MoE layer at T = 8192 with Zipf(1.1)-skewed routing (grouped GEMM on tcgen05).
-    lw: the decode layer's weights (the same seeded experts), reused with the skewed bias."""
+    lw, routed: the decode layer's weights (the same seeded experts), reused with the skewed bias."""
     dev = torch.device("cuda", local)
     sh, T = synth.V41_PREFILL, 8192
     if lw is None:
         lw = synth.layer_weights(SEED, 0, sh, device=dev)
+    if routed is None:
+        routed = api.routed_weights(lw.gate, lw.up, lw.down, sh.d, sh.F)
     bias = synth.route_bias(SEED, 0, sh.E, sh.bias_half_width, sh.zipf)
-    layer = MoeLayer(lw.w_r.to(dev), bias.to(dev), FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
+    layer = MoeLayer(lw.w_r.to(dev), bias.to(dev), routed,
                      FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T)
     xs = [synth.x_bf16(SEED + 1000 * rank, 0, s, T, sh.d).to(dev) for s in range(2)]
     out = torch.empty((T, sh.d), dtype=torch.bfloat16, device=dev)
@@ -418,16 +423,20 @@ def run_prefill(args, ws, rank, local, lw=None):
             "breakdown_us_median": bd, "clocks": clk}
 
 
-def run_verify(args, ws, rank, local, lw0=None):
+def run_verify(args, ws, rank, local, lw0=None, routed0=None):
     """Speculative-verify batch: T = 5 rows through 24 MoE layers (76 GB of experts resident).
-    lw0: layer 0's weights when already resident (the decode layer is layer 0)."""
+    lw0, routed0: layer 0's weights when already resident (the decode layer is layer 0)."""
     dev = torch.device("cuda", local)
     sh, T, L = synth.V41, 5, 24
     layers = []
     for l in range(L):
-        lw = lw0 if (l == 0 and lw0 is not None) else synth.layer_weights(SEED, l, sh, device=dev)
-        layers.append(MoeLayer(lw.w_r.to(dev), lw.bias.to(dev),
-                               FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, sh.d, sh.F),
+        if l == 0 and lw0 is not None:
+            lw, routed = lw0, routed0
+        else:
+            lw = synth.layer_weights(SEED, l, sh, device=dev)
+            routed = api.routed_weights(lw.gate, lw.up, lw.down, sh.d, sh.F)
+            lw.gate = lw.up = lw.down = None
+        layers.append(MoeLayer(lw.w_r.to(dev), lw.bias.to(dev), routed,
                                FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, sh.d, sh.F_shared), sh.k, T))
     stack = api.MoeStack(layers)
     xs = [synth.x_bf16(SEED + 1000 * rank, 0, 500 + s, T, sh.d).to(dev) for s in range(N_SETS)]
@@ -615,14 +624,14 @@ def run_engram_gate(args, ws, rank, local):
             "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms), "clocks": clk}
 
 
-def run_ours(args, ws, rank, local, T=None, lw=None, tables=None, full=True):
+def run_ours(args, ws, rank, local, T=None, lw=None, tables=None, routed=None, full=True):
     """The decode step at batch T (default --T): graph replays of the whole step, the same step
     end to end with its host copies (full=True), and the expert FFN call alone for the roofline.
     full=False (the other decode batch sizes) leaves out the end-to-end loop and the per-call
     breakdown.  Returns (record, workload)."""
     dev = torch.device("cuda", local)
     T = args.T if T is None else T
-    wl = DecodeWorkload(dev, T, rank, engram=not args.no_engram, lw=lw, tables=tables)
+    wl = DecodeWorkload(dev, T, rank, engram=not args.no_engram, lw=lw, tables=tables, routed=routed)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):
@@ -965,15 +974,16 @@ def main():
         # at the other batch sizes, the prefill layer, the Engram gather at scale, the verify pass
         for T in (1, 2, 4):
             if T != args.T:
-                sub[f"decode_T{T}"], _ = run_ours(args, ws, rank, local, T=T, lw=wl.lw, tables=wl.tables, full=False)
-        sub["prefill_T8192"] = run_prefill(args, ws, rank, local, lw=wl.lw)
+                sub[f"decode_T{T}"], _ = run_ours(args, ws, rank, local, T=T, lw=wl.lw, tables=wl.tables,
+                                                  routed=wl.routed, full=False)
+        sub["prefill_T8192"] = run_prefill(args, ws, rank, local, lw=wl.lw, routed=wl.routed)
         torch.cuda.empty_cache()
         sub["engram_T8192"] = run_engram(args, ws, rank, local, tables=wl.tables)
-        lw0 = wl.lw
+        lw0, routed0 = wl.lw, wl.routed
         del wl
         torch.cuda.empty_cache()
-        sub["verify_T5_24layers"] = run_verify(args, ws, rank, local, lw0=lw0)
-        del lw0
+        sub["verify_T5_24layers"] = run_verify(args, ws, rank, local, lw0=lw0, routed0=routed0)
+        del lw0, routed0
         torch.cuda.empty_cache()
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:

@@ -13,7 +13,7 @@ _lib = None
 
 BRE_OK, BRE_ERR_ARG, BRE_ERR_UNSUPPORTED, BRE_ERR_CUDA, BRE_ERR_WORKSPACE = range(5)
 BRE_DEVERR_EXPERT_ID, BRE_DEVERR_ROW_ID, BRE_DEVERR_TIMEOUT = 1, 2, 4
-BRE_FMT_Q2_K, BRE_FMT_Q8_0 = 1, 2
+BRE_FMT_Q2_K, BRE_FMT_Q8_0, BRE_FMT_Q2_K_R16 = 1, 2, 3
 
 # exported symbol -> (restype, argtypes)
 _P, _I, _I64, _SZ, _F = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
@@ -33,6 +33,7 @@ SIGNATURES = {
     "moe_residual_norm": (_I, [_P, _P, _I, _I, _F, _F, _P, _P, _P]),
     "engram_gather_decode": (_I, [_P, _P, _I, _P, _I, _I, _P, _P, _P]),
     "bre_dequant": (_I, [_I, _P, _I64, _P, _P]),
+    "bre_repack_q2k_r16": (_I, [_P, _P, _I, _I, _I, _I64, _I64, _P]),
 }
 
 

@@ -12,7 +12,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import BRE_FMT_Q2_K, BRE_FMT_Q8_0, BreWeights, check, ptr, stream_handle
+from ._lib import BRE_FMT_Q2_K, BRE_FMT_Q2_K_R16, BRE_FMT_Q8_0, BreWeights, check, ptr, stream_handle
 
 
 def _dev(t: torch.Tensor, name: str):
@@ -42,6 +42,25 @@ class FfnWeights:
         return BreWeights(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(), self.fmt, n, self.d,
                           self.d_ff, self.gate[0].numel() if n > 1 else 0, self.up[0].numel() if n > 1 else 0,
                           self.down[0].numel() if n > 1 else 0)
+
+
+def repack_q2k_r16(blocks, stream=None):
+    """Q2_K matrices, uint8 [n, rows, row_bytes] or [rows, row_bytes] on the device -> a new tensor of
+    the same shape holding the Q2_K_R16 layout the expert FFN reads (bre_repack_q2k_r16)."""
+    L = _lib.load()
+    t = _dev(blocks, "blocks")
+    n, rows, rb = (1, t.shape[0], t.shape[1]) if t.dim() == 2 else tuple(t.shape)
+    out = torch.empty_like(t)
+    stride = rows * rb
+    check(L.bre_repack_q2k_r16(ptr(t), ptr(out), n, rows, (rb // 84) * 256, stride, stride, stream_handle(stream)),
+          "bre_repack_q2k_r16")
+    return out
+
+
+def routed_weights(gate, up, down, d: int, d_ff: int) -> FfnWeights:
+    """Routed experts given as Q2_K matrices (gate/up [E, d_ff, d/256*84], down [E, d, d_ff/256*84],
+    uint8 on the device), regrouped once into the Q2_K_R16 layout moe_expert_ffn takes."""
+    return FfnWeights(repack_q2k_r16(gate), repack_q2k_r16(up), repack_q2k_r16(down), BRE_FMT_Q2_K_R16, d, d_ff)
 
 
 def moe_route_workspace(T: int, E: int) -> int:

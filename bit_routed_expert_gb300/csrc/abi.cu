@@ -118,7 +118,7 @@ bre_status moe_expert_ffn(const bre_ffn_weights* routed, const bre_ffn_weights* 
                           int32_t* dev_err, bre_stream_t stream) {
   if (!routed || !x_bf16 || !offsets || !perm || !active || !n_active || !y_pairs || T <= 0 || k <= 0)
     return BRE_ERR_ARG;
-  if (!weights_ok(routed, BRE_FMT_Q2_K)) return BRE_ERR_ARG;
+  if (!weights_ok(routed, BRE_FMT_Q2_K_R16)) return BRE_ERR_ARG;
   if (shared && (!weights_ok(shared, BRE_FMT_Q8_0) || shared->n_experts != 1 || !y_shared)) return BRE_ERR_ARG;
   if (!aligned(x_bf16, 16) || !aligned(y_pairs, 16) || (y_shared && !aligned(y_shared, 16))) return BRE_ERR_ARG;
   bre_status st = ffn_check_shapes(routed, shared, T);
@@ -188,6 +188,18 @@ bre_status engram_inject(const uint8_t* table, int64_t n_rows, const int64_t* ro
   return cuda_status(launch_engram_inject(table, n_rows, row_ids, R, static_cast<const uint16_t*>(w_kv_bf16), W,
                                           static_cast<uint16_t*>(resid_bf16), q_norm, k_norm, mask, T, eps, kv_out,
                                           gate_out, dev_err, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status bre_repack_q2k_r16(const void* src, void* dst, int n_matrices, int rows, int cols, int64_t src_stride,
+                              int64_t dst_stride, bre_stream_t stream) {
+  if (!src || !dst || n_matrices <= 0 || rows <= 0 || cols <= 0) return BRE_ERR_ARG;
+  if (rows % 16 || cols % 256) return BRE_ERR_UNSUPPORTED;
+  const int64_t bytes = (int64_t)rows * (cols / 256) * 84;
+  if (n_matrices > 1 && (src_stride < bytes || dst_stride < bytes)) return BRE_ERR_ARG;
+  if (!aligned(src, 16) || !aligned(dst, 16) || src_stride % 16 || dst_stride % 16) return BRE_ERR_ARG;
+  return cuda_status(launch_repack_q2k_r16(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), n_matrices,
+                                           rows, cols, n_matrices > 1 ? src_stride : bytes,
+                                           n_matrices > 1 ? dst_stride : bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bre_status bre_dequant(int fmt, const void* blocks, int64_t n_blocks, float* out, bre_stream_t stream) {

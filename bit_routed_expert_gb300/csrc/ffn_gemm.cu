@@ -33,6 +33,7 @@ constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
 constexpr int G_THREADS = 512;
 constexpr int G_PRODUCERS = 256;   // B-producer threads (warps 4-11)
 constexpr int G_MAX_GROUPS = 1025;
+constexpr int R16_BYTES = 1344;   // one Q2_K_R16 tile: 16 rows x one 256-weight block
 constexpr long long G_WAIT = 4000000000LL;   // cycles before a wait gives up (~2 s)
 
 // plan: per group g (routed active experts in order, then the shared expert):
@@ -186,24 +187,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // B producers: one weight row, one K step (64 values) -> 8 swizzled 16-byte chunks
 // ---------------------------------------------------------------------------
+// One row's quarter (64 values, sub-blocks 4kq .. 4kq+3) of a Q2_K_R16 block: the scale and
+// min nibble words of the lane that holds these sub-blocks (shifted so that sub-block
+// 4kq + 2p + h sits at bit 16h + 4p), d | dmin << 16, and the codes in the Q2_K order (word jj:
+// the 16 codes of sub-block 4kq + jj, code c at bits 2c).
 struct RawQ2K {
-  uint32_t sw, dd, q[4];
+  uint32_t s, m, dd, q[4];
 };
 
-// A whole Q2_K block of one row (21 words: scales, codes, d and dmin); the producers hold the
-// next block while dequantising the current one, so the load has four K steps to land.
+// A whole Q2_K_R16 block of one row as the producers hold it (25 words): the codes of the row's
+// four lanes (words 4kq .. 4kq+3: lane 4g + kq's words W(p, w) at 2p + w), the lanes' scale and
+// min words (2kq, 2kq + 1 at 16 + ...), and d | dmin << 16.  The producers hold the next block
+// while dequantising the current one, so the load has four K steps to land.
 struct RawBlk {
-  uint32_t w[21];
+  uint32_t c[16];
+  uint32_t sm[8];
+  uint32_t dd;
 };
 
-
-// The quarter kq (64 values, sub-blocks 4kq .. 4kq+3) of a held block.
-__device__ __forceinline__ RawQ2K quarter(const RawBlk& b, int kq) {
+// The quarter kq of a held block of row 8 rr + g.
+__device__ __forceinline__ RawQ2K quarter(const RawBlk& b, int kq, int rr) {
   RawQ2K r;
-  r.sw = b.w[kq];
-  r.dd = b.w[20];
+  r.s = b.sm[2 * kq] >> (8 * rr);
+  r.m = b.sm[2 * kq + 1] >> (8 * rr);
+  r.dd = b.dd;
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) r.q[jj] = b.w[4 + 4 * kq + jj];
+  for (int pp = 0; pp < 2; ++pp) {
+    // W(p, 0) holds codes 0..7 and W(p, 1) codes 8..15 of sub-blocks 4kq + 2p (low halves) and
+    // 4kq + 2p + 1 (high halves)
+    const uint32_t w0 = b.c[4 * kq + 2 * pp], w1 = b.c[4 * kq + 2 * pp + 1];
+    r.q[2 * pp] = prmt(w0, w1, 0x5410u);
+    r.q[2 * pp + 1] = prmt(w0, w1, 0x7632u);
+  }
   return r;
 }
 
@@ -225,9 +240,9 @@ __device__ __forceinline__ void store_q2k_row(const RawQ2K& r, unsigned char* b_
   const int sw = row & 7;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    const uint32_t sb = r.sw >> (8 * jj);
+    const int sh = 16 * (jj & 1) + 4 * (jj >> 1);
     uint32_t lo, hi;
-    q2k_lut(d, dmin, sb & 15u, (sb >> 4) & 15u, lo, hi);
+    q2k_lut(d, dmin, (r.s >> sh) & 15u, (r.m >> sh) & 15u, lo, hi);
     const uint32_t w = r.q[jj];
     const uint32_t c0 = w & 0x03030303u, c1 = (w >> 2) & 0x03030303u;
     const uint32_t c2 = (w >> 4) & 0x03030303u, c3 = (w >> 6) & 0x03030303u;
@@ -435,34 +450,52 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int pw = warp - 4;
       unsigned char* stg = stage_raw + pw * 32 * Q2K_BB;
       if (ti.expert >= 0) {
-        const int rb = (p.K_r / 256) * Q2K_BB;
-        const uint8_t* row;
-        if (PHASE == 1)
-          row = (i < 128) ? p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 128 + i) * rb
-                          : p.r1 + (long long)ti.expert * p.rs1 + (long long)(ti.nt * 128 + i - 128) * rb;
-        else
-          row = p.r0 + (long long)ti.expert * p.rs0 + (long long)(ti.nt * 256 + i) * rb;
-        // Whole blocks (4 K steps each) reach the warp's staging area by coalesced copies: lanes
-        // 0..20 copy the 21 words of one row per instruction (a row pointer that advances by the
-        // row pitch), 32 rows per warp, which never straddle the gate / up boundary.  Each thread
-        // then reads its row into registers, and the copy of the next block runs while this one
-        // is dequantised.
+        // Q2_K_R16: the warp's 32 rows are two 16-row tiles; each block of them is two
+        // 1344-byte tiles, copied whole into the warp's staging area by 16-byte cp.async
+        // (84 pieces a tile), then each thread takes its row's words
+        const int nb = p.K_r / 256;
+        const uint8_t* mat;
+        int r_mat;   // this thread's row within its matrix
+        if (PHASE == 1) {
+          mat = (i < 128) ? p.r0 + (long long)ti.expert * p.rs0 : p.r1 + (long long)ti.expert * p.rs1;
+          r_mat = ti.nt * 128 + (i & 127);
+        } else {
+          mat = p.r0 + (long long)ti.expert * p.rs0;
+          r_mat = ti.nt * 256 + i;
+        }
+        const long long rt0 = (r_mat - lane) >> 4;   // the warp's first row tile
+        const int tau = lane >> 4, R = lane & 15, g8 = R & 7, rr = R >> 3;
         const int NBK = KS / 4;
-        const uint8_t* pr0 = row - (long long)lane * rb + 4 * lane;   // row 32*pw of the tile
         auto stage_copy = [&](int blk) {
-          if (lane < 21) {
-            const uint8_t* pr = pr0 + blk * Q2K_BB;
-            unsigned char* dst = stg + 4 * lane;
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) cp_async4(dst + r * Q2K_BB, pr + (long long)r * rb, 4);
+#pragma unroll
+          for (int c = lane; c < 2 * (R16_BYTES / 16); c += 32) {
+            const int tt = c >= R16_BYTES / 16 ? 1 : 0;
+            const int off = (c - tt * (R16_BYTES / 16)) * 16;
+            cp_async16(stg + tt * R16_BYTES + off, mat + ((rt0 + tt) * nb + blk) * R16_BYTES + off, 16);
           }
           cp_async_commit();
         };
         auto stage_read = [&](RawBlk& a) {
           cp_async_wait<0>();
           __syncwarp();
+          const unsigned char* u = stg + tau * R16_BYTES;
 #pragma unroll
-          for (int w = 0; w < 21; ++w) a.w[w] = *reinterpret_cast<const uint32_t*>(stg + lane * Q2K_BB + 4 * w);
+          for (int v = 0; v < 4; ++v) {
+            const uint4 cw = *reinterpret_cast<const uint4*>(u + rr * 512 + 64 * g8 + 16 * v);
+            a.c[4 * v] = cw.x;
+            a.c[4 * v + 1] = cw.y;
+            a.c[4 * v + 2] = cw.z;
+            a.c[4 * v + 3] = cw.w;
+          }
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const uint4 sw4 = *reinterpret_cast<const uint4*>(u + 1024 + 32 * g8 + 16 * v);
+            a.sm[4 * v] = sw4.x;
+            a.sm[4 * v + 1] = sw4.y;
+            a.sm[4 * v + 2] = sw4.z;
+            a.sm[4 * v + 3] = sw4.w;
+          }
+          a.dd = *reinterpret_cast<const uint32_t*>(u + 1280 + 8 * g8 + 4 * rr);
           __syncwarp();
         };
         RawBlk ca;
@@ -478,7 +511,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
               ok = false;
               break;
             }
-            store_q2k_row(quarter(ca, kq), b_st + s * G_B_BYTES, i);
+            store_q2k_row(quarter(ca, kq, rr), b_st + s * G_B_BYTES, i);
             fence_proxy_async_smem();
             mbar_arrive(&full[s]);
           }

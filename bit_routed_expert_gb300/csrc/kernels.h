@@ -72,6 +72,9 @@ cudaError_t launch_combine(const float* y_pairs, const float* topk_w, const int3
 cudaError_t launch_residual_norm(const uint16_t* x, const uint16_t* moe, int T, int d, float scale, float eps,
                                  uint16_t* x_out, uint16_t* u_out, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t n_blocks, float* out, cudaStream_t s);
+// Q2_K [n_mat][rows][cols/256 blocks] -> Q2_K_R16 (repack.cu)
+cudaError_t launch_repack_q2k_r16(const uint8_t* src, uint8_t* dst, long long n_mat, int rows, int cols,
+                                  long long src_stride, long long dst_stride, cudaStream_t s);
 
 // tiled tensor map over global memory: dims innermost first, strides (bytes) of dims 1..rank-1
 bool encode_tiled(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,

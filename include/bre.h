@@ -59,7 +59,7 @@ typedef enum {
 #define BRE_DEVERR_ROW_ID 2    /* an Engram row id outside [0, n_rows): row decoded as +0 */
 #define BRE_DEVERR_TIMEOUT 4   /* a bounded device wait gave up; outputs of that CTA are invalid */
 
-typedef enum { BRE_FMT_Q2_K = 1, BRE_FMT_Q8_0 = 2 } bre_fmt;
+typedef enum { BRE_FMT_Q2_K = 1, BRE_FMT_Q8_0 = 2, BRE_FMT_Q2_K_R16 = 3 } bre_fmt;
 
 /* One FFN weight set.  gate, up: [n_experts][d_ff][d] and down: [n_experts][d][d_ff]
  * weights, each row stored as consecutive quant blocks along its inner
@@ -67,9 +67,11 @@ typedef enum { BRE_FMT_Q2_K = 1, BRE_FMT_Q8_0 = 2 } bre_fmt;
  * (low nibble scale, high nibble min), uint8 qs[64] (code i in bits
  * 2*(i%4) of qs[i/4]), fp16 d, fp16 dmin; w = d*sc*q - dmin*m for weight i
  * in sub-block i/16.  Q8_0 block (34 B / 32 weights): fp16 d, int8 q[32];
- * w = d*q.  expert_stride_*: bytes from one expert's matrix to the next
- * (ignored when n_experts == 1).  Base pointers and strides must be 16-byte
- * aligned. */
+ * w = d*q.  Q2_K_R16: the same Q2_K blocks regrouped by bre_repack_q2k_r16
+ * into 1344-byte tiles of 16 rows x one block (layout below); the matrix
+ * has the same size.  expert_stride_*: bytes from one expert's matrix to the
+ * next (ignored when n_experts == 1).  Base pointers and strides must be
+ * 16-byte aligned. */
 typedef struct {
   const void *gate;
   const void *up;
@@ -178,14 +180,30 @@ bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *
                              int32_t *active, int32_t *n_active, int32_t *dev_err, void *ws, size_t ws_bytes,
                              bre_stream_t stream);
 
+/* Regroup Q2_K matrices into the Q2_K_R16 tiles the expert FFN reads (a layout of
+ * this library, done once when weights are loaded; the pages' Q2_K block, strix-llama.cpp
+ * issue "Feature Description", is unchanged in content).  src: n_matrices matrices of
+ * [rows][cols/256] Q2_K blocks, src_stride bytes apart; dst: the same number of bytes per
+ * matrix, dst_stride apart, must not overlap src.  Tile (rt, b) of rows 16 rt .. 16 rt + 15 and
+ * block b sits at byte (rt * (cols/256) + b) * 1344 of the matrix; inside a tile, for row
+ * 8 rr + g (g < 8) and lane L = 4 g + t (t < 4):
+ *   [512 rr + 16 L, +16): four words W(p, w) (p, w in {0,1}, at word 2p + w); bits 16h + 2s
+ *     of W(p, w) hold code 8w + s (s < 8) of sub-block 4t + 2p + h (h in {0, 1}) of the row;
+ *   [1024 + 8 L, +8): two words, the scales then the mins of sub-blocks 4t .. 4t+3 of rows g
+ *     and g + 8: the nibble of (row 8 rr + g, sub-block 4t + 2p + h) at bit 16h + 4 (2 rr + p);
+ *   [1280 + 8 g + 4 rr, +4): fp16 d then fp16 dmin of row 8 rr + g.
+ * Requires rows % 16 == 0, cols % 256 == 0, pointers and strides 16-byte aligned. */
+bre_status bre_repack_q2k_r16(const void *src, void *dst, int n_matrices, int rows, int cols, int64_t src_stride,
+                              int64_t dst_stride, bre_stream_t stream);
+
 /* Routed expert FFN plus the always-on shared expert ([S] V4-Flash "How it
  * works", finish step; "Verifying it"): for every active expert e and each of
  * its pairs p (token t = p / k):
  *   h = silu(gate_e . x_t) * (up_e . x_t);  y_pairs[inv[p]] = down_e . h
  * and for the shared expert (weight 1) on every token: y_shared[t].  No
  * SwiGLU clamp.  Weights are dequantised exactly; accumulation is FP32.
- *   routed: fmt BRE_FMT_Q2_K, n_experts = E.  shared: fmt BRE_FMT_Q8_0,
- *   n_experts = 1, or NULL (then y_shared is not written).
+ *   routed: fmt BRE_FMT_Q2_K_R16 (bre_repack_q2k_r16 of the Q2_K experts), n_experts = E.
+ *   shared: fmt BRE_FMT_Q8_0, n_experts = 1, or NULL (then y_shared is not written).
  *   x_bf16 [T][d]; offsets/perm/active/n_active from moe_permute (k pairs per
  *   token); y_pairs [T*k][d] FP32 out, row q = permuted position q (rows of
  *   pairs with an invalid id are not written); y_shared [T][d] FP32 out.
@@ -196,9 +214,7 @@ bre_status moe_route_permute(const void *x_bf16, const float *w_r, const float *
  *   must not overlap any buffer of the call enqueued just before this one on the
  *   stream (for T <= 8 its first kernel packs x into the workspace while a
  *   preceding moe_route_permute may still be running; it reads only x_bf16).
- * Shapes: d and d_ff multiples of 256; for T <= 8 each of d, d_ff either
- * <= 1024 or a multiple of 1024 (Q2_K rows reach shared memory as whole
- * 16-row tiles or as 4-block tensor-copy pieces with a 16-byte row pitch). */
+ * Shapes: d and d_ff multiples of 256. */
 size_t moe_expert_ffn_workspace(int T, int k, int E, int d, int d_ff, int d_ff_shared);
 bre_status moe_expert_ffn(const bre_ffn_weights *routed, const bre_ffn_weights *shared, const void *x_bf16,
                           int T, int k, const int32_t *offsets, const int32_t *perm, const int32_t *active,

@@ -5,8 +5,8 @@ import numpy as np
 import torch
 
 import oracle
-from bit_routed_expert_gb300 import synth
-from bit_routed_expert_gb300.api import BRE_FMT_Q2_K, BRE_FMT_Q8_0, FfnWeights, MoeLayer
+from bit_routed_expert_gb300 import api, synth
+from bit_routed_expert_gb300.api import BRE_FMT_Q8_0, FfnWeights, MoeLayer
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
@@ -19,7 +19,7 @@ def bits_to_f64(u16: np.ndarray) -> np.ndarray:
 
 def device_layer(seed: int, layer: int, shape: synth.MoeShape, T_max: int, dev, with_shared: bool = True) -> MoeLayer:
     lw = synth.layer_weights(seed, layer, shape, device=dev)
-    routed = FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, shape.d, shape.F)
+    routed = api.routed_weights(lw.gate, lw.up, lw.down, shape.d, shape.F)
     shared = None
     if with_shared and shape.F_shared:
         shared = FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, shape.d, shape.F_shared)

@@ -57,6 +57,59 @@ def test_dequant_q2k_bit_exact(cuda_dev):
     assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
 
 
+def _np_repack_r16(m: np.ndarray) -> np.ndarray:
+    """The Q2_K_R16 layout restated from its definition (bre.h, bre_repack_q2k_r16): m uint8
+    [rows, nb * 84] Q2_K blocks -> [rows / 16, nb, 1344]."""
+    rows, nb = m.shape[0], m.shape[1] // 84
+    blk = m.reshape(rows, nb, 84).astype(np.uint32)
+    qs = blk[:, :, 16:80]
+    codes = np.stack([(qs >> (2 * c)) & 3 for c in range(4)], axis=-1).reshape(rows, nb, 256)
+    out = np.zeros((rows // 16, nb, 1344), dtype=np.uint8)
+    for R in range(16):
+        g, rr = R & 7, R >> 3
+        rsel = np.arange(rows // 16) * 16 + R
+        for t in range(4):
+            L = 4 * g + t
+            for p in range(2):
+                for w in range(2):
+                    word = np.zeros((rows // 16, nb), dtype=np.uint32)
+                    for h in range(2):
+                        j = 4 * t + 2 * p + h
+                        for s_ in range(8):
+                            word |= codes[rsel, :, 16 * j + 8 * w + s_] << (16 * h + 2 * s_)
+                    o = rr * 512 + 16 * L + 4 * (2 * p + w)
+                    out[:, :, o:o + 4] = word[..., None].view(np.uint8).reshape(rows // 16, nb, 4)
+        out[:, :, 1280 + 8 * g + 4 * rr:1280 + 8 * g + 4 * rr + 4] = blk[rsel, :, 80:84].astype(np.uint8)
+    for g in range(8):
+        for t in range(4):
+            L = 4 * g + t
+            scw = np.zeros((rows // 16, nb), dtype=np.uint32)
+            mw = np.zeros((rows // 16, nb), dtype=np.uint32)
+            for rr in range(2):
+                rsel = np.arange(rows // 16) * 16 + 8 * rr + g
+                for p in range(2):
+                    for h in range(2):
+                        j = 4 * t + 2 * p + h
+                        pos = 16 * h + 4 * (2 * rr + p)
+                        scw |= (blk[rsel, :, j] & 15) << pos
+                        mw |= (blk[rsel, :, j] >> 4) << pos
+            out[:, :, 1024 + 8 * L:1024 + 8 * L + 4] = scw[..., None].view(np.uint8).reshape(rows // 16, nb, 4)
+            out[:, :, 1028 + 8 * L:1028 + 8 * L + 4] = mw[..., None].view(np.uint8).reshape(rows // 16, nb, 4)
+    return out
+
+
+@pytest.mark.parametrize("n,rows,cols", [(3, 64, 1024), (1, 16, 256), (2, 48, 512)])
+def test_repack_q2k_r16_layout(cuda_dev, n, rows, cols):
+    """bre_repack_q2k_r16 against the layout's definition, byte for byte; the tiles hold exactly
+    the blocks' bytes (same size, every code, nibble and d/dmin accounted for)."""
+    shape = synth.MoeShape(d=cols, E=n, k=1, F=rows, F_shared=0, bias_half_width=0.1)
+    m = synth.expert_matrix(SEED, 3, synth.S_GATE, shape, 0, n)           # [n, rows, cols/256*84]
+    got = api.repack_q2k_r16(m.to(cuda_dev)).cpu().numpy()
+    for e in range(n):
+        ref = _np_repack_r16(m[e].numpy())
+        assert np.array_equal(got[e].reshape(-1), ref.reshape(-1))
+
+
 def test_dequant_q80_bit_exact(cuda_dev):
     blk = synth.q8_0_blocks(SEED, 98, 0, 20000)
     got = api.bre_dequant(BRE_FMT_Q8_0, blk.to(cuda_dev)).cpu().numpy()
@@ -512,8 +565,7 @@ def test_layer_gemm_tiny_dominant_expert(cuda_dev):
     lw = synth.layer_weights(SEED, 0, shape, device=cuda_dev)
     bias = synth.route_bias(SEED, 0, shape.E, shape.bias_half_width).clone()
     bias[5] += 4.0                                  # sigmoid scores lie in (0, 1): expert 5 always wins
-    layer = MoeLayer(lw.w_r.to(cuda_dev), bias.to(cuda_dev),
-                     FfnWeights(lw.gate, lw.up, lw.down, BRE_FMT_Q2_K, shape.d, shape.F),
+    layer = MoeLayer(lw.w_r.to(cuda_dev), bias.to(cuda_dev), api.routed_weights(lw.gate, lw.up, lw.down, shape.d, shape.F),
                      FfnWeights(lw.sh_gate, lw.sh_up, lw.sh_down, BRE_FMT_Q8_0, shape.d, shape.F_shared), shape.k, T)
     x = synth.x_bf16(SEED, 0, 61, T, shape.d)
     out, of, info = run_layer(layer, x.to(cuda_dev))
