@@ -34,6 +34,7 @@ SIGNATURES = {
     "engram_gather_decode": (_I, [_P, _P, _I, _P, _I, _I, _P, _P, _P]),
     "bre_dequant": (_I, [_I, _P, _I64, _P, _P]),
     "bre_repack_q2k_r16": (_I, [_P, _P, _I, _I, _I, _I64, _I64, _P]),
+    "bre_set_ffn_wait_limit": (_I, [_I64]),
 }
 
 

@@ -1,4 +1,6 @@
 // extern "C" entry points of libbre: host-side argument checks, then the launchers.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "bre.h"
@@ -24,6 +26,13 @@ const DevAttr& attr() {
   return a;
 }
 }  // namespace
+
+std::atomic<long long> g_ffn_wait{0};   // 0: the kernels' default budgets
+
+long long ffn_wait_budget(long long dflt) {
+  const long long v = g_ffn_wait.load(std::memory_order_relaxed);
+  return v > 0 ? v : dflt;
+}
 
 int device_sm_count() { return attr().sms; }
 int device_max_smem_optin() { return attr().smem_optin; }
@@ -188,6 +197,12 @@ bre_status engram_inject(const uint8_t* table, int64_t n_rows, const int64_t* ro
   return cuda_status(launch_engram_inject(table, n_rows, row_ids, R, static_cast<const uint16_t*>(w_kv_bf16), W,
                                           static_cast<uint16_t*>(resid_bf16), q_norm, k_norm, mask, T, eps, kv_out,
                                           gate_out, dev_err, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bre_status bre_set_ffn_wait_limit(int64_t cycles) {
+  if (cycles < 0) return BRE_ERR_ARG;
+  g_ffn_wait.store((long long)cycles, std::memory_order_relaxed);
+  return BRE_OK;
 }
 
 bre_status bre_repack_q2k_r16(const void* src, void* dst, int n_matrices, int rows, int cols, int64_t src_stride,

@@ -110,6 +110,7 @@ struct DecParams {
   int red;                   // phase 2: outputs are sums of two K parts added into zeros
   int* counters;
   int32_t* err;
+  long long wait;            // budget (cycles) of the ring and package waits; drains use WAIT_LIMIT
   DecConst kc;
 };
 
@@ -598,8 +599,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
     return i < n_items ? i : -1;
   };
 
-  // ids of the items whose stages are issued but not yet consumed (at most NS + 1), in three
-  // registers (an indexed array would live in local memory)
+  // ids of the items fetched but not yet taken up for processing, in three registers (an
+  // indexed array would live in local memory): the item being processed leaves the queue when
+  // it is taken up, so the queue holds at most the items with stages in flight (NS, when every
+  // item is one stage) and the one being loaded
   static_assert(NS + 1 <= 3, "item queue holds three ids");
   int q0 = -1, q1 = -1, q2 = -1, qn = 0;
   auto q_push = [&](int v) {
@@ -638,8 +641,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
   // the package in shared memory leaves room for more rings
   const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
   if (PHASE == 1) {
-    if (!mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT)) {
+    if (!mbar_wait_bounded(pkg_bar, 0, p.wait)) {
+      // give up: the package copy and this warp's ring copies land before the warp leaves
       if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
+      mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT);
       for (int q = 0; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
       return;
     }
@@ -650,6 +655,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
   while (true) {
     const int id = q0;
     if (id < 0) break;
+    q_pop();
     const Item it = decode_item<PHASE>(p, id, n_shared_items);
     // column -> token (phase 1) or h row (phase 2)
     auto col_src = [&](int col) -> int {
@@ -682,9 +688,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 
     for (int cc = 0; cc < it.nch; ++cc) {
       const int st = cs_seq % NS;
-      if (!mbar_wait_bounded(&my_bar[st], (cs_seq / NS) & 1, WAIT_LIMIT)) {
+      if (!mbar_wait_bounded(&my_bar[st], (cs_seq / NS) & 1, p.wait)) {
+        // give up: every copy this warp has issued (this stage's included) lands before it leaves
         if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
-        for (int q = cs_seq + 1; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
+        for (int q = cs_seq; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
         return;
       }
       const unsigned char* stage = my_stage + st * STAGE;
@@ -731,7 +738,6 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
       ++cs_seq;
       issue_next();
     }
-    q_pop();
 
     // ---- phase 1 ends an item by storing its FP32 partial sums of one matrix for the expert's
     // real columns; ffn_finish_kernel adds the K parts in order and forms h.  Phase 2 stores y
@@ -1079,6 +1085,7 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   p.xstride = x_stride(p.d);
   p.xlstride = xl_stride(p.d);
   p.kc = DecConst{0x43004300u, 0xC300C300u, 0x46804680u, 0x43434343u};
+  p.wait = ffn_wait_budget(WAIT_LIMIT);
 
   const int sms = device_sm_count();
   const int smem_max = device_max_smem_optin();

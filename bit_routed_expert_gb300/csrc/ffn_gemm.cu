@@ -349,6 +349,7 @@ struct GemmParams {
   int out_ld_r, out_ld_s;
   int out_v8;            // phase 2 outputs 32-byte aligned: 32-byte stores
   int32_t* err;
+  long long wait;        // budget (cycles) of the pipeline's waits; the drains at exit use G_WAIT
 };
 
 struct TileInfo {
@@ -386,11 +387,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   unsigned char* gsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* a_st = gsm;                                   // [G_STAGES][32 KB]
   unsigned char* b_st = gsm + G_STAGES * G_A_BYTES;            // [G_STAGES][32 KB]
-  uint64_t* full = reinterpret_cast<uint64_t*>(b_st + G_STAGES * G_B_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(b_st + G_STAGES * G_B_BYTES);   // B rows stored (producers)
   uint64_t* empty = full + G_STAGES;
   uint64_t* tfull = empty + G_STAGES;
   uint64_t* tempty = tfull + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 1);
+  uint64_t* aful = tempty + 1;             // A tile landed (the TMA alone completes it)
+  uint64_t* drain = aful + G_STAGES;       // every MMA issued so far has completed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   unsigned char* stage_raw = reinterpret_cast<unsigned char*>(full) + 256;   // [8 warps][32 rows][84 B]
 
@@ -398,11 +401,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   pdl_wait();
   if (threadIdx.x == 0) {
     for (int s = 0; s < G_STAGES; ++s) {
-      mbar_init(&full[s], 1 + G_PRODUCERS);
+      mbar_init(&full[s], G_PRODUCERS);
+      mbar_init(&aful[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, 256);
+    mbar_init(drain, 1);
     *abort_flag = 0;
   }
   fence_mbar_init();
@@ -436,14 +441,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int arow = (PHASE == 1) ? ti.a_row0 + ti.mt * G_BM : (ti.expert < 0 ? 0 : ti.a_row0) + ti.mt * G_BM;
       // wait until stage s is free, then (first thread) start its A tile
       auto open_stage = [&](int s, int ks) -> bool {
-        if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, G_WAIT)) {
+        if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, p.wait)) {
           fail();
           return false;
         }
         if (a_loader) {
-          mbar_arrive_expect_tx(&full[s], G_A_BYTES);
-          tma_load_2d(a_st + s * G_A_BYTES, amap, ks * G_BK, arow, &full[s]);
-          tma_load_2d(a_st + s * G_A_BYTES + G_A_BYTES / 2, amap, ks * G_BK, arow + 128, &full[s]);
+          mbar_arrive_expect_tx(&aful[s], G_A_BYTES);
+          tma_load_2d(a_st + s * G_A_BYTES, amap, ks * G_BK, arow, &aful[s]);
+          tma_load_2d(a_st + s * G_A_BYTES + G_A_BYTES / 2, amap, ks * G_BK, arow + 128, &aful[s]);
         }
         return true;
       };
@@ -558,6 +563,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         cp_async_wait<0>();   // no copy stays in flight past the tile
       }
     }
+    // the A tiles this thread started have landed before the CTA can exit (after an abort the
+    // MMA thread may not have consumed the last ones): the last phase armed on each stage
+    if (a_loader) {
+      for (int q = it - G_STAGES < 0 ? 0 : it - G_STAGES; q < it; ++q)
+        mbar_wait_bounded(&aful[q % G_STAGES], (q / G_STAGES) & 1, G_WAIT);
+    }
   } else {
     // ---------------- MMA issue (warp 0, lane 0) and epilogue (warps 0-3 and 12-15: tensor-memory
     // lanes 32*(warp & 3) .. +31, column half warp >= 12)
@@ -570,13 +581,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (warp == 0 && lane == 0) {
         const int KS = ti.K / G_BK;
         // the previous tile's epilogue has drained the accumulators
-        if (!mbar_wait_bounded(tempty, (tcount & 1) ^ 1, G_WAIT)) {
+        if (!mbar_wait_bounded(tempty, (tcount & 1) ^ 1, p.wait)) {
           fail();
         } else {
           tc_fence_after();
           for (int ks = 0; ks < KS; ++ks, ++it) {
             const int s = it % G_STAGES;
-            if (!mbar_wait_bounded(&full[s], (it / G_STAGES) & 1, G_WAIT)) {
+            if (!mbar_wait_bounded(&full[s], (it / G_STAGES) & 1, p.wait) ||
+                !mbar_wait_bounded(&aful[s], (it / G_STAGES) & 1, p.wait)) {
               fail();
               break;
             }
@@ -597,8 +609,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
       }
       __syncwarp();
-      if (!mbar_wait_bounded(tfull, tcount & 1, G_WAIT)) { fail(); break; }
+      if (!mbar_wait_bounded(tfull, tcount & 1, p.wait)) { fail(); break; }
       tc_fence_after();
+      if (aborted()) break;   // the accumulators may hold a partial sum: nothing is stored
       const int q4 = lane >> 2, p4 = lane & 3;
       const int eq = warp & 3, part = warp >> 3;   // lane quarter, column half
 #pragma unroll 1
@@ -653,6 +666,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       tc_fence_before();
       mbar_arrive(tempty);
     }
+    // every MMA this CTA issued has completed before its tensor memory is freed
+    if (warp == 0 && lane == 0) {
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, G_WAIT);
+    }
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -731,6 +750,7 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 
   GemmParams g{};
+  g.wait = ffn_wait_budget(G_WAIT);
   g.plan = plan;
   g.err = a.err;
   // phase 1: gate/up -> h

@@ -98,6 +98,11 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Budget (SM clock cycles) of the expert FFN kernels' pipeline waits: the value set by
+// bre_set_ffn_wait_limit, or dflt when none is set.  The waits that drain a kernel's own copies
+// before it exits always use the default budget.
+long long ffn_wait_budget(long long dflt);
+
 // device attributes (cached per device)
 int device_sm_count();
 int device_max_smem_optin();

@@ -277,6 +277,18 @@ bre_status engram_inject(const uint8_t *table, int64_t n_rows, const int64_t *ro
                          float eps, float *kv_out, float *gate_out, int32_t *dev_err, void *ws, size_t ws_bytes,
                          bre_stream_t stream);
 
+/* Budget, in SM clock cycles, of the bounded waits inside the expert FFN kernels
+ * (moe_expert_ffn, both paths) for calls made after this one, from any thread of the process;
+ * 0 restores the defaults (about 1 s on the decode path, 2 s on the grouped-GEMM path).  A wait
+ * that runs out sets BRE_DEVERR_TIMEOUT in the call's dev_err; the kernel then waits, with the
+ * default budget, for the copies and tensor-core operations it has in flight, frees its tensor
+ * memory and returns, and that call's outputs are invalid.  The workspace's counters are
+ * restored by the same call's later launches, so the next call on the same workspace needs
+ * nothing done to it.  A small budget exercises that path (the ROCm cached-expert notes of the
+ * strix-llama.cpp issue: errors surface after synchronisation rather than as a trap); serving
+ * code leaves the default.  Negative: BRE_ERR_ARG. */
+bre_status bre_set_ffn_wait_limit(int64_t cycles);
+
 /* Dequantise n_blocks blocks of format fmt to FP32 on the device, with the
  * same decode the FFN kernels use (exact: every product is exact in FP32 and
  * the one rounding is the final subtraction).  out [n_blocks * 256 or * 32]. */
