@@ -76,8 +76,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Budgets below this many cycles are polled without the hardware's suspend (try_wait may sleep
+// for a system-dependent time before it reports), so that the budget itself bounds the wait.
+constexpr long long SHORT_WAIT = 1000000LL;
+
 // Bounded wait: gives up after ~`limit` cycles and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+  if (limit < SHORT_WAIT) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity))
+      if (clock64() - t0 > limit) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {

@@ -268,15 +268,15 @@ __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
 // The block's B operand: PHASE 1 reads it from shared memory (xb: this lane's 16-byte column of
 // the block), PHASE 2 from registers filled a block ahead (B), refilling each step pair from
 // `next` once its MMAs are issued.
-template <int PHASE, int RT>
-__device__ __forceinline__ void q2k_block(const unsigned char* u0, int tile_stride, int lane, int g,
-                                          const unsigned char* xb, uint4 (&B)[8], const uint16_t* __restrict__ next,
-                                          const uint2 (&bm)[3], const DecConst& k, float (&acc)[RT][4]) {
+template <int PHASE, int RT, int TS>
+__device__ __forceinline__ void q2k_block(const unsigned char* u0, int lane, int g, const unsigned char* xb,
+                                          uint4 (&B)[8], const uint16_t* __restrict__ next, const uint2 (&bm)[3],
+                                          const DecConst& k, float (&acc)[RT][4]) {
   uint4 c0[RT], c1[RT];
   uint2 sw[RT], dd[RT];
 #pragma unroll
   for (int r = 0; r < RT; ++r) {
-    const unsigned char* u = u0 + r * tile_stride;
+    const unsigned char* u = u0 + r * TS;
     c0[r] = *reinterpret_cast<const uint4*>(u + 16 * lane);
     c1[r] = *reinterpret_cast<const uint4*>(u + 512 + 16 * lane);
     sw[r] = *reinterpret_cast<const uint2*>(u + 1024 + 8 * lane);
@@ -366,6 +366,38 @@ __device__ __forceinline__ void q2k_block(const unsigned char* u0, int tile_stri
   }
 }
 
+// One stage of a routed item: BPS consecutive blocks of RT row tiles (stage layout [row tile]
+// [block][1344]).  xb / xl: this lane's column of the activation fragments / limbs at the stage's
+// first block (phase 1); hcol / hl: the same for h in global memory (phase 2), with B holding the
+// stage's first block and refilled a block ahead (at the item's last block from itself).
+template <int PHASE, int RT, int BPS>
+__device__ __forceinline__ void routed_stage(const unsigned char* stage, int lane, int g, const unsigned char* xb,
+                                             const unsigned char* xl, uint4 (&B)[8], const uint16_t* hcol,
+                                             const uint16_t* hl, bool item_last, const DecConst& k,
+                                             float (&acc)[RT][4]) {
+  if constexpr (RT * BPS <= 4) {
+#pragma unroll 1
+    for (int bl = 0; bl < BPS; ++bl) {
+      uint2 bm[3];
+      if constexpr (PHASE == 1) {
+#pragma unroll
+        for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(xl + l * 32));
+        q2k_block<1, RT, BPS * R16>(stage, lane, g, xb, B, nullptr, bm, k, acc);
+        xb += 512;
+        xl += 96;
+      } else {
+#pragma unroll
+        for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(hl + l * 16));
+        const bool last = item_last && bl + 1 == BPS;
+        q2k_block<2, RT, BPS * R16>(stage, lane, g, nullptr, B, last ? hcol : hcol + 256, bm, k, acc);
+        hcol += 256;
+        hl += 48;
+      }
+      stage += R16;
+    }
+  }
+}
+
 // Q8_0 nibble planes of one row word (4 consecutive int8): (128+lo) and (128+hi') pairs.
 __device__ __forceinline__ void q80_frag(uint32_t w, uint32_t k43, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
                                          uint32_t& hi23) {
@@ -380,9 +412,12 @@ __device__ __forceinline__ void q80_frag(uint32_t w, uint32_t k43, uint32_t& lo0
 // ----------------------------------------------------------------------------
 // phase 1, shared Q8_0: 16 rows of one matrix over one chunk (natural k order)
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, int c, int g, int t,
+// CB > 0 fixes the chunk's block count at compile time (addresses base + immediate); CB == 0 takes cb_rt.
+template <int CB>
+__device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb_rt, int c, int g, int t,
                                            const uint16_t* xrow_g,  // global x row of column g
                                            const float* x32_0, const float* x32_1, uint32_t k43, float (&acc)[4]) {
+  const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q80_BB;
   // B (x from global memory) of block bl + 1 loads while block bl is processed
   auto load_b = [&](int bq, uint2 (&b)[2]) {
@@ -431,9 +466,11 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb, i
 // ----------------------------------------------------------------------------
 // phase 2, shared Q8_0 down: 16 rows over one chunk; B = h limbs (natural order)
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb, int c, int g, int t, int Fs,
+template <int CB>
+__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_rt, int c, int g, int t, int Fs,
                                              const uint16_t* hrow_g,  // hS[tok_g][0][:]
                                              const float* hs16_0, const float* hs16_1, uint32_t k43, float (&acc)[4]) {
+  const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q80_BB;
   // B (both limbs of h) and the 16-row sums of block bl + 1 load while block bl is processed
   auto load_b = [&](int bq, uint2 (&b)[4], float (&xs2)[2]) {
@@ -511,9 +548,9 @@ __host__ __device__ __forceinline__ int xl_stride(int d) { return (((d / 256) * 
 __host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
   PkgLayout L;
   L.xf = 0;
-  L.xl = T * x_stride(d);
-  L.smem = L.xl + T * xl_stride(d);
-  L.x32 = L.smem;
+  L.smem = T * x_stride(d);   // the part phase 1 copies into shared memory
+  L.xl = L.smem;
+  L.x32 = L.xl + T * xl_stride(d);
   L.total = L.x32 + round16(T * (d / 32) * 4);
   return L;
 }
@@ -581,7 +618,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
   const PkgLayout PL = pkg_layout(p.T, p.d);
   if (PHASE == 1 && threadIdx.x == 0) {
     mbar_arrive_expect_tx(pkg_bar, PL.smem);
-    bulk_g2s(xprep, p.pkg, PL.smem, pkg_bar);   // x fragments and limbs (a multiple of 16 bytes)
+    bulk_g2s(xprep, p.pkg, PL.smem, pkg_bar);   // x fragments (a multiple of 16 bytes)
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
 
@@ -635,8 +672,8 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 
   // ---- phase 1: the activation package arrives in shared memory by one bulk copy
   const int d = p.d;
-  const unsigned char* xF = xprep + PL.xf;   // [T][xstride]
-  const unsigned char* xL = xprep + PL.xl;   // [T][xlstride]
+  const unsigned char* xF = xprep + PL.xf;     // [T][xstride], shared memory
+  const unsigned char* xLg = p.pkg + PL.xl;    // [T][xlstride], global memory (read through L1)
   // the 32-value sums (read only by the shared expert's items) stay in global memory, so that
   // the package in shared memory leaves room for more rings
   const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
@@ -698,40 +735,42 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
       if (it.shared) {
         const int c = it.kp * p.cpp_s + cc;
         if (PHASE == 1) {
-          p1_q80_mat(stage, p.cb_s, c, g, t, p.x + (size_t)dg * d, X32 + d0 * (d / 32), X32 + d1 * (d / 32), p.kc.k43,
-                     acc[0]);
+          const uint16_t* xr = p.x + (size_t)dg * d;
+          const float* x0 = X32 + d0 * (d / 32);
+          const float* x1 = X32 + d1 * (d / 32);
+          if (p.cb_s == 8)
+            p1_q80_mat<8>(stage, 8, c, g, t, xr, x0, x1, p.kc.k43, acc[0]);
+          else
+            p1_q80_mat<0>(stage, p.cb_s, c, g, t, xr, x0, x1, p.kc.k43, acc[0]);
         } else {
-          p2_q80_chunk(stage, p.cb_s, c, g, t, p.Fs, p.hS + (size_t)dg * 2 * p.Fs, p.HS16 + (size_t)d0 * (p.Fs / 16),
-                       p.HS16 + (size_t)d1 * (p.Fs / 16), p.kc.k43, acc[0]);
+          const uint16_t* hr = p.hS + (size_t)dg * 2 * p.Fs;
+          const float* h0 = p.HS16 + (size_t)d0 * (p.Fs / 16);
+          const float* h1 = p.HS16 + (size_t)d1 * (p.Fs / 16);
+          if (p.cb_s == 8)
+            p2_q80_chunk<8>(stage, 8, c, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
+          else
+            p2_q80_chunk<0>(stage, p.cb_s, c, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
         }
       } else {
         const int b0 = (it.kp * p.cpp_r + cc) * p.bps;
-        const int tile_stride = p.bps * R16;
+        const bool item_last = cc + 1 == it.nch;
+        const unsigned char* xb = nullptr;
+        const unsigned char* xl = nullptr;
+        const uint16_t* hc = nullptr;
+        const uint16_t* hl = nullptr;
         if (PHASE == 1) {
-          const unsigned char* xb = xF + (size_t)dg * p.xstride + t * 16;
-          const unsigned char* xl = xL + (size_t)dg * p.xlstride + t * 8;
-#pragma unroll 1
-          for (int bl = 0; bl < p.bps; ++bl) {
-            const int b = b0 + bl;
-            uint2 bm[3];
-#pragma unroll
-            for (int l = 0; l < 3; ++l) bm[l] = *reinterpret_cast<const uint2*>(xl + b * 96 + l * 32);
-            q2k_block<1, RT>(stage + bl * R16, tile_stride, lane, g, xb + b * 512, B, nullptr, bm, p.kc, acc);
-          }
+          xb = xF + (size_t)dg * p.xstride + t * 16 + b0 * 512;
+          xl = xLg + (size_t)dg * p.xlstride + t * 8 + b0 * 96;
         } else {
-          const uint16_t* hl = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4;
-#pragma unroll 1
-          for (int bl = 0; bl < p.bps; ++bl) {
-            const int b = b0 + bl;
-            uint2 bm[3];
-#pragma unroll
-            for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(hl + b * 48 + l * 16));
-            // the next block of this item, or this block again at the item's end (an L1 hit)
-            const int bn = (bl + 1 < p.bps || cc + 1 < it.nch) ? b + 1 : b;
-            q2k_block<2, RT>(stage + bl * R16, tile_stride, lane, g, nullptr, B, hcol + (size_t)bn * 256, bm, p.kc,
-                             acc);
-          }
+          hc = hcol + (size_t)b0 * 256;
+          hl = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4 + b0 * 48;
         }
+        if (p.bps == 4)
+          routed_stage<PHASE, RT, 4>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+        else if (p.bps == 2)
+          routed_stage<PHASE, RT, 2>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+        else
+          routed_stage<PHASE, RT, 1>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
       }
       fence_proxy_async_smem();
       __syncwarp();
