@@ -2,6 +2,9 @@
 // row id, decoded to FP32, summed over heads in order and rounded to BF16.
 // (strix-llama.cpp issue, "Feature Description" and "DeepSeek V4.1 Engram graph
 // integration".)
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "bre_common.cuh"
@@ -34,14 +37,19 @@ __device__ __forceinline__ void decode8(uint2 v, uint32_t sb, float (&val)[8]) {
   val[6] = __fmul_rn(f67.x, sc); val[7] = __fmul_rn(f67.y, sc);
 }
 
-// decode8 with the scale already decoded (2^(e-127) as a float).
-__device__ __forceinline__ void decode8s(uint2 v, float sc, float (&val)[8]) {
-  const float2 f01 = e4m3x2_to_f32x2(v.x & 0xFFFFu), f23 = e4m3x2_to_f32x2(v.x >> 16);
-  const float2 f45 = e4m3x2_to_f32x2(v.y & 0xFFFFu), f67 = e4m3x2_to_f32x2(v.y >> 16);
-  val[0] = __fmul_rn(f01.x, sc); val[1] = __fmul_rn(f01.y, sc);
-  val[2] = __fmul_rn(f23.x, sc); val[3] = __fmul_rn(f23.y, sc);
-  val[4] = __fmul_rn(f45.x, sc); val[5] = __fmul_rn(f45.y, sc);
-  val[6] = __fmul_rn(f67.x, sc); val[7] = __fmul_rn(f67.y, sc);
+// Eight E4M3 bytes (values 8l .. 8l+7 of lane l) times one scale, as four float pairs: each byte
+// pair becomes an f16 pair (exact: E4M3 is a subset of f16), each f16 a float (exact), and the
+// products are packed FP32 multiplies (exact, or +-inf / NaN, as the scalar ones).
+__device__ __forceinline__ void decode8p(uint2 v, float sc, float2 (&o)[4]) {
+  const float2 s2 = make_float2(sc, sc);
+  const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    o[2 * i] = __fmul2_rn(__half22float2(__half2(lo)), s2);
+    o[2 * i + 1] = __fmul2_rn(__half22float2(__half2(hi)), s2);
+  }
 }
 
 // Eight heads (the configuration's H): one warp per (token, table); lanes 0..7 load the eight
@@ -80,19 +88,20 @@ __global__ void __launch_bounds__(256) engram_gather8_kernel(EngramTables tabs, 
     v[h] = ok ? __ldg(reinterpret_cast<const uint2*>(row) + lane) : make_uint2(0u, 0u);
     sb[h] = ok ? __ldg(row + 256 + (lane >> 2)) : 127u;
   }
-  float acc[8];
+  // the head sum in head order, two values per packed FP32 add (each half one IEEE add)
+  float2 acc[4];
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    float val[8];
-    decode8s(v[h], sc_tab[sb[h]], val);
+    float2 val[4];
+    decode8p(v[h], sc_tab[sb[h]], val);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = (h == 0) ? val[i] : __fadd_rn(acc[i], val[i]);
+    for (int i = 0; i < 4; ++i) acc[i] = (h == 0) ? val[i] : __fadd2_rn(acc[i], val[i]);
   }
   uint4 o;
-  o.x = f32_to_bf16_rne(acc[0]) | (f32_to_bf16_rne(acc[1]) << 16);
-  o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
-  o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
-  o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
+  o.x = f32_to_bf16_rne(acc[0].x) | (f32_to_bf16_rne(acc[0].y) << 16);
+  o.y = f32_to_bf16_rne(acc[1].x) | (f32_to_bf16_rne(acc[1].y) << 16);
+  o.z = f32_to_bf16_rne(acc[2].x) | (f32_to_bf16_rne(acc[2].y) << 16);
+  o.w = f32_to_bf16_rne(acc[3].x) | (f32_to_bf16_rne(acc[3].y) << 16);
   reinterpret_cast<uint4*>(out + w * 256)[lane] = o;
 }
 
