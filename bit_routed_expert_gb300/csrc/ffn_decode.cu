@@ -367,35 +367,32 @@ __device__ __forceinline__ void q2k_block(const unsigned char* u0, int lane, int
 }
 
 // One stage of a routed item: BPS consecutive blocks of RT row tiles (stage layout [row tile]
-// [block][1344]).  xb: this lane's column of the activation fragments at the stage's first block
-// (phase 1); hcol: the same for h in global memory (phase 2), with B holding the stage's first
-// block and refilled a block ahead (at the item's last block from itself).  lim: this lane's limb
-// words of the block after the stage's first (activation limbs in phase 1, h limbs in phase 2,
-// both in global memory, lstride elements apart), with BM holding the first block's and
-// refilled a block ahead in the same way.
+// [block][1344]).  xb / xl: this lane's column of the activation fragments / limbs at the stage's
+// first block (phase 1); hcol / hl: the same for h in global memory (phase 2), with B holding the
+// stage's first block and refilled a block ahead (at the item's last block from itself).
 template <int PHASE, int RT, int BPS>
 __device__ __forceinline__ void routed_stage(const unsigned char* stage, int lane, int g, const unsigned char* xb,
-                                             uint4 (&B)[8], const uint16_t* hcol, const uint16_t* lim, int lstride,
-                                             uint2 (&BM)[3], bool item_last, const DecConst& k, float (&acc)[RT][4]) {
+                                             const unsigned char* xl, uint4 (&B)[8], const uint16_t* hcol,
+                                             const uint16_t* hl, bool item_last, const DecConst& k,
+                                             float (&acc)[RT][4]) {
   if constexpr (RT * BPS <= 4) {
 #pragma unroll 1
     for (int bl = 0; bl < BPS; ++bl) {
-      const bool last = item_last && bl + 1 == BPS;
       uint2 bm[3];
-#pragma unroll
-      for (int l = 0; l < 3; ++l) bm[l] = BM[l];
-      if (!last) {
-#pragma unroll
-        for (int l = 0; l < 3; ++l) BM[l] = __ldg(reinterpret_cast<const uint2*>(lim) + l * 4);
-      }
       if constexpr (PHASE == 1) {
+#pragma unroll
+        for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(xl + l * 32));
         q2k_block<1, RT, BPS * R16>(stage, lane, g, xb, B, nullptr, bm, k, acc);
         xb += 512;
+        xl += 96;
       } else {
+#pragma unroll
+        for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(hl + l * 16));
+        const bool last = item_last && bl + 1 == BPS;
         q2k_block<2, RT, BPS * R16>(stage, lane, g, nullptr, B, last ? hcol : hcol + 256, bm, k, acc);
         hcol += 256;
+        hl += 48;
       }
-      lim += lstride;
       stage += R16;
     }
   }
@@ -718,25 +715,12 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 
     // phase 2 routed: the B registers of the item's first block (h of column dg)
     uint4 B[8];
-    uint2 BM[3];
     const uint16_t* hcol = nullptr;
-    const uint16_t* lim0 = nullptr;   // this lane's limb words at block 0 of the item's matrix row
-    int lstride = 0;                  // elements from one block's limbs to the next
-    if (!it.shared) {
-      const int kb0 = it.kp * p.cpp_r * p.bps;   // the item's first block
-      if (PHASE == 1) {
-        lim0 = reinterpret_cast<const uint16_t*>(xLg + (size_t)dg * p.xlstride) + t * 4;
-        lstride = 48;
-      } else {
-        hcol = p.hf + (size_t)dg * (p.F / 256) * 256 + t * 8;
-        const uint16_t* h0 = hcol + (size_t)kb0 * 256;
+    if (PHASE == 2 && !it.shared) {
+      hcol = p.hf + (size_t)dg * (p.F / 256) * 256 + t * 8;
+      const uint16_t* h0 = hcol + (size_t)(it.kp * p.cpp_r * p.bps) * 256;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) B[q] = __ldg(reinterpret_cast<const uint4*>(h0) + q * 4);
-        lim0 = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4;
-        lstride = 48;
-      }
-#pragma unroll
-      for (int l = 0; l < 3; ++l) BM[l] = __ldg(reinterpret_cast<const uint2*>(lim0 + (size_t)kb0 * lstride) + l * 4);
+      for (int q = 0; q < 8; ++q) B[q] = __ldg(reinterpret_cast<const uint4*>(h0) + q * 4);
     }
 
     for (int cc = 0; cc < it.nch; ++cc) {
@@ -771,18 +755,22 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
         const int b0 = (it.kp * p.cpp_r + cc) * p.bps;
         const bool item_last = cc + 1 == it.nch;
         const unsigned char* xb = nullptr;
+        const unsigned char* xl = nullptr;
         const uint16_t* hc = nullptr;
-        if (PHASE == 1)
+        const uint16_t* hl = nullptr;
+        if (PHASE == 1) {
           xb = xF + (size_t)dg * p.xstride + t * 16 + b0 * 512;
-        else
+          xl = xLg + (size_t)dg * p.xlstride + t * 8 + b0 * 96;
+        } else {
           hc = hcol + (size_t)b0 * 256;
-        const uint16_t* lim = lim0 + (size_t)(b0 + 1) * lstride;   // limbs of the block after b0
+          hl = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4 + b0 * 48;
+        }
         if (p.bps == 4)
-          routed_stage<PHASE, RT, 4>(stage, lane, g, xb, B, hc, lim, lstride, BM, item_last, p.kc, acc);
+          routed_stage<PHASE, RT, 4>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
         else if (p.bps == 2)
-          routed_stage<PHASE, RT, 2>(stage, lane, g, xb, B, hc, lim, lstride, BM, item_last, p.kc, acc);
+          routed_stage<PHASE, RT, 2>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
         else
-          routed_stage<PHASE, RT, 1>(stage, lane, g, xb, B, hc, lim, lstride, BM, item_last, p.kc, acc);
+          routed_stage<PHASE, RT, 1>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
       }
       fence_proxy_async_smem();
       __syncwarp();
