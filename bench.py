@@ -318,8 +318,18 @@ class DecodeWorkload:
         return router + self.ffn_bytes(n_active) + combine + engram
 
 
+_CLEAN = {}
+
+
 def flush_l2(buf):
+    """Flush L2 between timed steps: write a buffer larger than L2, then read a second one as large,
+    so that the written lines are evicted (and written back to DRAM) here rather than during the
+    timed step that follows."""
     buf.fill_(1)
+    key = (buf.device, buf.numel())
+    if key not in _CLEAN:
+        _CLEAN[key] = torch.ones(buf.numel() // 4, dtype=torch.int32, device=buf.device)
+    _CLEAN[key].max()
 
 
 def spread_us(ms):

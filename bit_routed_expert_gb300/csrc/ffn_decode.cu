@@ -41,15 +41,17 @@ namespace {
 constexpr int NS = 2;                 // ring stages per warp
 constexpr int STAGE = 5376;           // bytes per stage: four Q2_K_R16 tiles, or 16 Q8_0 rows x 8 blocks
 constexpr int R16 = 1344;             // bytes per Q2_K_R16 tile (16 rows x one block)
-constexpr int MAX_WARPS = 16;         // at most 128 registers a thread; fewer warps when the
-                                      // activation package leaves less shared memory
+constexpr int MAX_CONS = 15;          // consumer warps (plus one producer warp: 128 registers a
+                                      // thread); fewer when the activation package leaves less
+                                      // shared memory
 constexpr int RT1 = 2;                // row tiles per item, phase 1 (one B load serves both)
 constexpr int RT2 = 1;                // row tiles per item, phase 2 (B comes from global memory)
 constexpr uint32_t SEL_LO = 0x4140u;  // bytes 0,1 -> (128+b0, 128+b1) as bf16x2
 constexpr uint32_t SEL_HI = 0x4342u;  // bytes 2,3
 constexpr long long WAIT_LIMIT = 2000000000LL;  // cycles (~1 s) before a wait gives up
-constexpr int BAR_BYTES = 512;                  // mbarrier region: MAX_WARPS * NS ring barriers + package barrier
-static_assert((MAX_WARPS * NS + 1) * 8 <= BAR_BYTES, "mbarrier region too small");
+constexpr int BAR_BYTES = 1024;                 // mbarriers: full and empty per ring stage + the package's
+constexpr int DESC_BYTES = MAX_CONS * NS * 64;  // stage descriptors: 16 ints per ring stage
+static_assert((2 * MAX_CONS * NS + 1) * 8 <= BAR_BYTES, "mbarrier region too small");
 static_assert(RT1 * 2 * R16 == STAGE && RT2 * 4 * R16 == STAGE, "a full stage holds four tiles");
 
 // n / d as a multiply and shift, for 0 <= n < 2^31 (round-up multiplier m = ceil(2^(31+l) / d),
@@ -594,219 +596,222 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
 }
 
 // ----------------------------------------------------------------------------
-// the kernel
+// the kernel: one producer warp, whose lane w feeds the ring of consumer warp w (it takes items
+// from the launch's counter, decodes them, writes a stage descriptor and arms the stage's bulk
+// copies), and up to MAX_CONS consumer warps that wait for a stage, multiply and release it.
+// The consumers carry no item bookkeeping or copy issue of their own.
 // ----------------------------------------------------------------------------
+// Stage descriptor, written by the producer lane before it arms the stage:
+//   [0] flags (DF_*) | matrix << 4;  [1] routed: first block of the stage, shared: chunk index;
+//   [2] routed row group / shared tile;  [3] K part;  [4] columns n;  [5] pair offset;
+//   [8 + c] data source of column c (token in phase 1, pair position in phase 2, the token itself
+//   for the shared expert); an absent column (c >= n) repeats column 0's (0 when n == 0), whose
+//   products land only in outputs that are never stored.
+enum { DF_END = 1, DF_SHARED = 2, DF_FIRST = 4, DF_LAST = 8 };
+
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// The lanes of the producer warp (lane w feeds consumer w; lanes < nc take part) step together:
+// every round each lane whose consumer has released its next slot fills that slot, so that no
+// lane's wait holds up the others; a round in which no lane could act sleeps briefly.
 template <int PHASE>
-__global__ void __launch_bounds__(MAX_WARPS * 32, 1)
-    ffn_decode_kernel(const DecParams p, const __grid_constant__ CUtensorMap map_s0,
-                      const __grid_constant__ CUtensorMap map_s1) {
+__device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, unsigned char* ring, uint64_t* full,
+                                        uint64_t* empty, int* desc, const CUtensorMap* ms0, const CUtensorMap* ms1) {
   constexpr int RT = (PHASE == 1) ? RT1 : RT2;
-  extern __shared__ __align__(128) unsigned char sm[];
-  const int nw = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  unsigned char* stages = sm;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + nw * NS * STAGE);
-  uint64_t* pkg_bar = bars + MAX_WARPS * NS;
-  unsigned char* xprep = reinterpret_cast<unsigned char*>(bars) + BAR_BYTES;
-
-  pdl_wait();
-  if (threadIdx.x < nw * NS) mbar_init(&bars[threadIdx.x], 1);
-  if (threadIdx.x == 0) mbar_init(pkg_bar, 1);
-  fence_mbar_init();
-  __syncthreads();
-  const PkgLayout PL = pkg_layout(p.T, p.d);
-  if (PHASE == 1 && threadIdx.x == 0) {
-    mbar_arrive_expect_tx(pkg_bar, PL.smem);
-    bulk_g2s(xprep, p.pkg, PL.smem, pkg_bar);   // x fragments (a multiple of 16 bytes)
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
-
+  const unsigned lanes = nc >= 32 ? 0xffffffffu : ((1u << nc) - 1u);
   const int n_act = *p.n_active;
   const int n_shared_items = p.has_shared ? p.n_mat * p.tiles_s * p.kp_s : 0;
   const int n_items = n_shared_items + n_act * p.n_mat * p.rg_r * p.kp_r;
-
-  unsigned char* my_stage = stages + warp * NS * STAGE;
-  uint64_t* my_bar = bars + warp * NS;
-
-  auto fetch = [&]() -> int {
-    int i = 0;
-    if (lane == 0) i = atomicAdd(&p.counters[PHASE - 1], 1);
-    i = __shfl_sync(0xffffffffu, i, 0);
-    return i < n_items ? i : -1;
-  };
-
-  // ids of the items fetched but not yet taken up for processing, in three registers (an
-  // indexed array would live in local memory): the item being processed leaves the queue when
-  // it is taken up, so the queue holds at most the items with stages in flight (NS, when every
-  // item is one stage) and the one being loaded
-  static_assert(NS + 1 <= 3, "item queue holds three ids");
-  int q0 = -1, q1 = -1, q2 = -1, qn = 0;
-  auto q_push = [&](int v) {
-    if (qn == 0) q0 = v;
-    else if (qn == 1) q1 = v;
-    else q2 = v;
-    ++qn;
-  };
-  auto q_pop = [&]() {
-    q0 = q1;
-    q1 = q2;
-    --qn;
-  };
-  int ld_id = fetch();
-  q_push(ld_id);
-  Item ld_it = decode_item<PHASE>(p, ld_id, n_shared_items);
-  int ld_c = 0, ld_seq = 0;
-  auto issue_next = [&]() {
-    if (ld_it.id < 0) return;
-    issue_stage<RT>(p, ld_it, ld_c, my_stage + (ld_seq % NS) * STAGE, &my_bar[ld_seq % NS], lane, &map_s0, &map_s1);
-    ++ld_seq;
-    if (++ld_c == ld_it.nch) {
-      ld_id = fetch();
-      q_push(ld_id);
-      ld_it = decode_item<PHASE>(p, ld_id, n_shared_items);
-      ld_c = 0;
-    }
-  };
-  for (int i = 0; i < NS; ++i) issue_next();
-
-  // ---- phase 1: the activation package arrives in shared memory by one bulk copy
-  const int d = p.d;
-  const unsigned char* xF = xprep + PL.xf;     // [T][xstride], shared memory
-  const unsigned char* xLg = p.pkg + PL.xl;    // [T][xlstride], global memory (read through L1)
-  // the 32-value sums (read only by the shared expert's items) stay in global memory, so that
-  // the package in shared memory leaves room for more rings
-  const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
-  if (PHASE == 1) {
-    if (!mbar_wait_bounded(pkg_bar, 0, p.wait)) {
-      // give up: the package copy and this warp's ring copies land before the warp leaves
-      if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
-      mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT);
-      for (int q = 0; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
-      return;
-    }
-  }
-
-  int cs_seq = 0;
-  const int nb_r = p.nb_r;
+  int seq = 0, cc = 0;
+  bool more = true, done = false;
+  Item it;
+  it.id = -1;
+  int src[8];
+  long long t_last = clock64();
   while (true) {
-    const int id = q0;
-    if (id < 0) break;
-    q_pop();
-    const Item it = decode_item<PHASE>(p, id, n_shared_items);
-    // column -> token (phase 1) or h row (phase 2)
-    auto col_src = [&](int col) -> int {
-      if (col >= it.n) return -1;
-      if (it.shared) return col;   // token; phase-2 h row of the shared expert
-      const int pos = it.off + col;
-      return (PHASE == 1) ? fdiv(__ldg(p.perm + pos), p.fd_k) : pos;
-    };
-    const int sg = col_src(g), sc0 = col_src(2 * t), sc1 = col_src(2 * t + 1);
-    // data sources: an absent column (>= n) reads column 0's data (or row 0), whose products
-    // land only in that column's outputs, which are never stored; this keeps the inner loops
-    // free of presence tests
-    const int src0 = it.n > 0 ? col_src(0) : 0;
-    const int dg = sg >= 0 ? sg : src0, d0 = sc0 >= 0 ? sc0 : src0, d1 = sc1 >= 0 ? sc1 : src0;
-    float acc[RT][4];
+    bool acted = false;
+    if (!done) {
+      if (it.id < 0 && more) {
+        int id = atomicAdd(&p.counters[PHASE - 1], 1);
+        if (id >= n_items) {
+          id = -1;
+          more = false;
+        }
+        it = decode_item<PHASE>(p, id, n_shared_items);
+        cc = 0;
+        if (id >= 0) {
 #pragma unroll
-    for (int r = 0; r < RT; ++r)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[r][i] = 0.0f;
-
-    // phase 2 routed: the B registers of the item's first block (h of column dg)
-    uint4 B[8];
-    const uint16_t* hcol = nullptr;
-    if (PHASE == 2 && !it.shared) {
-      hcol = p.hf + (size_t)dg * (p.F / 256) * 256 + t * 8;
-      const uint16_t* h0 = hcol + (size_t)(it.kp * p.cpp_r * p.bps) * 256;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) B[q] = __ldg(reinterpret_cast<const uint4*>(h0) + q * 4);
-    }
-
-    for (int cc = 0; cc < it.nch; ++cc) {
-      const int st = cs_seq % NS;
-      if (!mbar_wait_bounded(&my_bar[st], (cs_seq / NS) & 1, p.wait)) {
-        // give up: every copy this warp has issued (this stage's included) lands before it leaves
-        if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
-        for (int q = cs_seq; q < ld_seq; ++q) mbar_wait_bounded(&my_bar[q % NS], (q / NS) & 1, WAIT_LIMIT);
-        return;
+          for (int c = 0; c < 8; ++c) {
+            const int col = c < it.n ? c : 0;
+            int v = 0;
+            if (it.n > 0) {
+              if (it.shared) v = col;
+              else v = (PHASE == 1) ? fdiv(__ldg(p.perm + it.off + col), p.fd_k) : it.off + col;
+            }
+            src[c] = v;
+          }
+        }
       }
-      const unsigned char* stage = my_stage + st * STAGE;
-      if (it.shared) {
-        const int c = it.kp * p.cpp_s + cc;
-        if (PHASE == 1) {
-          const uint16_t* xr = p.x + (size_t)dg * d;
-          const float* x0 = X32 + d0 * (d / 32);
-          const float* x1 = X32 + d1 * (d / 32);
-          if (p.cb_s == 8)
-            p1_q80_mat<8>(stage, 8, c, g, t, xr, x0, x1, p.kc.k43, acc[0]);
-          else
-            p1_q80_mat<0>(stage, p.cb_s, c, g, t, xr, x0, x1, p.kc.k43, acc[0]);
+      const int slot = seq % NS;
+      // the slot is free once its consumer has released the stage it held before
+      if (mbar_test_wait(&empty[slot], ((seq / NS) & 1) ^ 1)) {
+        acted = true;
+        t_last = clock64();
+        int* dsc = desc + slot * 16;
+        if (it.id < 0) {   // nothing left: an end marker, armed with no bytes
+          dsc[0] = DF_END;
+          mbar_arrive_plain(&full[slot]);
+          done = true;
         } else {
-          const uint16_t* hr = p.hS + (size_t)dg * 2 * p.Fs;
-          const float* h0 = p.HS16 + (size_t)d0 * (p.Fs / 16);
-          const float* h1 = p.HS16 + (size_t)d1 * (p.Fs / 16);
-          if (p.cb_s == 8)
-            p2_q80_chunk<8>(stage, 8, c, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
-          else
-            p2_q80_chunk<0>(stage, p.cb_s, c, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
+          dsc[0] = (it.shared ? DF_SHARED : 0) | (cc == 0 ? DF_FIRST : 0) | (cc + 1 == it.nch ? DF_LAST : 0) |
+                   (it.m << 4);
+          dsc[1] = it.shared ? it.kp * p.cpp_s + cc : (it.kp * p.cpp_r + cc) * p.bps;
+          dsc[2] = it.grp;
+          dsc[3] = it.kp;
+          dsc[4] = it.n;
+          dsc[5] = it.off;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dsc[8 + c] = src[c];
+          issue_stage<RT>(p, it, cc, ring + slot * STAGE, &full[slot], 0, ms0, ms1);
+          if (++cc == it.nch) it.id = -1;
         }
-      } else {
-        const int b0 = (it.kp * p.cpp_r + cc) * p.bps;
-        const bool item_last = cc + 1 == it.nch;
-        const unsigned char* xb = nullptr;
-        const unsigned char* xl = nullptr;
-        const uint16_t* hc = nullptr;
-        const uint16_t* hl = nullptr;
-        if (PHASE == 1) {
-          xb = xF + (size_t)dg * p.xstride + t * 16 + b0 * 512;
-          xl = xLg + (size_t)dg * p.xlstride + t * 8 + b0 * 96;
-        } else {
-          hc = hcol + (size_t)b0 * 256;
-          hl = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4 + b0 * 48;
-        }
-        if (p.bps == 4)
-          routed_stage<PHASE, RT, 4>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
-        else if (p.bps == 2)
-          routed_stage<PHASE, RT, 2>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+        ++seq;
+      } else if (clock64() - t_last > p.wait) {
+        set_err(p.err, BRE_DEVERR_TIMEOUT);   // the consumer stopped releasing stages
+        done = true;
+      }
+    }
+    if (__all_sync(lanes, done)) break;
+    if (!__any_sync(lanes, acted)) __nanosleep(64);
+  }
+  // every stage this lane armed has landed before the warp leaves (the last phase of each slot)
+  for (int q = seq - NS < 0 ? 0 : seq - NS; q < seq; ++q) mbar_wait_bounded(&full[q % NS], (q / NS) & 1, WAIT_LIMIT);
+}
+
+template <int PHASE>
+__device__ __forceinline__ void consume(const DecParams& p, int lane, const unsigned char* ring, uint64_t* full,
+                                        uint64_t* empty, const int* desc, const unsigned char* xF,
+                                        const unsigned char* xLg, const float* X32) {
+  constexpr int RT = (PHASE == 1) ? RT1 : RT2;
+  const int g = lane >> 2, t = lane & 3;
+  const int d = p.d;
+  float acc[RT][4];
+  uint4 B[8];
+  int n = 0, off = 0, grp = 0, kp = 0, m = 0, dg = 0, d0 = 0, d1 = 0;
+  bool shared = false;
+  const uint16_t* hcol = nullptr;
+  for (int seq = 0;; ++seq) {
+    const int slot = seq % NS;
+    if (!mbar_wait_bounded(&full[slot], (seq / NS) & 1, p.wait)) {
+      if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
+      return;   // the producer lane waits for the copies it armed
+    }
+    const int* dsc = desc + slot * 16;
+    const int fl = dsc[0];
+    if (fl & DF_END) return;
+    const int c1 = dsc[1];
+    if (fl & DF_FIRST) {
+      shared = (fl & DF_SHARED) != 0;
+      m = fl >> 4;
+      grp = dsc[2];
+      kp = dsc[3];
+      n = dsc[4];
+      off = dsc[5];
+      dg = dsc[8 + g];
+      d0 = dsc[8 + 2 * t];
+      d1 = dsc[8 + 2 * t + 1];
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[r][i] = 0.0f;
+      if (PHASE == 2 && !shared) {
+        // the B registers of the item's first block (h of column dg)
+        hcol = p.hf + (size_t)dg * (p.F / 256) * 256 + t * 8;
+        const uint16_t* h0 = hcol + (size_t)c1 * 256;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) B[q] = __ldg(reinterpret_cast<const uint4*>(h0) + q * 4);
+      }
+    }
+    const unsigned char* stage = ring + slot * STAGE;
+    if (shared) {
+      if (PHASE == 1) {
+        const uint16_t* xr = p.x + (size_t)dg * d;
+        const float* x0 = X32 + d0 * (d / 32);
+        const float* x1 = X32 + d1 * (d / 32);
+        if (p.cb_s == 8)
+          p1_q80_mat<8>(stage, 8, c1, g, t, xr, x0, x1, p.kc.k43, acc[0]);
         else
-          routed_stage<PHASE, RT, 1>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+          p1_q80_mat<0>(stage, p.cb_s, c1, g, t, xr, x0, x1, p.kc.k43, acc[0]);
+      } else {
+        const uint16_t* hr = p.hS + (size_t)dg * 2 * p.Fs;
+        const float* h0 = p.HS16 + (size_t)d0 * (p.Fs / 16);
+        const float* h1 = p.HS16 + (size_t)d1 * (p.Fs / 16);
+        if (p.cb_s == 8)
+          p2_q80_chunk<8>(stage, 8, c1, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
+        else
+          p2_q80_chunk<0>(stage, p.cb_s, c1, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      ++cs_seq;
-      issue_next();
+    } else {
+      const int b0 = c1;
+      const bool item_last = (fl & DF_LAST) != 0;
+      const unsigned char* xb = nullptr;
+      const unsigned char* xl = nullptr;
+      const uint16_t* hc = nullptr;
+      const uint16_t* hl = nullptr;
+      if (PHASE == 1) {
+        xb = xF + (size_t)dg * p.xstride + t * 16 + b0 * 512;
+        xl = xLg + (size_t)dg * p.xlstride + t * 8 + b0 * 96;
+      } else {
+        hc = hcol + (size_t)b0 * 256;
+        hl = p.hl + (size_t)dg * (p.F / 256) * 48 + t * 4 + b0 * 48;
+      }
+      if (p.bps == 4)
+        routed_stage<PHASE, RT, 4>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+      else if (p.bps == 2)
+        routed_stage<PHASE, RT, 2>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
+      else
+        routed_stage<PHASE, RT, 1>(stage, lane, g, xb, xl, B, hc, hl, item_last, p.kc, acc);
     }
+    // the stage goes back to the producer
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_plain(&empty[slot]);
+    if (!(fl & DF_LAST)) continue;
 
-    // ---- phase 1 ends an item by storing its FP32 partial sums of one matrix for the expert's
-    // real columns; ffn_finish_kernel adds the K parts in order and forms h.  Phase 2 stores y
-    // (or adds it into zeros when the call splits phase 2 into two K parts).
+    // ---- an item ends.  Phase 1 stores its FP32 partial sums of one matrix for the expert's real
+    // columns (ffn_finish_kernel adds the K parts in order and forms h); phase 2 stores y (or adds
+    // it into zeros when the call splits phase 2 into two K parts).
     if (PHASE == 1) {
-      const int tiles = it.shared ? p.tiles_s : p.rows_r / 16;
-      const int KP = it.shared ? p.kp_s : p.kp_r;
-      float* base = it.shared ? p.part_s : p.part_r;
+      const int tiles = shared ? p.tiles_s : p.rows_r / 16;
+      const int KP = shared ? p.kp_s : p.kp_r;
+      float* base = shared ? p.part_s : p.part_r;
 #pragma unroll
-      for (int r = 0; r < (it.shared ? 1 : RT); ++r) {
-        const int tile = it.shared ? it.grp : it.grp * RT + r;
+      for (int r = 0; r < RT; ++r) {
+        if (shared && r > 0) break;
+        const int tile = shared ? grp : grp * RT + r;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
-          if (col < it.n) {
-            const size_t src = it.shared ? (size_t)col : (size_t)(it.off + col);   // token / pair position
-            base[(((src * tiles + tile) * KP + it.kp) * 2 + it.m) * 16 + row] = acc[r][i];
+          if (col < n) {
+            const size_t src = shared ? (size_t)col : (size_t)(off + col);   // token / pair position
+            base[(((src * tiles + tile) * KP + kp) * 2 + m) * 16 + row] = acc[r][i];
           }
         }
       }
     } else {
 #pragma unroll
-      for (int r = 0; r < (it.shared ? 1 : RT); ++r) {
-        const int row0 = (it.shared ? it.grp : it.grp * RT + r) * 16;
+      for (int r = 0; r < RT; ++r) {
+        if (shared && r > 0) break;
+        const int row0 = (shared ? grp : grp * RT + r) * 16;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int cs = (i & 1) ? sc1 : sc0;
-          if (cs >= 0) {
+          const int col = 2 * t + (i & 1);
+          if (col < n) {
+            const int cs = (i & 1) ? d1 : d0;
             const int row = row0 + g + 8 * (i >> 1);
-            float* dst = it.shared ? p.y_shared + (size_t)cs * p.d + row : p.y_pairs + (size_t)cs * p.d + row;
+            float* dst = shared ? p.y_shared + (size_t)cs * p.d + row : p.y_pairs + (size_t)cs * p.d + row;
             if (p.red)
               atomicAdd(dst, acc[r][i]);
             else
@@ -816,6 +821,56 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
       }
     }
   }
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
+    ffn_decode_kernel(const DecParams p, const __grid_constant__ CUtensorMap map_s0,
+                      const __grid_constant__ CUtensorMap map_s1) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int nc = (blockDim.x >> 5) - 1;   // consumer warps; warp nc produces
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* stages = sm;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + nc * NS * STAGE);
+  uint64_t* empty = full + MAX_CONS * NS;
+  uint64_t* pkg_bar = empty + MAX_CONS * NS;
+  int* desc = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(full) + BAR_BYTES);   // [consumer][slot][16]
+  unsigned char* xprep = reinterpret_cast<unsigned char*>(desc) + DESC_BYTES;
+
+  pdl_wait();
+  if (threadIdx.x < nc * NS) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], 1);
+  }
+  if (threadIdx.x == 0) mbar_init(pkg_bar, 1);
+  fence_mbar_init();
+  __syncthreads();
+  const PkgLayout PL = pkg_layout(p.T, p.d);
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
+
+  if (warp == nc) {
+    if (PHASE == 1 && lane == 0) {
+      mbar_arrive_expect_tx(pkg_bar, PL.smem);
+      bulk_g2s(xprep, p.pkg, PL.smem, pkg_bar);   // x fragments (a multiple of 16 bytes)
+    }
+    if (lane < nc)
+      produce<PHASE>(p, nc, lane, stages + lane * NS * STAGE, full + lane * NS, empty + lane * NS,
+                     desc + lane * NS * 16, &map_s0, &map_s1);
+    return;
+  }
+
+  // ---- consumers.  Phase 1: the activation package arrives in shared memory by one bulk copy;
+  // its limbs and the 32-value sums (read only by the shared expert's items) stay in global memory
+  const unsigned char* xF = xprep + PL.xf;                              // [T][xstride], shared memory
+  const unsigned char* xLg = p.pkg + PL.xl;                             // [T][xlstride], global memory
+  const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
+  if (PHASE == 1 && !mbar_wait_bounded(pkg_bar, 0, p.wait)) {
+    if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
+    mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT);   // the package copy lands before this warp leaves
+    return;
+  }
+  consume<PHASE>(p, lane, stages + warp * NS * STAGE, full + warp * NS, empty + warp * NS, desc + warp * NS * 16, xF,
+                 xLg, X32);
 }
 
 // ----------------------------------------------------------------------------
@@ -1187,10 +1242,11 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     }
     const size_t xbytes = (phase == 1) ? (size_t)pkg_layout(a.T, p.d).smem : 0;   // shared-memory part
-    int nw = MAX_WARPS;
-    while (nw > 1 && (size_t)nw * NS * STAGE + BAR_BYTES + xbytes > (size_t)smem_max) --nw;
-    const size_t smem = (size_t)nw * NS * STAGE + BAR_BYTES + xbytes;
+    int nc = MAX_CONS;
+    while (nc > 1 && (size_t)nc * NS * STAGE + BAR_BYTES + DESC_BYTES + xbytes > (size_t)smem_max) --nc;
+    const size_t smem = (size_t)nc * NS * STAGE + BAR_BYTES + DESC_BYTES + xbytes;
     if (smem > (size_t)smem_max) return cudaErrorInvalidValue;
+    const int nw = nc + 1;   // consumers and the producer warp
     cudaError_t e;
     if (phase == 1) {
       kp_r1 = p.kp_r;
