@@ -52,20 +52,20 @@ __device__ __forceinline__ void decode8p(uint2 v, float sc, float2 (&o)[4]) {
   }
 }
 
-// Eight heads (the configuration's H).  A warp works through (token, table) pairs w, w + W, ...
-// (W the launch's warps), with the next pair's row ids and rows loaded before the current pair
-// is decoded, so that a warp always has a pair's loads in flight.  Lanes 0..7 load a pair's
-// eight row ids with one instruction and check them with one unsigned compare; the E8M0 scales
-// come from a 256-entry table in shared memory; the first head starts the sum.  Same arithmetic
-// as the general kernel below.
-struct Rows8 {
-  uint2 v[8];
-  uint32_t sb[8];
-  unsigned okm;
-};
-
-__device__ __forceinline__ void load_rows8(const EngramTables& tabs, int n_tables, const int64_t* __restrict__ ids,
-                                           long long w, int lane, Rows8& r) {
+// Eight heads (the configuration's H): one warp per (token, table); lanes 0..7 load the eight
+// row ids with one instruction and check them with one unsigned compare; every row's loads are
+// issued before any decode; the E8M0 scales come from a 256-entry table in shared memory; the
+// first head starts the sum.  Same arithmetic as the general kernel below.
+__global__ void __launch_bounds__(256) engram_gather8_kernel(EngramTables tabs, int n_tables,
+                                                             const int64_t* __restrict__ ids, int T,
+                                                             uint16_t* __restrict__ out, int32_t* err) {
+  __shared__ float sc_tab[256];
+  sc_tab[threadIdx.x] = e8m0_to_f32(threadIdx.x);   // blockDim.x == 256
+  __syncthreads();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)T * n_tables) return;
   const int tau = (int)(w % n_tables);
   const uint8_t* table = tabs.ptr[0];
   long long nrows = tabs.n_rows[0];
@@ -76,53 +76,33 @@ __device__ __forceinline__ void load_rows8(const EngramTables& tabs, int n_table
       nrows = tabs.n_rows[q];
     }
   const long long myid = lane < 8 ? __ldg(ids + w * 8 + lane) : 0;
-  r.okm = __ballot_sync(0xffffffffu, (unsigned long long)myid < (unsigned long long)nrows);
+  const unsigned okm = __ballot_sync(0xffffffffu, (unsigned long long)myid < (unsigned long long)nrows);
+  if ((okm & 0xFFu) != 0xFFu && lane == 0) set_err(err, BRE_DEVERR_ROW_ID);
+  uint2 v[8];
+  uint32_t sb[8];
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    const long long id = __shfl_sync(0xffffffffu, myid, h);
-    const bool ok = (r.okm >> h) & 1u;
-    const uint8_t* row = table + (ok ? id : 0) * ENGRAM_ROW;
-    r.v[h] = ok ? __ldg(reinterpret_cast<const uint2*>(row) + lane) : make_uint2(0u, 0u);
-    r.sb[h] = ok ? __ldg(row + 256 + (lane >> 2)) : 127u;
+    const long long r = __shfl_sync(0xffffffffu, myid, h);
+    const bool ok = (okm >> h) & 1u;
+    const uint8_t* row = table + (ok ? r : 0) * ENGRAM_ROW;
+    v[h] = ok ? __ldg(reinterpret_cast<const uint2*>(row) + lane) : make_uint2(0u, 0u);
+    sb[h] = ok ? __ldg(row + 256 + (lane >> 2)) : 127u;
   }
-}
-
-__global__ void __launch_bounds__(256) engram_gather8_kernel(EngramTables tabs, int n_tables,
-                                                             const int64_t* __restrict__ ids, int T,
-                                                             uint16_t* __restrict__ out, int32_t* err) {
-  __shared__ float sc_tab[256];
-  sc_tab[threadIdx.x] = e8m0_to_f32(threadIdx.x);   // blockDim.x == 256
-  __syncthreads();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const long long n_pairs = (long long)T * n_tables;
-  const long long stride = (long long)gridDim.x * (blockDim.x >> 5);
-  long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (w >= n_pairs) return;
-  Rows8 cur, nxt;
-  load_rows8(tabs, n_tables, ids, w, lane, cur);
-  for (;; w += stride) {
-    const bool more = w + stride < n_pairs;
-    if (more) load_rows8(tabs, n_tables, ids, w + stride, lane, nxt);
-    if ((cur.okm & 0xFFu) != 0xFFu && lane == 0) set_err(err, BRE_DEVERR_ROW_ID);
-    // the head sum in head order, two values per packed FP32 add (each half one IEEE add)
-    float2 acc[4];
+  // the head sum in head order, two values per packed FP32 add (each half one IEEE add)
+  float2 acc[4];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      float2 val[4];
-      decode8p(cur.v[h], sc_tab[cur.sb[h]], val);
+  for (int h = 0; h < 8; ++h) {
+    float2 val[4];
+    decode8p(v[h], sc_tab[sb[h]], val);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = (h == 0) ? val[i] : __fadd2_rn(acc[i], val[i]);
-    }
-    uint4 o;
-    o.x = f32_to_bf16_rne(acc[0].x) | (f32_to_bf16_rne(acc[0].y) << 16);
-    o.y = f32_to_bf16_rne(acc[1].x) | (f32_to_bf16_rne(acc[1].y) << 16);
-    o.z = f32_to_bf16_rne(acc[2].x) | (f32_to_bf16_rne(acc[2].y) << 16);
-    o.w = f32_to_bf16_rne(acc[3].x) | (f32_to_bf16_rne(acc[3].y) << 16);
-    reinterpret_cast<uint4*>(out + w * 256)[lane] = o;
-    if (!more) break;
-    cur = nxt;
+    for (int i = 0; i < 4; ++i) acc[i] = (h == 0) ? val[i] : __fadd2_rn(acc[i], val[i]);
   }
+  uint4 o;
+  o.x = f32_to_bf16_rne(acc[0].x) | (f32_to_bf16_rne(acc[0].y) << 16);
+  o.y = f32_to_bf16_rne(acc[1].x) | (f32_to_bf16_rne(acc[1].y) << 16);
+  o.z = f32_to_bf16_rne(acc[2].x) | (f32_to_bf16_rne(acc[2].y) << 16);
+  o.w = f32_to_bf16_rne(acc[3].x) | (f32_to_bf16_rne(acc[3].y) << 16);
+  reinterpret_cast<uint4*>(out + w * 256)[lane] = o;
 }
 
 // One warp per (token, table); HC heads per pass with every row load of the pass issued
@@ -187,17 +167,7 @@ cudaError_t launch_engram(const EngramTables& tabs, int n_tables, const int64_t*
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
   if (H == 8) {
-    // one wave of resident blocks, each warp taking several pairs
-    static int per_sm = 0;
-    if (per_sm == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, engram_gather8_kernel, threads, 0) != cudaSuccess || n < 1)
-        n = 1;
-      per_sm = n;
-    }
-    const long long cap = (long long)device_sm_count() * per_sm;
-    const long long b8 = blocks < cap ? blocks : cap;
-    const cudaError_t le = launch_k(engram_gather8_kernel, dim3((unsigned)b8), dim3(threads), 0, s, tabs,
+    const cudaError_t le = launch_k(engram_gather8_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, tabs,
                                     n_tables, ids, T, out, err);
     if (le != cudaSuccess) return le;
   } else if (H == 1)
