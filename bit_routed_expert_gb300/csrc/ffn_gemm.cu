@@ -91,23 +91,47 @@ __global__ void plan_kernel(const int32_t* __restrict__ offsets, const int32_t* 
   plan->tiles2 = t2;
 }
 
+// X_perm[q] = x[perm[q] / k] for valid pairs q < offsets[E]; X_perm[P + t] = x[t].  One warp per
+// row, eight 16-byte loads in flight per lane before their stores.
+__global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                              const int32_t* __restrict__ offsets, int E, int k, int T, int P, int d,
+                              uint16_t* __restrict__ xp, int has_shared) {
+  pdl_wait();
+  const int per_row = d / 8;
+  const int nvalid = __ldg(offsets + E);
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int q = blockIdx.x * wpb + (threadIdx.x >> 5); q < P + T; q += gridDim.x * wpb) {
+    int src = -1;
+    if (q < nvalid)
+      src = __ldg(perm + q) / k;
+    else if (q >= P && has_shared)
+      src = q - P;
+    if (src < 0) continue;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)src * d);
+    uint4* out = reinterpret_cast<uint4*>(xp + (size_t)q * d);
+    for (int c0 = 0; c0 < per_row; c0 += 8 * 32) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < per_row) v[u] = __ldg(in + c);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < per_row) out[c] = v[u];
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Four rows (r0..r3) of a 2-D tensor whose map's box is one row high, at column x, into four
-// consecutive rows of shared memory (the map's swizzle applied as for a tile load).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -326,8 +350,6 @@ struct GemmParams {
   int out_v8;            // phase 2 outputs 32-byte aligned: 32-byte stores
   int32_t* err;
   long long wait;        // budget (cycles) of the pipeline's waits; the drains at exit use G_WAIT
-  const int32_t* perm;   // phase 1: pair ids in permuted order (A rows are x[perm[q] / k])
-  int k;
 };
 
 struct TileInfo {
@@ -411,50 +433,26 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     // of the B tile.  The first producer thread also loads the A tile of every stage it opens.
     const int i = threadIdx.x - 128;
     const bool a_loader = (i == 0);
-    const int pw = warp - 4;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles && !aborted(); tile += gridDim.x) {
       const TileInfo ti = find_tile<PHASE>(p, tile);
       const int KS = ti.K / G_BK;
       const CUtensorMap* amap = (ti.expert < 0) ? &map_s : &map_r;
       const int arow = (PHASE == 1) ? ti.a_row0 + ti.mt * G_BM : (ti.expert < 0 ? 0 : ti.a_row0) + ti.mt * G_BM;
-      // phase 1: producer warp 0 gathers the A rows straight from x, lane l the tile's rows
-      // 8l .. 8l+7 (x rows perm[q] / k of the group's pairs q, or the shared expert's tokens); rows
-      // past the group's end repeat its first row (their products are never stored)
-      int ar[8];
-      if (PHASE == 1 && pw == 0) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = ti.mt * G_BM + 8 * lane + j;
-          const int rr = r < ti.n ? r : 0;
-          ar[j] = (ti.expert >= 0) ? __ldg(p.perm + ti.a_row0 + rr) / p.k : rr;
-        }
-      }
-      // wait until stage s is free, then start its A tile (phase 1: producer warp 0 by 64 four-row
-      // gathers, two a lane; phase 2: the first producer thread by two tile loads)
+      // wait until stage s is free, then (first thread) start its A tile
       auto open_stage = [&](int s, int ks) -> bool {
-        bool ok = mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, p.wait);
-        if (PHASE == 1 && pw == 0) {
-          ok = __all_sync(0xffffffffu, ok);   // the warp arms and fills the stage together or not at all
-          if (ok) {
-            if (lane == 0) mbar_arrive_expect_tx(&aful[s], G_A_BYTES);
-            __syncwarp();
-            unsigned char* dst = a_st + s * G_A_BYTES + (lane >= 16 ? G_A_BYTES / 2 : 0) + ((8 * lane) & 127) * 128;
-            tma_gather4(dst, amap, ks * G_BK, ar[0], ar[1], ar[2], ar[3], &aful[s]);
-            tma_gather4(dst + 512, amap, ks * G_BK, ar[4], ar[5], ar[6], ar[7], &aful[s]);
-          }
-        }
-        if (!ok) {
+        if (!mbar_wait_bounded(&empty[s], ((it / G_STAGES) & 1) ^ 1, p.wait)) {
           fail();
           return false;
         }
-        if (PHASE == 2 && a_loader) {
+        if (a_loader) {
           mbar_arrive_expect_tx(&aful[s], G_A_BYTES);
           tma_load_2d(a_st + s * G_A_BYTES, amap, ks * G_BK, arow, &aful[s]);
           tma_load_2d(a_st + s * G_A_BYTES + G_A_BYTES / 2, amap, ks * G_BK, arow + 128, &aful[s]);
         }
         return true;
       };
+      const int pw = warp - 4;
       unsigned char* stg = stage_raw + pw * 32 * Q2K_BB;
       if (ti.expert >= 0) {
         // Q2_K_R16: the warp's 32 rows are two 16-row tiles; each block of them is two
@@ -683,14 +681,6 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
 }
 
-// 2-D BF16 tensor [rows][K] for four-row gathers: box 64 x 1 (one row high), 128-byte swizzle.
-bool make_gather_map(CUtensorMap* m, const void* base, long long rows, int K) {
-  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)(rows > 0 ? rows : 1)};
-  const uint64_t strides[1] = {(uint64_t)K * 2};
-  const uint32_t box[2] = {64, 1};
-  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 // 2-D BF16 tensor [rows][K], box 64 x 128, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, long long rows, int K) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)(rows > 0 ? rows : 1)};
@@ -705,6 +695,7 @@ size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
   // the reserved prefix stays with the decode path's counters, which must keep their zeros
   size_t s = ffn_reserved_bytes(k, d, F, Fs) + ((sizeof(Plan) + 1023) & ~(size_t)1023);
+  s += ((P + T) * d * 2 + 1023) & ~(size_t)1023;     // gathered activations
   s += (P * F * 2 + 1023) & ~(size_t)1023;           // routed intermediate
   s += ((size_t)T * Fs * 2 + 1023) & ~(size_t)1023;  // shared intermediate
   return s;
@@ -718,6 +709,8 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   char* w = static_cast<char*>(a.ws) + ffn_reserved_bytes(k, d, F, Fs);
   Plan* plan = reinterpret_cast<Plan*>(w);
   w += (sizeof(Plan) + 1023) & ~(size_t)1023;
+  uint16_t* xp = reinterpret_cast<uint16_t*>(w);
+  w += ((P + T) * d * 2 + 1023) & ~(size_t)1023;
   uint16_t* h_r = reinterpret_cast<uint16_t*>(w);
   w += (P * F * 2 + 1023) & ~(size_t)1023;
   uint16_t* h_s = reinterpret_cast<uint16_t*>(w);
@@ -730,6 +723,12 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
+  {
+    const cudaError_t le = launch_k(gather_kernel, dim3(sms * 4), dim3(256), 0, s, a.x, a.perm, a.offsets, E, k, T,
+                                    (int)P, d, xp, S ? 1 : 0);
+    if (le != cudaSuccess) return le;
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const size_t smem = G_STAGES * (G_A_BYTES + G_B_BYTES) + 1024 + 256 + 8 * 32 * Q2K_BB;
   static int configured = -1;
@@ -745,15 +744,13 @@ cudaError_t launch_gemm(const FfnArgs& a, cudaStream_t s) {
     configured = dev;
   }
   CUtensorMap m_x, m_hr, m_hs;
-  if (!make_gather_map(&m_x, a.x, T, d)) return cudaErrorInvalidValue;
+  if (!make_map(&m_x, xp, (long long)(P + T), d)) return cudaErrorInvalidValue;
   if (!make_map(&m_hr, h_r, (long long)P, F)) return cudaErrorInvalidValue;
   if (!make_map(&m_hs, S ? (const void*)h_s : (const void*)h_r, S ? T : (long long)P, S ? Fs : F))
     return cudaErrorInvalidValue;
 
   GemmParams g{};
   g.wait = ffn_wait_budget(G_WAIT);
-  g.perm = a.perm;
-  g.k = k;
   g.plan = plan;
   g.err = a.err;
   // phase 1: gate/up -> h
