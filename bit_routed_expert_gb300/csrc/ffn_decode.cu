@@ -378,24 +378,32 @@ __device__ __forceinline__ void routed_stage(const unsigned char* stage, int lan
                                              const uint16_t* hl, bool item_last, const DecConst& k,
                                              float (&acc)[RT][4]) {
   if constexpr (RT * BPS <= 4) {
+    if constexpr (PHASE == 1) {
+      // the loop stays rolled (unrolled, its two row tiles per block run slower)
 #pragma unroll 1
-    for (int bl = 0; bl < BPS; ++bl) {
-      uint2 bm[3];
-      if constexpr (PHASE == 1) {
+      for (int bl = 0; bl < BPS; ++bl) {
+        uint2 bm[3];
 #pragma unroll
         for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(xl + l * 32));
         q2k_block<1, RT, BPS * R16>(stage, lane, g, xb, B, nullptr, bm, k, acc);
         xb += 512;
         xl += 96;
-      } else {
+        stage += R16;
+      }
+    } else {
+      // one row tile per block: unrolled, the h loads of the next block have more work to arrive in
+      // (measured 45.3 -> 41.8 us for the down projection of 36 experts at T = 8)
+#pragma unroll
+      for (int bl = 0; bl < BPS; ++bl) {
+        uint2 bm[3];
 #pragma unroll
         for (int l = 0; l < 3; ++l) bm[l] = __ldg(reinterpret_cast<const uint2*>(hl + l * 16));
         const bool last = item_last && bl + 1 == BPS;
         q2k_block<2, RT, BPS * R16>(stage, lane, g, nullptr, B, last ? hcol : hcol + 256, bm, k, acc);
         hcol += 256;
         hl += 48;
+        stage += R16;
       }
-      stage += R16;
     }
   }
 }
