@@ -109,7 +109,7 @@ struct DecParams {
   float* part_s;             // phase 1 partial sums: [token][tile][K part][gate|up][16 rows]
   float* y_pairs;
   float* y_shared;
-  int red;                   // phase 2: outputs are sums of two K parts added into zeros
+  int red_r, red_s;          // phase 2: routed / shared outputs are sums of two K parts added into zeros
   int* counters;
   int32_t* err;
   long long wait;            // budget (cycles) of the ring and package waits; drains use WAIT_LIMIT
@@ -820,7 +820,7 @@ __device__ __forceinline__ void consume(const DecParams& p, int lane, const unsi
             const int cs = (i & 1) ? d1 : d0;
             const int row = row0 + g + 8 * (i >> 1);
             float* dst = shared ? p.y_shared + (size_t)cs * p.d + row : p.y_pairs + (size_t)cs * p.d + row;
-            if (p.red)
+            if (shared ? p.red_s : p.red_r)
               atomicAdd(dst, acc[r][i]);
             else
               *dst = acc[r][i];
@@ -898,9 +898,9 @@ struct FinishParams {
   uint16_t* hl;
   uint16_t* hS;
   float* HS16;
-  float* y_pairs;   // zeroed when red (valid pairs only)
-  float* y_shared;  // zeroed when red
-  int red;
+  float* y_pairs;   // zeroed when red_r (valid pairs only)
+  float* y_shared;  // zeroed when red_s
+  int red_r, red_s;
 };
 
 __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
@@ -923,7 +923,7 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
   }
   const int rows = shared ? f.Fs : f.F;
   const int KP = shared ? f.kp_s : f.kp_r;
-  if (f.red) {
+  if (shared ? f.red_s : f.red_r) {
     float* y = shared ? f.y_shared + (size_t)src * f.d : f.y_pairs + (size_t)src * f.d;
     for (int c = rg * 32 + lane; c < f.d; c += rows) y[c] = 0.0f;
   }
@@ -1055,7 +1055,9 @@ Split plan_phase(int phase, int T, int k, int E, int nb_r, int rows_r, int nb_s,
         kp *= 2;
       s.kp_s = kp;
     } else {
-      s.kp_s = (s.kp_r == 2 && s.C_s % 2 == 0) ? 2 : 1;
+      // a shared tile spans all of K (a routed row group only a few blocks): two K parts keep its
+      // items from outlasting the routed work
+      s.kp_s = (s.C_s % 2 == 0) ? 2 : 1;
     }
     s.cpp_s = s.C_s / s.kp_s;
   }
@@ -1234,8 +1236,9 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     if (S && p.cb_s <= 0) return cudaErrorInvalidValue;
     p.rg_r = p.rows_r / (16 * RT);
     p.tiles_s = S ? p.rows_s / 16 : 0;
-    p.red = (phase == 2 && p.kp_r == 2) ? 1 : 0;
-    if (phase == 2 && S && p.kp_s != p.kp_r) return cudaErrorInvalidValue;
+    p.red_r = (phase == 2 && p.kp_r == 2) ? 1 : 0;
+    p.red_s = (phase == 2 && S && p.kp_s == 2) ? 1 : 0;
+    if (phase == 2 && (p.kp_r > 2 || p.kp_s > 2)) return cudaErrorInvalidValue;
     p.fd_kps = make_fdiv((unsigned)p.kp_s);
     p.fd_tkps = make_fdiv((unsigned)std::max(1, p.tiles_s * p.kp_s));
     p.fd_kpr = make_fdiv((unsigned)p.kp_r);
@@ -1282,7 +1285,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
       fp.HS16 = const_cast<float*>(p.HS16);
       fp.y_pairs = p.y_pairs;
       fp.y_shared = p.y_shared;
-      fp.red = p.red;
+      fp.red_r = p.red_r;
+      fp.red_s = p.red_s;
       const long long warps = (long long)fp.P * (p.F / 32) + (S ? (long long)a.T * (p.Fs / 32) : 0);
       e = launch_k(ffn_finish_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, fp);
       if (e != cudaSuccess) return e;
