@@ -426,8 +426,7 @@ def test_layer_one_expert_all_tokens(cuda_dev):
 
 @pytest.mark.parametrize("E,k,T", [(64, 8, 8), (96, 12, 8), (80, 11, 6)])
 def test_layer_decode_many_pairs(cuda_dev, E, k, T):
-    # the decode path holds the routing in registers up to 64 active experts and 64 pairs and reads
-    # it from memory above that: both sides of the bound
+    # decode batches with many (token, expert) pairs: up to 96 pairs over up to 96 active experts
     shape = synth.MoeShape(d=512, E=E, k=k, F=256, F_shared=256, bias_half_width=0.1)
     layer = device_layer(5, 0, shape, 8, cuda_dev)
     x = synth.x_bf16(5, 0, 1, T, shape.d)
