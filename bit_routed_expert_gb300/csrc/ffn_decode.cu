@@ -567,7 +567,7 @@ __host__ __device__ __forceinline__ PkgLayout pkg_layout(int T, int d) {
 
 // grid (d/256, T), 256 threads: thread i owns value i of block b of token t.
 __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restrict__ x, int T, int d,
-                                                       unsigned char* __restrict__ pkg) {
+                                                       unsigned char* __restrict__ pkg, int* __restrict__ counters) {
   // x was final before the preceding launch (the router) passed its own wait, and nothing before
   // this kernel touches the package, so the work runs first and the wait (which the kernels
   // after this one rely on) comes last: behind a router that triggers early, it overlaps it
@@ -601,6 +601,9 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
     dst[limb_pos(j, 2)] = (uint16_t)lo;
   }
   pdl_wait();
+  // both phases' item counters start from zero (behind the wait every earlier launch, the previous
+  // call on this workspace included, has completed)
+  if (b == 0 && t == 0 && i < 2) counters[i] = 0;
 }
 
 // ----------------------------------------------------------------------------
@@ -638,6 +641,7 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
   it.id = -1;
   int src[8];
   long long t_last = clock64();
+  bool triggered = false;
   while (true) {
     bool acted = false;
     if (!done) {
@@ -690,6 +694,12 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
         set_err(p.err, BRE_DEVERR_TIMEOUT);   // the consumer stopped releasing stages
         done = true;
       }
+    }
+    if (PHASE == 1 && !triggered && !__any_sync(lanes, more)) {
+      // every item of this launch has been taken: the finishing launch (and, behind it, the down
+      // projection's weight copies) may be scheduled on the SMs that this launch's CTAs leave
+      pdl_launch_dependents();
+      triggered = true;
     }
     if (__all_sync(lanes, done)) break;
     if (!__any_sync(lanes, acted)) __nanosleep(64);
@@ -845,7 +855,11 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   int* desc = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(full) + BAR_BYTES);   // [consumer][slot][16]
   unsigned char* xprep = reinterpret_cast<unsigned char*>(desc) + DESC_BYTES;
 
-  pdl_wait();
+  // Phase 1 waits for the activation package first.  Phase 2 may be scheduled before the finishing
+  // launch completes (that launch lets it start at once): its producer reads only the weights, the
+  // routing and its item counter, all final before the finishing launch began, so only the
+  // consumers, which read h, wait.
+  if (PHASE == 1) pdl_wait();
   if (threadIdx.x < nc * NS) {
     mbar_init(&full[threadIdx.x], 1);
     mbar_init(&empty[threadIdx.x], 1);
@@ -854,7 +868,6 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   fence_mbar_init();
   __syncthreads();
   const PkgLayout PL = pkg_layout(p.T, p.d);
-  if (blockIdx.x == 0 && threadIdx.x == 0) p.counters[PHASE == 1 ? 1 : 0] = 0;
 
   if (warp == nc) {
     if (PHASE == 1 && lane == 0) {
@@ -872,6 +885,7 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   const unsigned char* xF = xprep + PL.xf;                              // [T][xstride], shared memory
   const unsigned char* xLg = p.pkg + PL.xl;                             // [T][xlstride], global memory
   const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
+  if (PHASE == 2) pdl_wait();
   if (PHASE == 1 && !mbar_wait_bounded(pkg_bar, 0, p.wait)) {
     if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
     mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT);   // the package copy lands before this warp leaves
@@ -903,7 +917,12 @@ struct FinishParams {
   int red_r, red_s;
 };
 
+// The launch lets the down projection be scheduled at once: that kernel's producers start the
+// weight copies on the SMs this launch and the gate/up launch leave, and its consumers wait for
+// this grid.  (Fewer, grid-stride CTAs, which leave more SMs, were measured slower: 64 CTAs
+// +1.5 us at T = 8, +99 us on the 24-layer verify pass.)
 __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
+  pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -1194,7 +1213,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   const int sms = device_sm_count();
   const int smem_max = device_max_smem_optin();
   {
-    const cudaError_t le = launch_k(ffn_prep_kernel, dim3(p.d / 256, a.T), dim3(256), 0, s, a.x, a.T, p.d, pkg_w);
+    const cudaError_t le =
+        launch_k(ffn_prep_kernel, dim3(p.d / 256, a.T), dim3(256), 0, s, a.x, a.T, p.d, pkg_w, p.counters);
     if (le != cudaSuccess) return le;
   }
   int kp_r1 = 1, kp_s1 = 1;
