@@ -916,7 +916,7 @@ def host_cpu():
 
 def decode_config(T: int, engram: bool, ws: int) -> dict:
     """The decode line's config (the reference arm reports the same)."""
-    return {"workload": "decode MoE layer T=8" + (" + Engram gather" if engram else "") + " (V4.1 shape)",
+    return {"workload": f"decode MoE layer T={T}" + (" + Engram gather" if engram else "") + " (V4.1 shape)",
             "T": T, "d": 4096, "E": 384, "k": 6, "d_ff": 2048, "shared_d_ff": 2048, "route_bias": "U(-0.5,0.5)",
             "expert_format": "Q2_K (84 B / 256)", "shared_format": "Q8_0 (34 B / 32)",
             "engram": "2 tables x 4194304 rows x 264 B, 8 heads/table", "token_sets": N_SETS,
