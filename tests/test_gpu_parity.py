@@ -389,6 +389,61 @@ def test_permute_bad_ids(cuda_dev):
     assert int(err) & 1
 
 
+@pytest.mark.parametrize("T", [5, 40])
+def test_expert_ffn_pairs_with_invalid_ids(cuda_dev, T):
+    """moe_expert_ffn on a permutation whose ids include -1 and E (both paths: T = 5 decode, T = 40
+    grouped GEMM): every valid pair's y row and the shared expert's rows match the oracle's expert
+    FFN of that token; the rows of the parked invalid pairs are not written."""
+    shape = synth.MoeShape(d=512, E=8, k=3, F=256, F_shared=256, bias_half_width=0.1)
+    lw = synth.layer_weights(11, 0, shape)
+    routed = api.routed_weights(lw.gate.to(cuda_dev), lw.up.to(cuda_dev), lw.down.to(cuda_dev), shape.d, shape.F)
+    shared = FfnWeights(lw.sh_gate.to(cuda_dev), lw.sh_up.to(cuda_dev), lw.sh_down.to(cuda_dev), BRE_FMT_Q8_0,
+                        shape.d, shape.F_shared)
+    rng = np.random.default_rng(T)
+    ids = np.stack([rng.permutation(shape.E)[:shape.k] for _ in range(T)]).astype(np.int32)
+    ids[0, 1] = -1
+    ids[T // 2, 0] = shape.E
+    ids[T - 1, 2] = 1 << 20
+    x = synth.x_bf16(11, 0, T, T, shape.d)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    perm = api.moe_permute(torch.from_numpy(ids).to(cuda_dev), shape.E, dev_err=err)
+    P = T * shape.k
+    y = torch.full((P, shape.d), float("nan"), dtype=torch.float32, device=cuda_dev)
+    ys = torch.full((T, shape.d), float("nan"), dtype=torch.float32, device=cuda_dev)
+    api.moe_expert_ffn(routed, shared, x.to(cuda_dev), shape.k, perm, dev_err=err, y_pairs=y, y_shared=ys)
+    _sync()
+    assert int(err) & 1   # the permutation reported the bad ids
+    n_valid = int(perm["offsets"][shape.E])
+    assert n_valid == P - 3
+    inv = perm["inv"].cpu().numpy()
+    got = y.cpu().double().numpy()
+    assert np.all(np.isnan(got[n_valid:])), "rows of invalid pairs were written"
+    rows, refs = [], []
+    for q in range(P):
+        t, e = q // shape.k, int(ids.reshape(-1)[q])
+        if not 0 <= e < shape.E:
+            continue
+        refs.append(oracle.expert_ffn(BRE_FMT_Q2_K, lw.gate[e].numpy(), lw.up[e].numpy(), lw.down[e].numpy(),
+                                      shape.d, shape.F, x[t:t + 1])[0])
+        rows.append(got[inv[q]])
+    refs.append(oracle.expert_ffn(BRE_FMT_Q8_0, lw.sh_gate.numpy(), lw.sh_up.numpy(), lw.sh_down.numpy(), shape.d,
+                                  shape.F_shared, x))
+    rows.append(ys.cpu().double().numpy())
+    ref, g = np.concatenate([r.reshape(-1, shape.d) for r in refs]), np.concatenate([r.reshape(-1, shape.d) for r in rows])
+    assert np.all(np.isfinite(g))
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    err = np.abs(g - ref)
+    if T <= 8:
+        # the decode path: the layer bar on these intermediate outputs (exact weights, h in BF16)
+        assert float(err.max()) <= 1e-2 * rms
+    else:
+        # the grouped GEMM holds the dequantised weights and h in BF16, two roundings of at most
+        # 2^-9 each per product term that the layer's weighted sum of pairs averages down: the
+        # intermediate rows are held to 1e-2 of rms in the rms of the error and 2e-2 in its maximum
+        assert float(np.sqrt(np.mean(err * err))) <= 1e-2 * rms
+        assert float(err.max()) <= 2e-2 * rms
+
+
 # --------------------------------------------------------------------------- #
 # MoE layer
 # --------------------------------------------------------------------------- #
