@@ -434,14 +434,13 @@ __global__ void __cluster_dims__(1, RC_CLUSTER, 1) __launch_bounds__(RC_THREADS)
       }
     }
   }
+  if (!wm.use) cp_async_wait_all();
+  __syncthreads();   // x staged; the slice barrier's initialisation is visible to every thread
   if (wm.use) {
     // bounded: on a timeout the error word is set and the CTA carries on (it must still reach
     // the cluster barriers its peers wait on)
     if (!mbar_wait_bounded(&wbar, 0, RC_WAIT_LIMIT) && err && tid == 0) atomicOr(err, BRE_DEVERR_TIMEOUT);
-  } else {
-    cp_async_wait_all();
   }
-  __syncthreads();
   // partial j of expert e: rows c = j + 32 i in ascending i, fmaf from +0; the operands of eight
   // rows are loaded before their FMAs (one warp per scheduler: the loads' latency is not hidden
   // by other warps)
