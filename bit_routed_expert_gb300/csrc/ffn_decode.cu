@@ -1085,8 +1085,8 @@ Split plan_phase(int phase, int T, int k, int E, int nb_r, int rows_r, int nb_s,
 
 }  // namespace
 
-// Leading bytes of the FFN workspace that hold the decode path's work counters; every call
-// leaves them at zero.
+// Leading bytes of the FFN workspace that hold the decode path's item counters (the packing
+// kernel of every decode call clears them behind its wait).
 size_t ffn_reserved_bytes(int k, int d, int F, int Fs) {
   (void)k, (void)d, (void)F, (void)Fs;
   return 1024;

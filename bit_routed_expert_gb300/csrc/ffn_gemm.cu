@@ -693,7 +693,7 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int K) {
 
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
-  // the reserved prefix stays with the decode path's counters, which must keep their zeros
+  // the reserved prefix stays with the decode path's item counters (each decode call clears them)
   size_t s = ffn_reserved_bytes(k, d, F, Fs) + ((sizeof(Plan) + 1023) & ~(size_t)1023);
   s += ((P + T) * d * 2 + 1023) & ~(size_t)1023;     // gathered activations
   s += (P * F * 2 + 1023) & ~(size_t)1023;           // routed intermediate

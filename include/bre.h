@@ -208,9 +208,10 @@ bre_status bre_repack_q2k_r16(const void *src, void *dst, int n_matrices, int ro
  *   token); y_pairs [T*k][d] FP32 out, row q = permuted position q (rows of
  *   pairs with an invalid id are not written); y_shared [T][d] FP32 out.
  *   ws: moe_expert_ffn_workspace(T, ...) bytes, zero-filled once after allocation.
- *   Its leading part holds counters that each call leaves at zero again; a
- *   workspace sized for T serves every call with T' <= T (same k, d, d_ff,
- *   d_ff_shared).  Calls sharing one workspace must be ordered.  The workspace
+ *   Its leading part holds the decode path's (T <= 8) item counters, which each
+ *   such call clears before use; a workspace sized for T serves every call with
+ *   T' <= T (same k, d, d_ff, d_ff_shared).  Calls sharing one workspace must be
+ *   ordered.  The workspace
  *   must not overlap any buffer of the call enqueued just before this one on the
  *   stream (for T <= 8 its first kernel packs x into the workspace while a
  *   preceding moe_route_permute may still be running; it reads only x_bf16).
@@ -282,9 +283,8 @@ bre_status engram_inject(const uint8_t *table, int64_t n_rows, const int64_t *ro
  * 0 restores the defaults (about 1 s on the decode path, 2 s on the grouped-GEMM path).  A wait
  * that runs out sets BRE_DEVERR_TIMEOUT in the call's dev_err; the kernel then waits, with the
  * default budget, for the copies and tensor-core operations it has in flight, frees its tensor
- * memory and returns, and that call's outputs are invalid.  The workspace's counters are
- * restored by the same call's later launches, so the next call on the same workspace needs
- * nothing done to it.  A small budget exercises that path (the ROCm cached-expert notes of the
+ * memory and returns, and that call's outputs are invalid.  The next call on the same workspace
+ * needs nothing done to it (the decode path clears its counters at the start of every call).  A small budget exercises that path (the ROCm cached-expert notes of the
  * strix-llama.cpp issue: errors surface after synchronisation rather than as a trap); serving
  * code leaves the default.  Negative: BRE_ERR_ARG. */
 bre_status bre_set_ffn_wait_limit(int64_t cycles);
