@@ -103,7 +103,7 @@ struct DecParams {
   int xstride, xlstride;     // bytes per token of the package's fragment-order x and limb rows
   const uint16_t* hf;        // phase 2: routed h (BF16), fragment order: [P][F/256][256]
   const uint16_t* hl;        // phase 2: routed 16-row sums of h, 3 limbs: [P][F/256][3][4][4]
-  const uint16_t* hS;        // phase 2: shared h, natural, 2 limbs: [T][2][Fs]
+  const uint16_t* hS;        // phase 2: shared h (BF16), natural order: [T][Fs]
   const float* HS16;         // phase 2: shared 16-row sums of h: [T][Fs/16]
   float* part_r;             // phase 1 partial sums: [pair][tile][K part][gate|up][16 rows]
   float* part_s;             // phase 1 partial sums: [token][tile][K part][gate|up][16 rows]
@@ -474,25 +474,22 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb_rt
 }
 
 // ----------------------------------------------------------------------------
-// phase 2, shared Q8_0 down: 16 rows over one chunk; B = h limbs (natural order)
+// phase 2, shared Q8_0 down: 16 rows over one chunk; B = h (BF16, natural order)
 // ----------------------------------------------------------------------------
 template <int CB>
-__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_rt, int c, int g, int t, int Fs,
-                                             const uint16_t* hrow_g,  // hS[tok_g][0][:]
+__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_rt, int c, int g, int t,
+                                             const uint16_t* hrow_g,  // hS[tok_g][:]
                                              const float* hs16_0, const float* hs16_1, uint32_t k43, float (&acc)[4]) {
   const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q80_BB;
-  // B (both limbs of h) and the 16-row sums of block bl + 1 load while block bl is processed
-  auto load_b = [&](int bq, uint2 (&b)[4], float (&xs2)[2]) {
+  // B and the 16-row sums of block bl + 1 load while block bl is processed
+  auto load_b = [&](int bq, uint2 (&b)[2], float (&xs2)[2]) {
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      b[2 * hf] = __ldg(reinterpret_cast<const uint2*>(hrow_g + 32 * bq + 16 * hf + 4 * t));
-      b[2 * hf + 1] = __ldg(reinterpret_cast<const uint2*>(hrow_g + Fs + 32 * bq + 16 * hf + 4 * t));
-    }
+    for (int hf = 0; hf < 2; ++hf) b[hf] = __ldg(reinterpret_cast<const uint2*>(hrow_g + 32 * bq + 16 * hf + 4 * t));
     xs2[0] = hs16_0[2 * bq] + hs16_0[2 * bq + 1];
     xs2[1] = hs16_1[2 * bq] + hs16_1[2 * bq + 1];
   };
-  uint2 bcur[4], bnext[4];
+  uint2 bcur[2], bnext[2];
   float xcur[2], xnext[2];
   load_b(c * cb, bcur, xcur);
   for (int bl = 0; bl < cb; ++bl) {
@@ -502,7 +499,7 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_
     uint32_t dd[2];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      const uint2 bh = bcur[2 * hf], blo = bcur[2 * hf + 1];
+      const uint2 bh = bcur[hf];
       uint32_t l01[2], l23[2], h01[2], h23[2];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
@@ -517,8 +514,6 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_
         mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
         mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
       }
-      mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], blo.x, blo.y);
-      mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], blo.x, blo.y);
     }
     const float x0 = xcur[0], x1 = xcur[1];
 #pragma unroll
@@ -529,7 +524,7 @@ __device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_
       acc[i] = fmaf(dv, v, acc[i]);
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) bcur[q] = bnext[q];
+    for (int q = 0; q < 2; ++q) bcur[q] = bnext[q];
     xcur[0] = xnext[0];
     xcur[1] = xnext[1];
   }
@@ -763,13 +758,13 @@ __device__ __forceinline__ void consume(const DecParams& p, int lane, const unsi
         else
           p1_q80_mat<0>(stage, p.cb_s, c1, g, t, xr, x0, x1, p.kc.k43, acc[0]);
       } else {
-        const uint16_t* hr = p.hS + (size_t)dg * 2 * p.Fs;
+        const uint16_t* hr = p.hS + (size_t)dg * p.Fs;
         const float* h0 = p.HS16 + (size_t)d0 * (p.Fs / 16);
         const float* h1 = p.HS16 + (size_t)d1 * (p.Fs / 16);
         if (p.cb_s == 8)
-          p2_q80_chunk<8>(stage, 8, c1, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
+          p2_q80_chunk<8>(stage, 8, c1, g, t, hr, h0, h1, p.kc.k43, acc[0]);
         else
-          p2_q80_chunk<0>(stage, p.cb_s, c1, g, t, p.Fs, hr, h0, h1, p.kc.k43, acc[0]);
+          p2_q80_chunk<0>(stage, p.cb_s, c1, g, t, hr, h0, h1, p.kc.k43, acc[0]);
       }
     } else {
       const int b0 = c1;
@@ -898,8 +893,8 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
 // ----------------------------------------------------------------------------
 // finish: for every (pair or token, row) add the K-part partial sums of gate and up in order
 // 0..KP-1, form h = silu(gate) * up and store it in the layouts phase 2 reads (routed: BF16 of
-// h * 4^-e in the fragment order plus three limbs of each 16-row sum of the BF16 h; shared: two
-// limbs in natural order plus FP32 16-row sums).  One warp per 32 rows of one pair/token.  When
+// h * 4^-e in the fragment order plus three limbs of each 16-row sum of the BF16 h; shared: the
+// BF16 h in natural order plus FP32 16-row sums of it).  One warp per 32 rows of one pair/token.  When
 // phase 2 adds two K parts into its outputs, the same warps zero those outputs first.
 // ----------------------------------------------------------------------------
 struct FinishParams {
@@ -966,13 +961,11 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
     }
   }
   const float h = silu_mul(gv, uv);
-  uint32_t hi, lo;
-  split_bf16x2(h, hi, lo);
-  float hq = bf16_bits_to_f32(hi) + bf16_bits_to_f32(lo);
+  const uint32_t hi = f32_to_bf16_rne(h);   // the down projections read h rounded once to BF16
+  float hq = bf16_bits_to_f32(hi);
   const int Fnb = f.F / 256;
   if (shared) {
-    f.hS[((size_t)src * 2 + 0) * f.Fs + row] = (uint16_t)hi;
-    f.hS[((size_t)src * 2 + 1) * f.Fs + row] = (uint16_t)lo;
+    f.hS[(size_t)src * f.Fs + row] = (uint16_t)hi;
   } else {
     int e;
     const int pos = frag_pos(row & 255, &e);
@@ -980,7 +973,6 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
     // commutes with the rounding, so the 16-row sums below use h rounded to BF16
     const float hs = __fmul_rn(h, e == 0 ? 1.0f : (e == 1 ? 0.25f : 0.0625f));
     f.hf[((size_t)src * Fnb + (row >> 8)) * 256 + pos] = (uint16_t)f32_to_bf16_rne(hs);
-    hq = bf16_bits_to_f32(f32_to_bf16_rne(h));
   }
   // 16-row sums of the limb values (half warps)
 #pragma unroll
@@ -1114,7 +1106,7 @@ DecWs dec_ws_layout(int T, int k, int E, int d, int F, int Fs) {
   w.hf = up256(w.pkg + pkg_layout(T, d).total);
   w.hl = up256(w.hf + P * (F / 256) * 256 * 2);
   w.hS = up256(w.hl + P * (F / 256) * 48 * 2);
-  w.HS16 = up256(w.hS + (size_t)T * 2 * Fs * 2);
+  w.HS16 = up256(w.hS + (size_t)T * Fs * 2);
   w.part_r = up256(w.HS16 + (size_t)T * (Fs / 16) * 4);
   w.part_s = up256(w.part_r + pr);
   w.total = up256(w.part_s + (Fs > 0 ? ps : 0));
