@@ -690,9 +690,10 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
         done = true;
       }
     }
-    if (PHASE == 1 && !triggered && !__any_sync(lanes, more)) {
-      // every item of this launch has been taken: the finishing launch (and, behind it, the down
-      // projection's weight copies) may be scheduled on the SMs that this launch's CTAs leave
+    if (!triggered && !__any_sync(lanes, more)) {
+      // every item of this launch has been taken: the next launch (after gate/up the finishing
+      // launch and, behind it, the down projection's weight copies; after down whatever reads y,
+      // which waits for this grid before it does) may be scheduled on the SMs this launch leaves
       pdl_launch_dependents();
       triggered = true;
     }
