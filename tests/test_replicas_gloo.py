@@ -33,7 +33,7 @@ def _worker(rank, ws, port, out):
 def test_two_replicas_max_time_and_job_throughput():
     ws = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of this (threaded) process
         out = m.dict()
         mp.start_processes(_worker, args=(ws, port, out), nprocs=ws, start_method="spawn")
         res = dict(out)
