@@ -517,6 +517,17 @@ def run_engram(args, ws, rank, local, tables=None):
     # their mean over the calls is the unbiased figure (the median picks one of the steps)
     avg = statistics.fmean(ms)
     alg = T * 2 * ENGRAM_H * 264 + T * 2 * ENGRAM_H * 8 + T * 512 * 2
+    # Back-to-back figure: one graph of BATCH calls over BATCH distinct id sets, L2 flushed before
+    # each replay, time / BATCH (the launch ramp and tail of a call overlap the next one's)
+    BATCH = 20
+    ids_b = [torch.from_numpy(synth.engram_ids_ngram(SEED + 1000 + 17 * s + rank, T, 2, ENGRAM_H, ENGRAM_ROWS)).to(dev)
+             for s in range(BATCH)]
+    g = api.StepGraph(lambda: [api.engram_gather_decode(tables, ids_b[j], out=out) for j in range(BATCH)])
+    n_rep = max(3, min(args.steps, 20))
+    ms_b = timed(lambda i: g.replay(), n_rep, flush, stream)
+    per_call_b = statistics.median(ms_b) / BATCH
+    gbs_b = alg / (per_call_b * 1e-3) / 1e9
+    del g, ids_b
     pk = peaks()
     total = max_over_ranks(ws, sum(ms))
     gbs = alg / (avg * 1e-3) / 1e9
@@ -530,6 +541,9 @@ def run_engram(args, ws, rank, local, tables=None):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "traffic": None, "peak_source": pk["source"]},
             "us_mean": round(avg * 1e3, 2), "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms),
+            "back_to_back": {"calls_per_graph": BATCH, "replays": n_rep, "us_per_call": round(per_call_b * 1e3, 2),
+                             "gbs": round(gbs_b, 1), "frac": round(gbs_b / pk["hbm_gbs"], 4),
+                             "l2": "flushed before each replay"},
             "clocks": clk}
 
 
