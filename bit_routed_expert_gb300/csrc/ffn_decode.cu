@@ -39,6 +39,7 @@ namespace bre {
 namespace {
 
 constexpr int NS = 2;                 // ring stages per warp
+constexpr int TAIL_ROUNDS = 1;        // phase 1: finer K parts for about this many items per consumer
 constexpr int STAGE = 5376;           // bytes per stage: four Q2_K_R16 tiles, or 16 Q8_0 rows x 8 blocks
 constexpr int R16 = 1344;             // bytes per Q2_K_R16 tile (16 rows x one block)
 constexpr int MAX_CONS = 15;          // consumer warps (plus one producer warp: 128 registers a
@@ -93,7 +94,11 @@ struct DecParams {
   int tiles_s;         // shared 16-row tiles per matrix
   int kp_r, kp_s;      // K parts of a routed row group / a shared tile
   int cpp_r, cpp_s;    // stages of a routed / shared item (per K part)
-  FDiv fd_kps, fd_tkps, fd_kpr, fd_rgkpr, fd_per_exp, fd_k;
+  // phase 1 tail: the last experts of the active list take kp_t (= 2 kp_r when the row's stages
+  // allow it) K parts of cpp_t stages, so that the items claimed last are short; enough experts
+  // for about tail_items items.  Partial sums of every routed item use the stride kp_t.
+  int kp_t, cpp_t, tail_items;
+  FDiv fd_kps, fd_tkps, fd_kpr, fd_rgkpr, fd_per_exp, fd_k, fd_kpt, fd_rgkpt, fd_per_exp_t;
   const uint16_t* x;
   const int32_t* offsets;
   const int32_t* perm;
@@ -127,10 +132,18 @@ struct Item {
   const uint8_t* src;
 };
 
+// Experts at the end of the active list that take the tail's finer K parts (phase 1): enough
+// of them for about tail_items items, none when the K parts cannot be split further.
+__host__ __device__ __forceinline__ int tail_experts(int n_act, int per_exp_t, int tail_items, int kp_t, int kp_r) {
+  if (kp_t == kp_r || n_act <= 0) return 0;
+  const int n = (tail_items + per_exp_t - 1) / per_exp_t;
+  return n < n_act ? n : n_act;
+}
+
 // Items: the shared expert's (matrix, tile, K part) first, then per active expert (matrix, row
-// group, K part).
+// group, K part); in phase 1 the experts from a_split on take the tail's K parts.
 template <int PHASE>
-__device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_shared_items) {
+__device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_shared_items, int a_split) {
   Item it;
   it.id = id;
   if (id < 0) return it;
@@ -147,13 +160,28 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_sh
     it.src = it.m ? p.sw1 : p.sw0;
   } else {
     const int r = id - n_shared_items;
-    const int a = fdiv(r, p.fd_per_exp);
-    const int r2 = r - a * (p.n_mat * p.rg_r * p.kp_r);
+    const int per_exp = p.n_mat * p.rg_r * p.kp_r;
+    int a, r2, kpn;
+    if (PHASE == 2 || r < a_split * per_exp) {
+      a = fdiv(r, p.fd_per_exp);
+      r2 = r - a * per_exp;
+      it.m = fdiv(r2, p.fd_rgkpr);
+      const int r3 = r2 - it.m * (p.rg_r * p.kp_r);
+      it.grp = fdiv(r3, p.fd_kpr);
+      it.kp = r3 - it.grp * p.kp_r;
+      kpn = 0;
+    } else {
+      const int rt = r - a_split * per_exp;
+      const int at = fdiv(rt, p.fd_per_exp_t);
+      a = a_split + at;
+      r2 = rt - at * (p.n_mat * p.rg_r * p.kp_t);
+      it.m = fdiv(r2, p.fd_rgkpt);
+      const int r3 = r2 - it.m * (p.rg_r * p.kp_t);
+      it.grp = fdiv(r3, p.fd_kpt);
+      it.kp = r3 - it.grp * p.kp_t;
+      kpn = 1;
+    }
     it.shared = false;
-    it.m = fdiv(r2, p.fd_rgkpr);
-    const int r3 = r2 - it.m * (p.rg_r * p.kp_r);
-    it.grp = fdiv(r3, p.fd_kpr);
-    it.kp = r3 - it.grp * p.kp_r;
     it.e = __ldg(p.active + a);
     if ((unsigned)it.e >= (unsigned)p.E) {
       // an expert id the weights do not hold: no columns, and no copy outside the weights
@@ -165,7 +193,7 @@ __device__ __forceinline__ Item decode_item(const DecParams& p, int id, int n_sh
       it.off = __ldg(p.offsets + it.e);
       it.n = __ldg(p.offsets + it.e + 1) - it.off;
     }
-    it.nch = p.cpp_r;
+    it.nch = kpn ? p.cpp_t : p.cpp_r;
     it.src = it.m ? p.rw1 + (long long)it.e * p.rs1 : p.rw0 + (long long)it.e * p.rs0;
   }
   return it;
@@ -192,7 +220,7 @@ __device__ __forceinline__ void issue_stage(const DecParams& p, const Item& it, 
   } else {
     const uint32_t span = (uint32_t)p.bps * R16;
     mbar_arrive_expect_tx(bar, RT * span);
-    const int b0 = (it.kp * p.cpp_r + c) * p.bps;
+    const int b0 = (it.kp * it.nch + c) * p.bps;
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
       const long long tile = (long long)(it.grp * RT + r) * p.nb_r + b0;
@@ -629,7 +657,18 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
   const unsigned lanes = nc >= 32 ? 0xffffffffu : ((1u << nc) - 1u);
   const int n_act = *p.n_active;
   const int n_shared_items = p.has_shared ? p.n_mat * p.tiles_s * p.kp_s : 0;
-  const int n_items = n_shared_items + n_act * p.n_mat * p.rg_r * p.kp_r;
+  const int per_exp_t = p.n_mat * p.rg_r * p.kp_t;
+  const int n_tail = PHASE == 1 ? tail_experts(n_act, per_exp_t, p.tail_items, p.kp_t, p.kp_r) : 0;
+  const int a_split = n_act - n_tail;
+  const int n_items = n_shared_items + a_split * p.n_mat * p.rg_r * p.kp_r + n_tail * per_exp_t;
+  if (PHASE == 1 && blockIdx.x == 0 && lane == 0) {
+    // the first pair of the tail's experts (their pairs come last: the active list and the pair
+    // order both ascend by expert), for the finishing kernel, which reads it behind its wait
+    p.counters[2] = n_tail > 0 ? __ldg(p.offsets + __ldg(p.active + a_split)) : 0x7FFFFFFF;
+  }
+  // each lane's first item is fixed (CTA-major), the rest come from the launch's counter
+  const int n_first = (int)gridDim.x * nc;
+  bool first_claim = true;
   int seq = 0, cc = 0;
   bool more = true, done = false;
   Item it;
@@ -641,12 +680,13 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
     bool acted = false;
     if (!done) {
       if (it.id < 0 && more) {
-        int id = atomicAdd(&p.counters[PHASE - 1], 1);
+        int id = first_claim ? (int)blockIdx.x * nc + lane : n_first + atomicAdd(&p.counters[PHASE - 1], 1);
+        first_claim = false;
         if (id >= n_items) {
           id = -1;
           more = false;
         }
-        it = decode_item<PHASE>(p, id, n_shared_items);
+        it = decode_item<PHASE>(p, id, n_shared_items, a_split);
         cc = 0;
         if (id >= 0) {
 #pragma unroll
@@ -674,7 +714,7 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
         } else {
           dsc[0] = (it.shared ? DF_SHARED : 0) | (cc == 0 ? DF_FIRST : 0) | (cc + 1 == it.nch ? DF_LAST : 0) |
                    (it.m << 4);
-          dsc[1] = it.shared ? it.kp * p.cpp_s + cc : (it.kp * p.cpp_r + cc) * p.bps;
+          dsc[1] = it.shared ? it.kp * p.cpp_s + cc : (it.kp * it.nch + cc) * p.bps;
           dsc[2] = it.grp;
           dsc[3] = it.kp;
           dsc[4] = it.n;
@@ -799,7 +839,7 @@ __device__ __forceinline__ void consume(const DecParams& p, int lane, const unsi
     // it into zeros when the call splits phase 2 into two K parts).
     if (PHASE == 1) {
       const int tiles = shared ? p.tiles_s : p.rows_r / 16;
-      const int KP = shared ? p.kp_s : p.kp_r;
+      const int KP = shared ? p.kp_s : p.kp_t;   // the partial-sum stride
       float* base = shared ? p.part_s : p.part_r;
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
@@ -902,6 +942,8 @@ struct FinishParams {
   const float* part_r;
   const float* part_s;
   int kp_r, kp_s;
+  int kp_t;                  // K parts of the tail's experts, and the routed partial-sum stride
+  const int* tail_pos;       // first pair of the tail's experts (written by the gate/up launch)
   int F, Fs, P, T, E, d;
   const int32_t* offsets;
   uint16_t* hf;
@@ -937,13 +979,14 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
     rg = (int)(w2 % gs);
   }
   const int rows = shared ? f.Fs : f.F;
-  const int KP = shared ? f.kp_s : f.kp_r;
+  const int KP = shared ? f.kp_s : (src >= __ldg(f.tail_pos) ? f.kp_t : f.kp_r);   // parts to add
+  const int KS = shared ? f.kp_s : f.kp_t;                                       // their stride
   if (shared ? f.red_s : f.red_r) {
     float* y = shared ? f.y_shared + (size_t)src * f.d : f.y_pairs + (size_t)src * f.d;
     for (int c = rg * 32 + lane; c < f.d; c += rows) y[c] = 0.0f;
   }
   const int row = rg * 32 + lane, tile = row >> 4, r = row & 15;
-  const float* pc = (shared ? f.part_s : f.part_r) + ((size_t)src * (rows / 16) + tile) * KP * 32 + r;
+  const float* pc = (shared ? f.part_s : f.part_r) + ((size_t)src * (rows / 16) + tile) * KS * 32 + r;
   // every part's load is issued before the sum (up to four at once)
   float gv = 0.0f, uv = 0.0f;
   for (int q0 = 0; q0 < KP; q0 += 4) {
@@ -1031,7 +1074,7 @@ long long expected_active(int T, int k, int E) {
 }
 
 struct Split {
-  int bps, kp_r, cpp_r, cb_s, whole_s, C_s, kp_s, cpp_s;
+  int bps, kp_r, cpp_r, kp_t, cpp_t, cb_s, whole_s, C_s, kp_s, cpp_s;
 };
 
 // Stage and K-part plan of one phase (the same on every call with the same shapes, so the
@@ -1051,6 +1094,9 @@ Split plan_phase(int phase, int T, int k, int E, int nb_r, int rows_r, int nb_s,
     s.kp_r = (stages_row % 2 == 0 && n_est * (rows_r / (16 * RT)) < target) ? 2 : 1;
   }
   s.cpp_r = stages_row / s.kp_r;
+  // phase 1's tail experts: twice the K parts when the row's stages divide that way
+  s.kp_t = (phase == 1 && stages_row % (2 * s.kp_r) == 0) ? 2 * s.kp_r : s.kp_r;
+  s.cpp_t = stages_row / s.kp_t;
   s.cb_s = 1;
   s.whole_s = 0;
   s.C_s = 1;
@@ -1079,7 +1125,8 @@ Split plan_phase(int phase, int T, int k, int E, int nb_r, int rows_r, int nb_s,
 }  // namespace
 
 // Leading bytes of the FFN workspace that hold the decode path's item counters (the packing
-// kernel of every decode call clears them behind its wait).
+// kernel of every decode call clears them behind its wait) and the first pair of the gate/up
+// launch's tail experts (written by that launch, read by the finishing launch).
 size_t ffn_reserved_bytes(int k, int d, int F, int Fs) {
   (void)k, (void)d, (void)F, (void)Fs;
   return 1024;
@@ -1099,7 +1146,7 @@ constexpr int PLAN_WARPS = 152 * 13;
 DecWs dec_ws_layout(int T, int k, int E, int d, int F, int Fs) {
   const size_t P = (size_t)T * k;
   const Split s1 = plan_phase(1, T, k, E, d / 256, F, d / 32, Fs > 0, PLAN_WARPS);
-  const size_t pr = P * (F / 16) * s1.kp_r * 2 * 16 * 4;
+  const size_t pr = P * (F / 16) * s1.kp_t * 2 * 16 * 4;
   const size_t ps = (size_t)T * (Fs / 16) * s1.kp_s * 2 * 16 * 4;
   auto up256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
   DecWs w;
@@ -1210,7 +1257,7 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
         launch_k(ffn_prep_kernel, dim3(p.d / 256, a.T), dim3(256), 0, s, a.x, a.T, p.d, pkg_w, p.counters);
     if (le != cudaSuccess) return le;
   }
-  int kp_r1 = 1, kp_s1 = 1;
+  int kp_r1 = 1, kp_s1 = 1, kp_t1 = 1;
   for (int phase = 1; phase <= 2; ++phase) {
     const int RT = phase == 1 ? RT1 : RT2;
     if (phase == 1) {
@@ -1242,6 +1289,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     p.bps = sp.bps;
     p.kp_r = sp.kp_r;
     p.cpp_r = sp.cpp_r;
+    p.kp_t = sp.kp_t;
+    p.cpp_t = sp.cpp_t;
     p.cb_s = sp.cb_s;
     p.whole_s = sp.whole_s;
     p.kp_s = sp.kp_s;
@@ -1257,6 +1306,9 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     p.fd_kpr = make_fdiv((unsigned)p.kp_r);
     p.fd_rgkpr = make_fdiv((unsigned)(p.rg_r * p.kp_r));
     p.fd_per_exp = make_fdiv((unsigned)(p.n_mat * p.rg_r * p.kp_r));
+    p.fd_kpt = make_fdiv((unsigned)p.kp_t);
+    p.fd_rgkpt = make_fdiv((unsigned)(p.rg_r * p.kp_t));
+    p.fd_per_exp_t = make_fdiv((unsigned)(p.n_mat * p.rg_r * p.kp_t));
     p.fd_k = make_fdiv((unsigned)a.k);
     // tensor maps for the shared expert's chunked rows (unused when whole tiles fit a stage)
     CUtensorMap ms0{}, ms1{};
@@ -1275,6 +1327,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
     if (phase == 1) {
       kp_r1 = p.kp_r;
       kp_s1 = p.kp_s;
+      kp_t1 = p.kp_t;
+      p.tail_items = TAIL_ROUNDS * sms * nc;   // about one item per consumer warp
       e = cudaFuncSetAttribute(ffn_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       e = launch_k(ffn_decode_kernel<1>, dim3(sms), dim3(nw * 32), smem, s, p, ms0, ms1);
@@ -1285,6 +1339,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
       fp.part_s = p.part_s;
       fp.kp_r = kp_r1;
       fp.kp_s = kp_s1;
+      fp.kp_t = kp_t1;
+      fp.tail_pos = p.counters + 2;
       fp.F = p.F;
       fp.Fs = p.Fs;
       fp.P = (int)((size_t)a.T * a.k);

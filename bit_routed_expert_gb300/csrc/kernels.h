@@ -57,8 +57,8 @@ struct FfnArgs {
   int32_t* err;
 };
 constexpr int DECODE_T_MAX = 8;   // larger batches take the grouped-GEMM path
-// Leading bytes of the FFN workspace that hold the decode path's item counters (cleared by
-// every decode call); both paths place everything else after them.
+// Leading bytes of the FFN workspace that hold the decode path's item counters and tail
+// position (set by every decode call); both paths place everything else after them.
 size_t ffn_reserved_bytes(int k, int d, int F, int Fs);
 size_t ffn_ws_bytes(int T, int k, int E, int d, int F, int Fs);
 size_t ffn_gemm_ws_bytes(int T, int k, int d, int F, int Fs);

@@ -208,8 +208,8 @@ bre_status bre_repack_q2k_r16(const void *src, void *dst, int n_matrices, int ro
  *   token); y_pairs [T*k][d] FP32 out, row q = permuted position q (rows of
  *   pairs with an invalid id are not written); y_shared [T][d] FP32 out.
  *   ws: moe_expert_ffn_workspace(T, ...) bytes, zero-filled once after allocation.
- *   Its leading part holds the decode path's (T <= 8) item counters, which each
- *   such call clears before use; a workspace sized for T serves every call with
+ *   Its leading part holds the decode path's (T <= 8) item counters and a
+ *   scheduling word, which each such call sets before use; a workspace sized for T serves every call with
  *   T' <= T (same k, d, d_ff, d_ff_shared).  Calls sharing one workspace must be
  *   ordered.  The workspace
  *   must not overlap any buffer of the call enqueued just before this one on the
