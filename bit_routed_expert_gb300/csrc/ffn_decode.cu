@@ -593,7 +593,9 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
                                                        unsigned char* __restrict__ pkg, int* __restrict__ counters) {
   // x was final before the preceding launch (the router) passed its own wait, and nothing before
   // this kernel touches the package, so the work runs first and the wait (which the kernels
-  // after this one rely on) comes last: behind a router that triggers early, it overlaps it
+  // after this one rely on) comes last: behind a router that triggers early, it overlaps it.
+  // The gate/up launch may start at once: before its own wait it reads only weights.
+  pdl_launch_dependents();
   const int b = blockIdx.x, t = blockIdx.y, i = threadIdx.x, lane = i & 31;
   const PkgLayout L = pkg_layout(T, d);
   const uint32_t v = x[(size_t)t * d + 256 * b + i];
@@ -652,11 +654,51 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
 // lane's wait holds up the others; a round in which no lane could act sleeps briefly.
 template <int PHASE>
 __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, unsigned char* ring, uint64_t* full,
-                                        uint64_t* empty, int* desc, const CUtensorMap* ms0, const CUtensorMap* ms1) {
+                                        uint64_t* empty, int* desc, const CUtensorMap* ms0, const CUtensorMap* ms1,
+                                        uint64_t* pkg_bar, unsigned char* xprep, int pkg_bytes) {
   constexpr int RT = (PHASE == 1) ? RT1 : RT2;
   const unsigned lanes = nc >= 32 ? 0xffffffffu : ((1u << nc) - 1u);
-  const int n_act = *p.n_active;
   const int n_shared_items = p.has_shared ? p.n_mat * p.tiles_s * p.kp_s : 0;
+  int seq = 0, cc = 0;
+  Item it;
+  it.id = -1;
+  int src[8];
+  // writes the descriptor of stage cc of `it` into slot `slot` and arms the slot's copies
+  auto arm = [&](int slot) {
+    int* dsc = desc + slot * 16;
+    dsc[0] = (it.shared ? DF_SHARED : 0) | (cc == 0 ? DF_FIRST : 0) | (cc + 1 == it.nch ? DF_LAST : 0) | (it.m << 4);
+    dsc[1] = it.shared ? it.kp * p.cpp_s + cc : (it.kp * it.nch + cc) * p.bps;
+    dsc[2] = it.grp;
+    dsc[3] = it.kp;
+    dsc[4] = it.n;
+    dsc[5] = it.off;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dsc[8 + c] = src[c];
+    issue_stage<RT>(p, it, cc, ring + slot * STAGE, &full[slot], 0, ms0, ms1);
+    if (++cc == it.nch) it.id = -1;
+    ++seq;
+  };
+  // each lane's first item is fixed (CTA-major), the rest come from the launch's counter
+  bool first_claim = true;
+  if (PHASE == 1) {
+    // A first item of the shared expert's needs only weights and shapes, so its first stage is
+    // armed before the wait (the packing kernel lets this launch start at once, on the SMs the
+    // router leaves); the package, the routing and the counters are read behind the wait.
+    const int id0 = (int)blockIdx.x * nc + lane;
+    if (id0 < n_shared_items) {
+      it = decode_item<PHASE>(p, id0, n_shared_items, 0);
+      first_claim = false;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) src[c] = c < it.n ? c : 0;
+      arm(0);
+    }
+    pdl_wait();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(pkg_bar, (uint32_t)pkg_bytes);
+      bulk_g2s(xprep, p.pkg, (uint32_t)pkg_bytes, pkg_bar);   // x fragments (a multiple of 16 bytes)
+    }
+  }
+  const int n_act = *p.n_active;
   const int per_exp_t = p.n_mat * p.rg_r * p.kp_t;
   const int n_tail = PHASE == 1 ? tail_experts(n_act, per_exp_t, p.tail_items, p.kp_t, p.kp_r) : 0;
   const int a_split = n_act - n_tail;
@@ -666,14 +708,8 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
     // order both ascend by expert), for the finishing kernel, which reads it behind its wait
     p.counters[2] = n_tail > 0 ? __ldg(p.offsets + __ldg(p.active + a_split)) : 0x7FFFFFFF;
   }
-  // each lane's first item is fixed (CTA-major), the rest come from the launch's counter
   const int n_first = (int)gridDim.x * nc;
-  bool first_claim = true;
-  int seq = 0, cc = 0;
   bool more = true, done = false;
-  Item it;
-  it.id = -1;
-  int src[8];
   long long t_last = clock64();
   bool triggered = false;
   while (true) {
@@ -706,25 +742,14 @@ __device__ __forceinline__ void produce(const DecParams& p, int nc, int lane, un
       if (mbar_test_wait(&empty[slot], ((seq / NS) & 1) ^ 1)) {
         acted = true;
         t_last = clock64();
-        int* dsc = desc + slot * 16;
         if (it.id < 0) {   // nothing left: an end marker, armed with no bytes
-          dsc[0] = DF_END;
+          desc[slot * 16] = DF_END;
           mbar_arrive_plain(&full[slot]);
           done = true;
+          ++seq;
         } else {
-          dsc[0] = (it.shared ? DF_SHARED : 0) | (cc == 0 ? DF_FIRST : 0) | (cc + 1 == it.nch ? DF_LAST : 0) |
-                   (it.m << 4);
-          dsc[1] = it.shared ? it.kp * p.cpp_s + cc : (it.kp * it.nch + cc) * p.bps;
-          dsc[2] = it.grp;
-          dsc[3] = it.kp;
-          dsc[4] = it.n;
-          dsc[5] = it.off;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) dsc[8 + c] = src[c];
-          issue_stage<RT>(p, it, cc, ring + slot * STAGE, &full[slot], 0, ms0, ms1);
-          if (++cc == it.nch) it.id = -1;
+          arm(slot);
         }
-        ++seq;
       } else if (clock64() - t_last > p.wait) {
         set_err(p.err, BRE_DEVERR_TIMEOUT);   // the consumer stopped releasing stages
         done = true;
@@ -891,11 +916,11 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   int* desc = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(full) + BAR_BYTES);   // [consumer][slot][16]
   unsigned char* xprep = reinterpret_cast<unsigned char*>(desc) + DESC_BYTES;
 
-  // Phase 1 waits for the activation package first.  Phase 2 may be scheduled before the finishing
-  // launch completes (that launch lets it start at once): its producer reads only the weights, the
-  // routing and its item counter, all final before the finishing launch began, so only the
-  // consumers, which read h, wait.
-  if (PHASE == 1) pdl_wait();
+  // Both phases may be scheduled before their predecessor completes (the packing and finishing
+  // launches let them start at once).  Phase 1's producer arms its shared-expert first stages
+  // (weights only) before it waits; phase 2's producer reads only the weights, the routing and
+  // its item counter, all final before the finishing launch began.  The consumers, which read
+  // the package or h, wait.
   if (threadIdx.x < nc * NS) {
     mbar_init(&full[threadIdx.x], 1);
     mbar_init(&empty[threadIdx.x], 1);
@@ -906,13 +931,9 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   const PkgLayout PL = pkg_layout(p.T, p.d);
 
   if (warp == nc) {
-    if (PHASE == 1 && lane == 0) {
-      mbar_arrive_expect_tx(pkg_bar, PL.smem);
-      bulk_g2s(xprep, p.pkg, PL.smem, pkg_bar);   // x fragments (a multiple of 16 bytes)
-    }
     if (lane < nc)
       produce<PHASE>(p, nc, lane, stages + lane * NS * STAGE, full + lane * NS, empty + lane * NS,
-                     desc + lane * NS * 16, &map_s0, &map_s1);
+                     desc + lane * NS * 16, &map_s0, &map_s1, pkg_bar, xprep, PL.smem);
     return;
   }
 
@@ -921,7 +942,7 @@ __global__ void __launch_bounds__((MAX_CONS + 1) * 32, 1)
   const unsigned char* xF = xprep + PL.xf;                              // [T][xstride], shared memory
   const unsigned char* xLg = p.pkg + PL.xl;                             // [T][xlstride], global memory
   const float* X32 = reinterpret_cast<const float*>(p.pkg + PL.x32);   // [T][d/32]
-  if (PHASE == 2) pdl_wait();
+  pdl_wait();
   if (PHASE == 1 && !mbar_wait_bounded(pkg_bar, 0, p.wait)) {
     if (lane == 0) set_err(p.err, BRE_DEVERR_TIMEOUT);
     mbar_wait_bounded(pkg_bar, 0, WAIT_LIMIT);   // the package copy lands before this warp leaves
