@@ -8,11 +8,11 @@
 // once and the work per byte is kept small.  The routed experts are stored in the Q2_K_R16
 // layout (repack.cu): each 1344-byte tile holds one 256-weight block of 16 rows arranged so
 // that lane L of a warp finds the codes of its two fragment rows as one 16-byte word group,
-// and the scale and min nibbles of its sub-blocks in one 8-byte pair.  Each warp owns a
-// two-stage ring in shared memory that the TMA engine fills with one-dimensional bulk copies
-// of whole tiles; the warp dequantises in registers straight into mma.sync A fragments and
-// multiplies by the expert's tokens (N = 8 columns).  Work items are handed out by an atomic
-// counter so that busy SMs take fewer items.
+// and the scale and min nibbles of its sub-blocks in one 8-byte pair.  Each consumer warp owns
+// a two-stage ring in shared memory that a producer warp fills with one-dimensional bulk copies
+// of whole tiles; the consumer dequantises in registers straight into mma.sync A fragments and
+// multiplies by the expert's tokens (N = 8 columns).  After a fixed first item per consumer,
+// work items are handed out by an atomic counter so that busy SMs take fewer items.
 //
 // Exactness: a Q2_K weight is (d*sc)*q - dmin*m.  A fragment register holds two BF16 values
 // sc*q*4^e (e in {0, 1, 2}, exact): a mask leaves the code in place inside the mantissa of 128
