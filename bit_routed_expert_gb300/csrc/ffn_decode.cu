@@ -28,6 +28,8 @@
 // codes (p = s / 8, w = (s / 4) % 2) and in it slots 2u and 2u + 1 (u = s % 4; slot v holds
 // code 8w + v of the sub-blocks 4t + 2p (low half) and 4t + 2p + 1 (high half)); the
 // activations are stored in that order (frag_pos).  Q8_0 uses natural order.
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -72,9 +74,10 @@ static FDiv make_fdiv(unsigned d) {
 
 // Bit patterns held in registers (kernel parameters) rather than rebuilt as immediates inside
 // the loops: m43 = BF16 (128, 128), m128 = (-128, -128), k16384 = (16384, 16384), k43 = the
-// byte 0x43 four times (PRMT source of the exponent byte of 128).
+// byte 0x43 four times (PRMT source of the exponent byte of 128), k64 = the byte 0x64 four
+// times (the high byte of FP16 1024 + u, u < 256).
 struct DecConst {
-  uint32_t m43, m128, k16384, k43;
+  uint32_t m43, m128, k16384, k43, k64;
 };
 
 struct DecParams {
@@ -108,8 +111,8 @@ struct DecParams {
   int xstride, xlstride;     // bytes per token of the package's fragment-order x and limb rows
   const uint16_t* hf;        // phase 2: routed h (BF16), fragment order: [P][F/256][256]
   const uint16_t* hl;        // phase 2: routed 16-row sums of h, 3 limbs: [P][F/256][3][4][4]
-  const uint16_t* hS;        // phase 2: shared h (BF16), natural order: [T][Fs]
-  const float* HS16;         // phase 2: shared 16-row sums of h: [T][Fs/16]
+  const uint16_t* hS16;      // phase 2: shared h as block-scaled FP16 (block_f16), natural order: [T][Fs]
+  const float2* HQ;          // phase 2: per 32-row block of it, (sum of the 32 FP16 values, 2^s): [T][Fs/32]
   float* part_r;             // phase 1 partial sums: [pair][tile][K part][gate|up][16 rows]
   float* part_s;             // phase 1 partial sums: [token][tile][K part][gate|up][16 rows]
   float* y_pairs;
@@ -437,7 +440,7 @@ __device__ __forceinline__ void routed_stage(const unsigned char* stage, int lan
 }
 
 // Q8_0 nibble planes of one row word (4 consecutive int8): (128+lo) and (128+hi') pairs.
-__device__ __forceinline__ void q80_frag(uint32_t w, uint32_t k43, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
+__device__ __forceinline__ void q80_nibbles(uint32_t w, uint32_t k43, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
                                          uint32_t& hi23) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
   const uint32_t hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;
@@ -478,7 +481,7 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb_rt
       for (int rr = 0; rr < 2; ++rr) {
         const unsigned char* base = stage + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
         if (hf == 0) dd[rr] = lds_u16(base);
-        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k43, l01[rr], l23[rr], h01[rr], h23[rr]);
+        q80_nibbles(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k43, l01[rr], l23[rr], h01[rr], h23[rr]);
       }
       if (hf == 0) {
         mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bv.x, bv.y);
@@ -501,60 +504,93 @@ __device__ __forceinline__ void p1_q80_mat(const unsigned char* stage, int cb_rt
   }
 }
 
+// One Q8_0 row word (4 consecutive int8 codes q) as FP16 A fragments: u = q + 128 (flip the
+// sign bit), then 1024 + u exactly (u sits in the mantissa of 1024) for codes 0, 1 and 2, 3.
+__device__ __forceinline__ void q80_frag(uint32_t w, uint32_t k64, uint32_t& f01, uint32_t& f23) {
+  const uint32_t u = w ^ 0x80808080u;
+  f01 = prmt(u, k64, SEL_LO);
+  f23 = prmt(u, k64, SEL_HI);
+}
+
+// h for the shared down projection's MMAs, one 32-value block (one value a lane) at a time:
+// scaled by 2^-s, s from the block's largest magnitude so that every value is below 2^15, and
+// rounded to FP16 (exact for BF16 values in FP16's normal range; smaller ones lose bits below
+// 2^-24 of the block's largest).  Returns the lane's FP16 bits; sum = the FP32 sum of the 32 FP16 values
+// (fixed butterfly order, the same in every lane), scale = 2^s.
+__device__ __forceinline__ uint32_t block_f16(float v, float& sum, float& scale) {
+  float m = fabsf(v);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int sh = 0;
+  if (m > 0.0f) {
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+    sh = min(max(e - 14, -100), 100);
+  }
+  const float down = __uint_as_float((uint32_t)(127 - sh) << 23);   // 2^-s
+  scale = __uint_as_float((uint32_t)(127 + sh) << 23);               // 2^s
+  const __half hv = __float2half_rn(__fmul_rn(v, down));
+  float f = __half2float(hv);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) f = __fadd_rn(f, __shfl_xor_sync(0xffffffffu, f, o));
+  sum = f;
+  return (uint32_t)__half_as_ushort(hv);
+}
+
 // ----------------------------------------------------------------------------
-// phase 2, shared Q8_0 down: 16 rows over one chunk; B = h (BF16, natural order)
+// phase 2, shared Q8_0 down: 16 rows over one chunk (natural k order); B = block-scaled FP16 h of
+// column g, q0 / q1 = (sum, 2^s) of the block for columns 2t, 2t + 1.
+// Per 32-value block: P = sum (1152 + q) b over the FP16 MMAs, so sum q b = P - 1152 * sum b, and
+// the row's d and the column's 2^s scale it back.
 // ----------------------------------------------------------------------------
+// CB > 0 fixes the chunk's block count at compile time (addresses base + immediate); CB == 0 takes cb_rt.
 template <int CB>
-__device__ __forceinline__ void p2_q80_chunk(const unsigned char* stage, int cb_rt, int c, int g, int t,
-                                             const uint16_t* hrow_g,  // hS[tok_g][:]
-                                             const float* hs16_0, const float* hs16_1, uint32_t k43, float (&acc)[4]) {
+__device__ __forceinline__ void q80_chunk(const unsigned char* stage, int cb_rt, int c, int g, int t,
+                                          const uint16_t* brow_g, const float2* q0, const float2* q1, uint32_t k64,
+                                          float (&acc)[4]) {
   const int cb = CB > 0 ? CB : cb_rt;
   const int chunk_bytes = cb * Q80_BB;
-  // B and the 16-row sums of block bl + 1 load while block bl is processed
-  auto load_b = [&](int bq, uint2 (&b)[2], float (&xs2)[2]) {
+  // B and the block's (sum, scale) of block bl + 1 load while block bl is processed
+  auto load_b = [&](int bq, uint2 (&b)[2], float2 (&q)[2]) {
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) b[hf] = __ldg(reinterpret_cast<const uint2*>(hrow_g + 32 * bq + 16 * hf + 4 * t));
-    xs2[0] = hs16_0[2 * bq] + hs16_0[2 * bq + 1];
-    xs2[1] = hs16_1[2 * bq] + hs16_1[2 * bq + 1];
+    for (int hf = 0; hf < 2; ++hf) b[hf] = __ldg(reinterpret_cast<const uint2*>(brow_g + 32 * bq + 16 * hf + 4 * t));
+    q[0] = __ldg(q0 + bq);
+    q[1] = __ldg(q1 + bq);
   };
   uint2 bcur[2], bnext[2];
-  float xcur[2], xnext[2];
-  load_b(c * cb, bcur, xcur);
+  float2 qcur[2], qnext[2];
+  load_b(c * cb, bcur, qcur);
   for (int bl = 0; bl < cb; ++bl) {
     const int bq = c * cb + bl;
-    if (bl + 1 < cb) load_b(bq + 1, bnext, xnext);
-    float Ph[4], Pl[4];
+    if (bl + 1 < cb) load_b(bq + 1, bnext, qnext);
+    float P[4];
     uint32_t dd[2];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      const uint2 bh = bcur[hf];
-      uint32_t l01[2], l23[2], h01[2], h23[2];
+      const uint2 bv = bcur[hf];
+      uint32_t f01[2], f23[2];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const unsigned char* base = stage + (g + 8 * rr) * chunk_bytes + bl * Q80_BB;
         if (hf == 0) dd[rr] = lds_u16(base);
-        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k43, l01[rr], l23[rr], h01[rr], h23[rr]);
+        q80_frag(lds_u32_a2(base + 2 + 16 * hf + 4 * t), k64, f01[rr], f23[rr]);
       }
-      if (hf == 0) {
-        mma_bf16_16816_z(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
-        mma_bf16_16816_z(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
-      } else {
-        mma_bf16_16816(Pl, l01[0], l01[1], l23[0], l23[1], bh.x, bh.y);
-        mma_bf16_16816(Ph, h01[0], h01[1], h23[0], h23[1], bh.x, bh.y);
-      }
+      if (hf == 0)
+        mma_f16_16816_z(P, f01[0], f01[1], f23[0], f23[1], bv.x, bv.y);
+      else
+        mma_f16_16816(P, f01[0], f01[1], f23[0], f23[1], bv.x, bv.y);
     }
-    const float x0 = xcur[0], x1 = xcur[1];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float dv = f16_bits_to_f32(dd[i >> 1]);
-      const float xs = (i & 1) ? x1 : x0;
-      const float v = fmaf(-2304.0f, xs, fmaf(16.0f, Ph[i], Pl[i]));
-      acc[i] = fmaf(dv, v, acc[i]);
+      const float2 q = (i & 1) ? qcur[1] : qcur[0];
+      const float v = fmaf(-1152.0f, q.x, P[i]);
+      acc[i] = fmaf(__fmul_rn(dv, q.y), v, acc[i]);
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) bcur[q] = bnext[q];
-    xcur[0] = xnext[0];
-    xcur[1] = xnext[1];
+    for (int q = 0; q < 2; ++q) {
+      bcur[q] = bnext[q];
+      qcur[q] = qnext[q];
+    }
   }
 }
 
@@ -824,13 +860,13 @@ __device__ __forceinline__ void consume(const DecParams& p, int lane, const unsi
         else
           p1_q80_mat<0>(stage, p.cb_s, c1, g, t, xr, x0, x1, p.kc.k43, acc[0]);
       } else {
-        const uint16_t* hr = p.hS + (size_t)dg * p.Fs;
-        const float* h0 = p.HS16 + (size_t)d0 * (p.Fs / 16);
-        const float* h1 = p.HS16 + (size_t)d1 * (p.Fs / 16);
+        const uint16_t* hr = p.hS16 + (size_t)dg * p.Fs;
+        const float2* q0 = p.HQ + (size_t)d0 * (p.Fs / 32);
+        const float2* q1 = p.HQ + (size_t)d1 * (p.Fs / 32);
         if (p.cb_s == 8)
-          p2_q80_chunk<8>(stage, 8, c1, g, t, hr, h0, h1, p.kc.k43, acc[0]);
+          q80_chunk<8>(stage, 8, c1, g, t, hr, q0, q1, p.kc.k64, acc[0]);
         else
-          p2_q80_chunk<0>(stage, p.cb_s, c1, g, t, hr, h0, h1, p.kc.k43, acc[0]);
+          q80_chunk<0>(stage, p.cb_s, c1, g, t, hr, q0, q1, p.kc.k64, acc[0]);
       }
     } else {
       const int b0 = c1;
@@ -969,8 +1005,8 @@ struct FinishParams {
   const int32_t* offsets;
   uint16_t* hf;
   uint16_t* hl;
-  uint16_t* hS;
-  float* HS16;
+  uint16_t* hS16;
+  float2* HQ;
   float* y_pairs;   // zeroed when red_r (valid pairs only)
   float* y_shared;  // zeroed when red_s
   int red_r, red_s;
@@ -1028,10 +1064,16 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
   const float h = silu_mul(gv, uv);
   const uint32_t hi = f32_to_bf16_rne(h);   // the down projections read h rounded once to BF16
   float hq = bf16_bits_to_f32(hi);
-  const int Fnb = f.F / 256;
   if (shared) {
-    f.hS[(size_t)src * f.Fs + row] = (uint16_t)hi;
-  } else {
+    // the warp's 32 rows are one Q8_0 block of the shared down projection's K: block-scaled FP16
+    float bsum, bscale;
+    const uint32_t h16 = block_f16(hq, bsum, bscale);
+    f.hS16[(size_t)src * f.Fs + row] = (uint16_t)h16;
+    if (lane == 0) f.HQ[(size_t)src * (f.Fs / 32) + rg] = make_float2(bsum, bscale);
+    return;
+  }
+  const int Fnb = f.F / 256;
+  {
     int e;
     const int pos = frag_pos(row & 255, &e);
     // BF16 of h * 4^-e (the down projection's A fragments keep codes in place); a power of two
@@ -1043,19 +1085,15 @@ __global__ void __launch_bounds__(256) ffn_finish_kernel(const FinishParams f) {
 #pragma unroll
   for (int o = 1; o <= 8; o <<= 1) hq += __shfl_xor_sync(0xffffffffu, hq, o);
   if ((lane & 15) == 0) {
-    if (shared) {
-      f.HS16[(size_t)src * (f.Fs / 16) + tile] = hq;
-    } else {
-      const int b2 = tile >> 4, j = tile & 15;
-      const uint32_t h1 = f32_to_bf16_rne(hq);
-      const float r1 = hq - bf16_bits_to_f32(h1);
-      const uint32_t h2 = f32_to_bf16_rne(r1);
-      const uint32_t h3 = f32_to_bf16_rne(r1 - bf16_bits_to_f32(h2));
-      uint16_t* dst = f.hl + ((size_t)src * Fnb + b2) * 48;
-      dst[limb_pos(j, 0)] = (uint16_t)h1;
-      dst[limb_pos(j, 1)] = (uint16_t)h2;
-      dst[limb_pos(j, 2)] = (uint16_t)h3;
-    }
+    const int b2 = tile >> 4, j = tile & 15;
+    const uint32_t h1 = f32_to_bf16_rne(hq);
+    const float r1 = hq - bf16_bits_to_f32(h1);
+    const uint32_t h2 = f32_to_bf16_rne(r1);
+    const uint32_t h3 = f32_to_bf16_rne(r1 - bf16_bits_to_f32(h2));
+    uint16_t* dst = f.hl + ((size_t)src * Fnb + b2) * 48;
+    dst[limb_pos(j, 0)] = (uint16_t)h1;
+    dst[limb_pos(j, 1)] = (uint16_t)h2;
+    dst[limb_pos(j, 2)] = (uint16_t)h3;
   }
 }
 
@@ -1157,7 +1195,7 @@ namespace {
 
 // Workspace of the decode path, in order.
 struct DecWs {
-  size_t pkg, hf, hl, hS, HS16, part_r, part_s, total;
+  size_t pkg, hf, hl, hS16, HQ, part_r, part_s, total;
 };
 
 // A fixed warp count for the split plan (the actual launch may run fewer warps a CTA): keeps the
@@ -1174,9 +1212,9 @@ DecWs dec_ws_layout(int T, int k, int E, int d, int F, int Fs) {
   w.pkg = ffn_reserved_bytes(k, d, F, Fs);
   w.hf = up256(w.pkg + pkg_layout(T, d).total);
   w.hl = up256(w.hf + P * (F / 256) * 256 * 2);
-  w.hS = up256(w.hl + P * (F / 256) * 48 * 2);
-  w.HS16 = up256(w.hS + (size_t)T * Fs * 2);
-  w.part_r = up256(w.HS16 + (size_t)T * (Fs / 16) * 4);
+  w.hS16 = up256(w.hl + P * (F / 256) * 48 * 2);
+  w.HQ = up256(w.hS16 + (size_t)T * Fs * 2);
+  w.part_r = up256(w.HQ + (size_t)T * (Fs / 32) * 8);
   w.part_s = up256(w.part_r + pr);
   w.total = up256(w.part_s + (Fs > 0 ? ps : 0));
   return w;
@@ -1262,13 +1300,13 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
   unsigned char* pkg_w = reinterpret_cast<unsigned char*>(w + L.pkg);
   p.hf = reinterpret_cast<uint16_t*>(w + L.hf);
   p.hl = reinterpret_cast<uint16_t*>(w + L.hl);
-  p.hS = reinterpret_cast<uint16_t*>(w + L.hS);
-  p.HS16 = reinterpret_cast<float*>(w + L.HS16);
+  p.hS16 = reinterpret_cast<uint16_t*>(w + L.hS16);
+  p.HQ = reinterpret_cast<float2*>(w + L.HQ);
   p.part_r = reinterpret_cast<float*>(w + L.part_r);
   p.part_s = reinterpret_cast<float*>(w + L.part_s);
   p.xstride = x_stride(p.d);
   p.xlstride = xl_stride(p.d);
-  p.kc = DecConst{0x43004300u, 0xC300C300u, 0x46804680u, 0x43434343u};
+  p.kc = DecConst{0x43004300u, 0xC300C300u, 0x46804680u, 0x43434343u, 0x64646464u};
   p.wait = ffn_wait_budget(WAIT_LIMIT);
 
   const int sms = device_sm_count();
@@ -1371,8 +1409,8 @@ static cudaError_t launch_decode(const FfnArgs& a, cudaStream_t s) {
       fp.offsets = a.offsets;
       fp.hf = const_cast<uint16_t*>(p.hf);
       fp.hl = const_cast<uint16_t*>(p.hl);
-      fp.hS = const_cast<uint16_t*>(p.hS);
-      fp.HS16 = const_cast<float*>(p.HS16);
+      fp.hS16 = const_cast<uint16_t*>(p.hS16);
+      fp.HQ = const_cast<float2*>(p.HQ);
       fp.y_pairs = p.y_pairs;
       fp.y_shared = p.y_shared;
       fp.red_r = p.red_r;
