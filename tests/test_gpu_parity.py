@@ -479,6 +479,22 @@ def test_layer_one_expert_all_tokens(cuda_dev):
     assert_layer_close(out, of, oracle_layer(3, 0, shape, x))
 
 
+@pytest.mark.parametrize("scale_exp", [20, -20])
+def test_layer_decode_activation_scales(cuda_dev, scale_exp):
+    # activations scaled by a power of two (exact in BF16): the intermediate h then lies far
+    # outside FP16's range (~2^40 or ~2^-40), which the shared expert's down projection, fed h as
+    # FP16 scaled per 32-row block, has to absorb
+    shape = synth.TINY
+    layer = device_layer(SEED, 0, shape, 8, cuda_dev)
+    for T in (1, 5):
+        x = (synth.x_bf16(SEED, 0, 40 + T, T, shape.d).float() * 2.0 ** scale_exp).to(torch.bfloat16)
+        out, of, info = run_layer(layer, x.to(cuda_dev))
+        ref = oracle_layer(SEED, 0, shape, x)
+        assert np.array_equal(info["ids"].cpu().numpy(), ref["ids"])
+        assert_layer_close(out, of, ref)
+        assert int(layer.dev_err) == 0
+
+
 @pytest.mark.parametrize("E,k,T", [(64, 8, 8), (96, 12, 8), (80, 11, 6)])
 def test_layer_decode_many_pairs(cuda_dev, E, k, T):
     # decode batches with many (token, expert) pairs: up to 96 pairs over up to 96 active experts
