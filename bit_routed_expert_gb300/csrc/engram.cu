@@ -37,20 +37,21 @@ __device__ __forceinline__ void decode8(uint2 v, uint32_t sb, float (&val)[8]) {
   val[6] = __fmul_rn(f67.x, sc); val[7] = __fmul_rn(f67.y, sc);
 }
 
-// Eight E4M3 bytes (values 8l .. 8l+7 of lane l) times one scale, as four float pairs: each byte
-// pair becomes an f16 pair (exact: E4M3 is a subset of f16), each f16 a float (exact), and the
-// products are packed FP32 multiplies (exact, or +-inf / NaN, as the scalar ones).
-__device__ __forceinline__ void decode8p(uint2 v, float sc, float2 (&o)[4]) {
-  const float2 s2 = make_float2(sc, sc);
+// Eight E4M3 bytes (values 8l .. 8l+7 of lane l) as four float pairs, unscaled (exact).
+__device__ __forceinline__ void e4m3x8_f32(uint2 v, float2 (&o)[4]) {
   const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-    o[2 * i] = __fmul2_rn(__half22float2(__half2(lo)), s2);
-    o[2 * i + 1] = __fmul2_rn(__half22float2(__half2(hi)), s2);
+    o[2 * i] = __half22float2(__half2(lo));
+    o[2 * i + 1] = __half22float2(__half2(hi));
   }
 }
+
+// Scale bytes below this make value * 2^(e-127) exact and finite for every E4M3 value (|v| <=
+// 448 < 2^9, and no E4M3 bit falls below FP32's subnormal floor).
+constexpr uint32_t E8M0_NO_OVERFLOW = 246;
 
 // Eight heads (the configuration's H): one warp per (token, table); lanes 0..7 load the eight
 // row ids with one instruction and check them with one unsigned compare; every row's loads are
@@ -88,14 +89,38 @@ __global__ void __launch_bounds__(256) engram_gather8_kernel(EngramTables tabs, 
     v[h] = ok ? __ldg(reinterpret_cast<const uint2*>(row) + lane) : make_uint2(0u, 0u);
     sb[h] = ok ? __ldg(row + 256 + (lane >> 2)) : 127u;
   }
-  // the head sum in head order, two values per packed FP32 add (each half one IEEE add)
+  // the head sum in head order, two values per packed FP32 instruction.  The result is defined
+  // as acc + (value * scale) with the product rounded first.  While the product is exact and
+  // finite (scale byte below E8M0_NO_OVERFLOW) a fused multiply-add rounds the same sum once, so
+  // a packed FMA does each step; a larger scale may overflow the product, which must then be
+  // infinite before the add, so it is formed by scalar multiplies (the compiler fuses a packed
+  // multiply into a following packed add, but never a scalar __fmul_rn).
   float2 acc[4];
+  uint32_t sb_max = 0;
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    float2 val[4];
-    decode8p(v[h], sc_tab[sb[h]], val);
+  for (int h = 0; h < 8; ++h) sb_max = max(sb_max, sb[h]);
+  if (sb_max < E8M0_NO_OVERFLOW) {   // the lane's eight heads (the common case)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = (h == 0) ? val[i] : __fadd2_rn(acc[i], val[i]);
+    for (int h = 0; h < 8; ++h) {
+      const float sc = sc_tab[sb[h]];
+      const float2 s2 = make_float2(sc, sc);
+      float2 raw[4];
+      e4m3x8_f32(v[h], raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = (h == 0) ? __fmul2_rn(raw[i], s2) : __ffma2_rn(raw[i], s2, acc[i]);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float sc = sc_tab[sb[h]];
+      float2 raw[4];
+      e4m3x8_f32(v[h], raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 pr = make_float2(__fmul_rn(raw[i].x, sc), __fmul_rn(raw[i].y, sc));
+        acc[i] = (h == 0) ? pr : __fadd2_rn(acc[i], pr);
+      }
+    }
   }
   uint4 o;
   o.x = f32_to_bf16_rne(acc[0].x) | (f32_to_bf16_rne(acc[0].y) << 16);

@@ -139,6 +139,17 @@ def test_engram_exhaustive_codes_and_scales(cuda_dev):
     assert np.array_equal(bf16_bits(got), ref)
 
 
+def test_engram_eight_heads_all_pairs(cuda_dev):
+    # the 8-head kernel: token t sums rows (t + 37 h) mod 256 of the all-pairs table over heads
+    # h = 0..7, so every (code, scale) pair, NaN, infinite and subnormal scales included, enters
+    # the head sum at every head position
+    tab = _all_pairs_table()
+    ids = ((np.arange(256)[:, None] + 37 * np.arange(8)[None, :]) % 256).astype(np.int64).reshape(256, 1, 8)
+    ref, err = oracle.engram_gather([tab], ids)
+    got = api.engram_gather_decode([torch.from_numpy(tab).to(cuda_dev)], torch.from_numpy(ids).to(cuda_dev))
+    assert np.array_equal(bf16_bits(got), ref)
+
+
 def test_engram_tiny_config(cuda_dev):
     tab = synth.engram_table(SEED, synth.stream(synth.S_ENGRAM_TABLE), 1024)
     ids = synth.engram_ids_uniform(SEED, 64, 1024).view(64, 1, 1)
