@@ -493,11 +493,11 @@ def test_layer_one_expert_all_tokens(cuda_dev):
 @pytest.mark.parametrize("scale_exp", [20, -20])
 def test_layer_decode_activation_scales(cuda_dev, scale_exp):
     # activations scaled by a power of two (exact in BF16): the intermediate h then lies far
-    # outside FP16's range (~2^40 or ~2^-40), which the shared expert's down projection, fed h as
-    # FP16 scaled per 32-row block, has to absorb
+    # outside FP16's range (~2^40 or ~2^-40), which the decode path's shared down projection, fed
+    # h as FP16 scaled per 32-row block, has to absorb; the grouped-GEMM path is run on the same
     shape = synth.TINY
-    layer = device_layer(SEED, 0, shape, 8, cuda_dev)
-    for T in (1, 5):
+    layer = device_layer(SEED, 0, shape, 64, cuda_dev)
+    for T in (1, 5, 64):   # 64: the grouped-GEMM path, whose intermediate stays BF16
         x = (synth.x_bf16(SEED, 0, 40 + T, T, shape.d).float() * 2.0 ** scale_exp).to(torch.bfloat16)
         out, of, info = run_layer(layer, x.to(cuda_dev))
         ref = oracle_layer(SEED, 0, shape, x)
