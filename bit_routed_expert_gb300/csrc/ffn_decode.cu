@@ -20,7 +20,8 @@
 // One 256-weight block of a row contributes d * P - dmin * M with P = sum sc q x and
 // M = sum_j m_j X_j, X_j the 16-value sub-block sums of the activations (three BF16 limbs, a
 // second small MMA whose A fragments are the 4-bit mins).  A Q8_0 weight d*q is split into
-// nibbles: q + 128 = 16*hi + lo, each held as 128 + nibble.  Products are exact; accumulation
+// nibbles in phase 1 (q + 128 = 16*hi + lo, each held as BF16 128 + nibble) and held as FP16
+// 1024 + (q + 128) in phase 2, against h as block-scaled FP16.  Products are exact; accumulation
 // is FP32.
 //
 // K order: the MMA sums over k, so the k order inside a block is free as long as A and B
