@@ -539,7 +539,8 @@ def run_engram(args, ws, rank, local, tables=None):
                        "algorithmic_bytes": alg, "l2": "flushed before every timed call"},
             "roofline": {"bound": "hbm", "kernel": "engram_gather_kernel", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                         "traffic": None, "peak_source": pk["source"]},
+                         "traffic": measured_traffic("engram_gather_T8192", "engram.cu"),
+                         "peak_source": pk["source"]},
             "us_mean": round(avg * 1e3, 2), "us_median": round(med * 1e3, 2), "us_spread": spread_us(ms),
             "back_to_back": {"calls_per_graph": BATCH, "replays": n_rep, "us_per_call": round(per_call_b * 1e3, 2),
                              "gbs": round(gbs_b, 1), "frac": round(gbs_b / pk["hbm_gbs"], 4),
